@@ -1,0 +1,358 @@
+"""Oracle: fp64 CPU statement of what the overlay library computes.
+
+TEST INFRASTRUCTURE ONLY (see the package docstring): the library's product
+path never reaches this module, and this module never reaches the library.
+
+Sources (cited by page title and section):
+
+* [OVR]  "We propose a content-addressed overlay system ..." report
+  (mikekappel.com/reports/runtime/we-propose-a-content-addressed-overlay-system/)
+* [DTD]  "Deep Technical Design: Exact, Atomic, Reversible Specialist Overlays on
+  Quantized Transformer Bases"
+  (mikekappel.com/reports/runtime/quantized-adapter-runtime-architecture/)
+* [MODELD] contenox modeld blueprint "LoRA adapters"
+  (contenox.com/docs/development/blueprints/modeld/lora-adapters/)
+
+Function -> pin (tests/test_oracle_pins.py):
+
+* f16_to_float            exhaustive vs numpy's binary16 decoder (all 65536 patterns)
+* dequantize_q8_0/q4_0    exhaustive (every finite scale x every code) vs exact
+                          products; exact rationals on a sample; hand-built nibbles
+* dual_path / merged_path exact-rational brute force on tiny shapes; dual == merged
+                          identity; zero-B and unit outer-product closed forms
+* effective_weight        closed forms (zero-B, e_i e_j^T), order invariance in
+                          exact arithmetic
+* error_bound             hand-evaluated 2x2 example
+* segmented               reduces to dual_path per token (brute force)
+* tree_digest             single-leaf closed form SHA256(SHA256(data)); FIPS 180
+                          test vectors for the primitive
+* composition_id          invariants (order, scale bits, base-only) + golden file
+* SwitchModel             invariants + golden transcript of the switch sequence
+No function here is "parity unpinned".
+"""
+from __future__ import annotations
+
+import hashlib
+import struct
+from dataclasses import dataclass, field
+
+import numpy as np
+
+QK = 32
+Q8_0 = 1
+Q4_0 = 2
+MODE_STACK = 1
+MODE_TABLE = 2
+LEAF = 65536
+
+# status codes of the library's boundary, restated from its specification
+OVL_OK = 0
+OVL_E_ARG = -1
+OVL_E_HASH = -2
+OVL_E_SHAPE = -3
+OVL_E_QUANT = -4
+OVL_E_OOM = -5
+OVL_E_NONFINITE = -6
+OVL_E_DUPLICATE = -7
+OVL_E_NOTARGET = -8
+OVL_E_BUSY = -9
+OVL_E_NO_PREVIOUS = -10
+OVL_E_STATE = -11
+
+RUNTIME_TAG = b"ovl-gb300 v1\0\0\0\0"   # 16 bytes: runtime version in the identity
+
+
+# --------------------------------------------------------------------------
+# Block dequantization.
+# [DTD] §5 "Quantized-Base Numerical Analysis": a q8_0 block is 32 weights and
+# one f16 scale; the benchmark's q4_0 block is 32 4-bit codes and an f16 scale
+# with value d*(code-8).  [OVR] §"Immutable base": full-precision values are
+# only materialized transiently.
+# --------------------------------------------------------------------------
+def f16_to_float(bits) -> np.ndarray:
+    """IEEE 754 binary16 -> float64, from the format's definition.
+
+    sign s, 5-bit exponent e (bias 15), 10-bit fraction f:
+      e = 0          -> (-1)^s * f * 2^-24            (zero / subnormal)
+      0 < e < 31     -> (-1)^s * (1024 + f) * 2^(e-25) (normal)
+      e = 31         -> +-inf (f = 0) or NaN
+    """
+    b = np.asarray(bits, dtype=np.uint16).astype(np.int64)
+    s = np.where((b >> 15) & 1, -1.0, 1.0)
+    e = (b >> 10) & 0x1F
+    f = (b & 0x3FF).astype(np.float64)
+    mag = np.where(e == 0, np.ldexp(f, -24), np.ldexp(1024.0 + f, (e - 25).astype(np.int64)))
+    mag = np.where(e == 31, np.where(f == 0, np.inf, np.nan), mag)
+    return s * mag
+
+
+def dequantize_q8_0(qs: np.ndarray, d_bits: np.ndarray) -> np.ndarray:
+    """w[i][j] = d[i][j/32] * q[i][j], q int8, in float64 (exact)."""
+    qs = np.asarray(qs).view(np.int8)
+    m, n = qs.shape
+    d = f16_to_float(d_bits).reshape(m, n // QK)
+    return np.repeat(d, QK, axis=1) * qs.astype(np.float64)
+
+
+def q4_0_codes(packed: np.ndarray) -> np.ndarray:
+    """Unpack nibbles: element 2p <- low nibble of byte p, 2p+1 <- high nibble."""
+    packed = np.asarray(packed, dtype=np.uint8)
+    m, half = packed.shape
+    codes = np.empty((m, 2 * half), dtype=np.int64)
+    codes[:, 0::2] = packed & 0x0F
+    codes[:, 1::2] = packed >> 4
+    return codes
+
+
+def dequantize_q4_0(packed: np.ndarray, d_bits: np.ndarray) -> np.ndarray:
+    """w[i][j] = d[i][j/32] * (code[i][j] - 8), in float64 (exact)."""
+    codes = q4_0_codes(packed)
+    m, n = codes.shape
+    d = f16_to_float(d_bits).reshape(m, n // QK)
+    return np.repeat(d, QK, axis=1) * (codes - 8).astype(np.float64)
+
+
+def dequantize(quant: int, qs, d_bits) -> np.ndarray:
+    if quant == Q8_0:
+        return dequantize_q8_0(qs, d_bits)
+    if quant == Q4_0:
+        return dequantize_q4_0(qs, d_bits)
+    raise ValueError("unknown quant profile")
+
+
+# --------------------------------------------------------------------------
+# Effective weights and the two evaluation paths.
+# [OVR] §"Explicit Correctness and Atomicity Invariants" (Compositional
+# Integrity): W' = W + sum_i dW_i in load order.  [OVR] §"Quantized-Base
+# Numerical Analysis": fresh-base oracle Y = W + sum_i dW_i from one dequant.
+# [OVR] §"Annotated Primary-Source Bibliography" (LoRA): dW = (alpha/r) B A;
+# the scale s folds alpha/r and any merge weight.
+# [OVR] §"Native/WASM Kernel Implications": direct low-rank addition
+# y = xW + x(BA) (two small matmuls) vs pre-merged W' = W + BA.
+# --------------------------------------------------------------------------
+def effective_weight(deq: np.ndarray, adapters) -> np.ndarray:
+    """W' = deq + sum_k s_k * B_k A_k, adapters [(A [r][n], B [m][r], s)] in order."""
+    W = np.array(deq, dtype=np.float64, copy=True)
+    for A, B, s in adapters:
+        W += float(s) * (np.asarray(B, np.float64) @ np.asarray(A, np.float64))
+    return W
+
+
+def dual_path(deq: np.ndarray, adapters, x: np.ndarray) -> np.ndarray:
+    """y[t] = deq x[t] + sum_k s_k B_k (A_k x[t]); x [T][n] -> y [T][m], float64."""
+    x = np.asarray(x, dtype=np.float64)
+    y = x @ np.asarray(deq, np.float64).T
+    for A, B, s in adapters:
+        v = x @ np.asarray(A, np.float64).T            # [T][r]   shrink
+        y = y + float(s) * (v @ np.asarray(B, np.float64).T)   # [T][m] expand
+    return y
+
+
+def merged_path(W_eff: np.ndarray, x: np.ndarray) -> np.ndarray:
+    """y[t] = W' x[t] (the per-layer materialized path), float64."""
+    return np.asarray(x, np.float64) @ np.asarray(W_eff, np.float64).T
+
+
+def error_bound(W_eff: np.ndarray, x: np.ndarray, rel: float = 2e-3, abs_: float = 1e-5) -> np.ndarray:
+    """Per-output tolerance rel * sum_j |W'_ij x_j| + abs_  ([T][m])."""
+    return rel * (np.abs(np.asarray(x, np.float64)) @ np.abs(np.asarray(W_eff, np.float64)).T) + abs_
+
+
+def materialize_bound(deq: np.ndarray, adapters, ulps: float = 4.0) -> np.ndarray:
+    """Element bound for an fp32 materialization of W' = deq + sum s B A.
+
+    Each term of the sum is formed and added in fp32; the bound is
+    ulps * 2^-24 * (rank+2) * (|deq| + sum_k |s_k| |B_k| |A_k|).
+    """
+    mag = np.abs(np.asarray(deq, np.float64)).copy()
+    terms = 2
+    for A, B, s in adapters:
+        mag += abs(float(s)) * (np.abs(np.asarray(B, np.float64)) @ np.abs(np.asarray(A, np.float64)))
+        terms += np.asarray(A).shape[0] + 1
+    return ulps * 2.0 ** -24 * terms * mag
+
+
+def segmented(deq: np.ndarray, table, x: np.ndarray, slot_of_token) -> np.ndarray:
+    """Multi-adapter batch ([DTD] §1, SGMV): token t uses table[slot_of_token[t]].
+
+    y[t] = deq x[t] + s B (A x[t]) with (A, B, s) = table[slot]; slot < 0 means
+    base only.  Output rows in the original request order.
+    """
+    x = np.asarray(x, np.float64)
+    y = np.empty((x.shape[0], deq.shape[0]), dtype=np.float64)
+    for t in range(x.shape[0]):
+        sl = int(slot_of_token[t])
+        ads = [table[sl]] if sl >= 0 else []
+        y[t] = dual_path(deq, ads, x[t:t + 1])[0]
+    return y
+
+
+# --------------------------------------------------------------------------
+# Content digests and composition identity.
+# [OVR] §"Composition Identity and Manifest Schema": identity = base hash,
+# layout + quantization profile, ordered adapter list with hashes and merge
+# coefficients, runtime version.  [DTD] §3 (same tuple, formula lost in the
+# export).  [MODELD] §"Runtime Identity and Cache Safety": adapter list in
+# deterministic order, each digest and scale.  [OVR] §"Checksum Verification":
+# SHA-256 of every artifact.
+# --------------------------------------------------------------------------
+def tree_digest(buf, leaf: int = LEAF) -> bytes:
+    """SHA-256 over the concatenation of SHA-256(leaf_i), leaves of `leaf` bytes."""
+    mv = memoryview(np.ascontiguousarray(np.frombuffer(bytes(buf), dtype=np.uint8)
+                                         if isinstance(buf, (bytes, bytearray)) else buf
+                                         ).view(np.uint8)).cast("B")
+    leaves = [hashlib.sha256(mv[i:i + leaf]).digest() for i in range(0, len(mv), leaf)]
+    return hashlib.sha256(b"".join(leaves)).digest()
+
+
+def base_key(digest: bytes, quant: int, tensors) -> bytes:
+    """tensors: iterable of (layer, proj, d_out, d_in, qs_off, d_off)."""
+    tensors = list(tensors)
+    h = hashlib.sha256()
+    h.update(b"OVLB")
+    h.update(digest)
+    h.update(struct.pack("<II", quant, len(tensors)))
+    for (layer, proj, d_out, d_in, qs_off, d_off) in tensors:
+        h.update(struct.pack("<IIIIQQ", layer, proj, d_out, d_in, qs_off, d_off))
+    return h.digest()
+
+
+def adapter_key(digest: bytes, targets) -> bytes:
+    """targets: iterable of (tensor_index, rank, a_off, b_off)."""
+    targets = list(targets)
+    h = hashlib.sha256()
+    h.update(b"OVLA")
+    h.update(digest)
+    h.update(struct.pack("<I", len(targets)))
+    for (ti, r, ao, bo) in targets:
+        h.update(struct.pack("<IIQQ", ti, r, ao, bo))
+    return h.digest()
+
+
+def f32_bits(s: float) -> int:
+    return struct.unpack("<I", struct.pack("<f", float(s)))[0]
+
+
+def composition_id(bkey: bytes, mode: int, entries) -> bytes:
+    """entries: ordered [(adapter_key, scale)]; empty = base only (mode STACK)."""
+    entries = list(entries)
+    h = hashlib.sha256()
+    h.update(b"OVLC")
+    h.update(RUNTIME_TAG)
+    h.update(bkey)
+    h.update(struct.pack("<II", mode if entries else MODE_STACK, len(entries)))
+    for akey, s in entries:
+        h.update(akey)
+        h.update(struct.pack("<I", f32_bits(s)))
+    return h.digest()
+
+
+# --------------------------------------------------------------------------
+# Activation state machine.
+# [OVR] §"Proposed Activation/Deactivation State Machine": validate -> stage ->
+# atomic swap; on error the pointer is unchanged; the old state may be kept for
+# rollback; deactivation = activating the base-only manifest.
+# [OVR] §"Explicit Correctness and Atomicity Invariants": idempotency (repeated
+# activation of the same composition does nothing); concurrent safety (reject
+# the switch while generation runs).  [DTD] §6: VALIDATION, ALLOCATION,
+# STAGING, CHECKSUM, COMMIT/SWAP, ROLLBACK.
+# --------------------------------------------------------------------------
+@dataclass
+class SwitchModel:
+    """Pure-Python model of the observable switch state.
+
+    Rollback is one level deep: it restores the composition that was active
+    before the last successful swap and clears the rollback slot.
+    """
+    base_key: bytes
+    staged: dict = field(default_factory=dict)      # handle -> adapter_key
+    active: tuple = ()                              # ((handle, scale), ...)
+    mode: int = MODE_STACK
+    prev: object = None                             # (entries, mode) or None
+    epoch: int = 0
+    next_handle: int = 1
+
+    def _id(self, entries, mode):
+        return composition_id(self.base_key, mode, [(self.staged[h], s) for h, s in entries])
+
+    def current_id(self):
+        return self._id(self.active, self.mode)
+
+    def stage(self, akey: bytes, ok: bool = True, err: int = OVL_E_HASH):
+        if not ok:
+            return err, None
+        h = self.next_handle
+        self.next_handle += 1
+        self.staged[h] = akey
+        return OVL_OK, h
+
+    def activate(self, handles, scales, mode=MODE_STACK):
+        handles = list(handles)
+        if any(h not in self.staged for h in handles):
+            return OVL_E_ARG, self.current_id()
+        if len(set(handles)) != len(handles):
+            return OVL_E_DUPLICATE, self.current_id()
+        if any(not np.isfinite(s) for s in scales):
+            return OVL_E_ARG, self.current_id()
+        entries = tuple(zip(handles, [float(np.float32(s)) for s in scales]))
+        mode = mode if entries else MODE_STACK
+        new_id = self._id(entries, mode)
+        if new_id == self.current_id():
+            return OVL_OK, new_id                    # idempotent no-op
+        self.prev = (self.active, self.mode)
+        self.active, self.mode = entries, mode
+        self.epoch += 1
+        return OVL_OK, new_id
+
+    def rollback(self):
+        if self.prev is None:
+            return OVL_E_NO_PREVIOUS, self.current_id()
+        self.active, self.mode = self.prev
+        self.prev = None
+        self.epoch += 1
+        return OVL_OK, self.current_id()
+
+    def unstage(self, h):
+        if h not in self.staged:
+            return OVL_E_ARG
+        in_use = any(hh == h for hh, _ in self.active)
+        if self.prev is not None:
+            in_use = in_use or any(hh == h for hh, _ in self.prev[0])
+        if in_use:
+            return OVL_E_STATE
+        del self.staged[h]
+        return OVL_OK
+
+
+def switch_sequence(n_ops: int = 100, n_adapters: int = 4, corrupt: int = 3):
+    """The timed switch workload: op i even -> activate adapter (i/2) mod 4
+    (the corrupt one is re-staged instead and must fail its hash check);
+    op i odd -> rollback.  Returns [(op, adapter_or_None)]."""
+    ops = []
+    for i in range(n_ops):
+        if i % 2 == 0:
+            a = (i // 2) % n_adapters
+            ops.append(("stage_corrupt", a) if a == corrupt else ("activate", a))
+        else:
+            ops.append(("rollback", None))
+    return ops
+
+
+def switch_transcript(bkey: bytes, adapter_keys, scale: float = 2.0, n_ops: int = 100, corrupt: int = 3):
+    """Expected (status, composition id hex) of every op of switch_sequence()."""
+    m = SwitchModel(bkey)
+    handles = {}
+    for a, k in enumerate(adapter_keys):
+        st, h = m.stage(k, ok=(a != corrupt))
+        handles[a] = h
+    out = []
+    for op, a in switch_sequence(n_ops, len(adapter_keys), corrupt):
+        if op == "activate":
+            st, cid = m.activate([handles[a]], [scale])
+        elif op == "stage_corrupt":
+            st, _ = m.stage(adapter_keys[a], ok=False)
+            cid = m.current_id()
+        else:
+            st, cid = m.rollback()
+        out.append((op, a, st, cid.hex()))
+    return out

@@ -1,0 +1,317 @@
+"""Seeded synthetic inputs for the dual-path overlay library and its oracle.
+
+This module only *produces inputs*: Gaussian base weights quantized into the
+q8_0 / q4_0 byte layout, fp32 LoRA factors, activations, adapter-id draws and
+the byte buffers that carry them.  It holds none of the method's arithmetic
+(no dequantization, no GEMV, no LoRA application): both the CUDA library and
+the CPU oracle consume the bytes produced here, each with its own code.
+
+Workload shapes follow the configurations of the benchmark: a Llama-style
+decoder block at 8B shape (hidden 4096, GQA k/v 1024, MLP 14336), base
+weights ~ N(0, 0.02), LoRA factors ~ N(0, 0.01), activations ~ N(0, 1).
+
+Byte layout (the library's written format; see the header ``include/ovl.h``):
+
+* base buffer: per tensor a ``qs`` plane and a ``d`` plane, each starting on a
+  256-byte boundary.  q8_0: ``qs`` is int8 ``[d_out][d_in]`` row-major.
+  q4_0: ``qs`` is uint8 ``[d_out][d_in/2]``; byte ``p`` of a row holds element
+  ``2p`` in bits 0-3 and element ``2p+1`` in bits 4-7, codes 0..15.
+  ``d`` is IEEE binary16 ``[d_out][d_in/32]`` (one scale per 32-block).
+* adapter payload: per target an fp32 ``A [r][d_in]`` and fp32 ``B [d_out][r]``,
+  each starting on a 256-byte boundary.
+"""
+from __future__ import annotations
+
+import hashlib
+from dataclasses import dataclass, field
+
+import numpy as np
+
+QK = 32                      # weights per quantization block
+ALIGN = 256                  # plane / factor alignment inside a buffer
+LEAF = 65536                 # leaf size of the content digest (bytes)
+
+Q8_0 = 1
+Q4_0 = 2
+
+PROJ = ("q", "k", "v", "o", "gate", "up", "down")
+# (d_out, d_in) of the seven projections of one decoder block at 8B shape
+SHAPES_8B = {
+    "q": (4096, 4096),
+    "k": (1024, 4096),
+    "v": (1024, 4096),
+    "o": (4096, 4096),
+    "gate": (14336, 4096),
+    "up": (14336, 4096),
+    "down": (4096, 14336),
+}
+
+
+def _align(n: int, a: int = ALIGN) -> int:
+    return (n + a - 1) // a * a
+
+
+# --------------------------------------------------------------------------
+# seeds
+# --------------------------------------------------------------------------
+def base_seed(layer: int, proj: int) -> int:
+    return 10_000 + 8 * layer + proj
+
+
+def adapter_seed(adapter: int, layer: int, proj: int) -> int:
+    return 1_000_000 + 10_000 * adapter + 8 * layer + proj
+
+
+def x_seed(T: int, d_in: int) -> int:
+    return 2000 + 16 * T + (0 if d_in == 4096 else 1)
+
+
+ZIPF_SEED = 3000
+
+
+def gaussian(rng: np.random.Generator, shape, sigma: float) -> np.ndarray:
+    """N(0, sigma^2) drawn in float32, row-major (sigma is a standard deviation)."""
+    return rng.standard_normal(shape, dtype=np.float32) * np.float32(sigma)
+
+
+def round_half_away(v: np.ndarray) -> np.ndarray:
+    return np.sign(v) * np.floor(np.abs(v) + np.float32(0.5))
+
+
+# --------------------------------------------------------------------------
+# quantizers (input generation only: the library never quantizes)
+# --------------------------------------------------------------------------
+def quantize_q8_0(w: np.ndarray):
+    """float32 [m][n] -> (qs int8 [m][n], d uint16 bits [m][n/32]).
+
+    d = fp16(max|w_block| / 127) (fp32 division, round-to-nearest-even into
+    binary16); q = clamp(round_half_away(w / d), -127, 127); an all-zero block
+    gets d = 0, q = 0.
+    """
+    w = np.ascontiguousarray(w, dtype=np.float32)
+    m, n = w.shape
+    assert n % QK == 0
+    blk = w.reshape(m, n // QK, QK)
+    amax = np.abs(blk).max(axis=2)
+    d16 = (amax / np.float32(127.0)).astype(np.float16)
+    d32 = d16.astype(np.float32)[..., None]
+    with np.errstate(divide="ignore", invalid="ignore"):
+        q = np.where(d32 > 0, round_half_away(blk / d32), np.float32(0))
+    q = np.clip(q, -127, 127).astype(np.int8).reshape(m, n)
+    return q, d16.view(np.uint16)
+
+
+def quantize_q4_0(w: np.ndarray):
+    """float32 [m][n] -> (qs uint8 [m][n/2] packed nibbles, d uint16 bits).
+
+    d = fp16(max|w_block| / 8); code = clamp(round_half_away(w / d) + 8, 0, 15),
+    value d * (code - 8); element 2p in the low nibble of byte p.
+    """
+    w = np.ascontiguousarray(w, dtype=np.float32)
+    m, n = w.shape
+    assert n % QK == 0
+    blk = w.reshape(m, n // QK, QK)
+    amax = np.abs(blk).max(axis=2)
+    d16 = (amax / np.float32(8.0)).astype(np.float16)
+    d32 = d16.astype(np.float32)[..., None]
+    with np.errstate(divide="ignore", invalid="ignore"):
+        q = np.where(d32 > 0, round_half_away(blk / d32), np.float32(0))
+    code = np.clip(q + 8, 0, 15).astype(np.uint8).reshape(m, n)
+    packed = (code[:, 0::2] | (code[:, 1::2] << 4)).astype(np.uint8)
+    return packed, d16.view(np.uint16)
+
+
+def to_bf16_bits(x: np.ndarray) -> np.ndarray:
+    """float32 -> bfloat16 bit patterns (uint16), round-to-nearest-even."""
+    u = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32).astype(np.uint64)
+    rounded = (u + 0x7FFF + ((u >> 16) & 1)) >> 16
+    return rounded.astype(np.uint16)
+
+
+def bf16_bits_to_f32(b: np.ndarray) -> np.ndarray:
+    return (b.astype(np.uint32) << 16).view(np.float32)
+
+
+# --------------------------------------------------------------------------
+# buffers
+# --------------------------------------------------------------------------
+@dataclass
+class TensorDesc:
+    layer: int
+    proj: int
+    d_out: int
+    d_in: int
+    qs_off: int
+    d_off: int
+
+
+@dataclass
+class Base:
+    quant: int
+    tensors: list
+    buf: np.ndarray            # uint8, the whole base
+    # per-tensor views (host) for convenience of tests: (qs, d_bits)
+    planes: list = field(default_factory=list)
+
+
+def qs_bytes(quant: int, d_out: int, d_in: int) -> int:
+    return d_out * d_in if quant == Q8_0 else d_out * d_in // 2
+
+
+def d_bytes(d_out: int, d_in: int) -> int:
+    return d_out * (d_in // QK) * 2
+
+
+def build_base(quant: int, items) -> Base:
+    """items: iterable of (layer, proj, w_float32[d_out][d_in]) -> Base."""
+    qz = quantize_q8_0 if quant == Q8_0 else quantize_q4_0
+    enc = []
+    off = 0
+    descs = []
+    for layer, proj, w in items:
+        qs, d = qz(w)
+        d_out, d_in = w.shape
+        qs_off = off
+        off = _align(off + qs.nbytes)
+        d_off = off
+        off = _align(off + d.nbytes)
+        descs.append(TensorDesc(layer, proj, d_out, d_in, qs_off, d_off))
+        enc.append((qs, d))
+    buf = np.zeros(max(off, ALIGN), dtype=np.uint8)
+    for t, (qs, d) in zip(descs, enc):
+        buf[t.qs_off:t.qs_off + qs.nbytes] = qs.reshape(-1).view(np.uint8)
+        buf[t.d_off:t.d_off + d.nbytes] = d.reshape(-1).view(np.uint8)
+    b = Base(quant, descs, buf)
+    b.planes = [base_planes(b, i) for i in range(len(descs))]
+    return b
+
+
+def base_planes(base: Base, i: int):
+    """(qs, d_bits) numpy views of tensor i inside the base buffer."""
+    t = base.tensors[i]
+    nq = qs_bytes(base.quant, t.d_out, t.d_in)
+    qs = base.buf[t.qs_off:t.qs_off + nq]
+    if base.quant == Q8_0:
+        qs = qs.view(np.int8).reshape(t.d_out, t.d_in)
+    else:
+        qs = qs.reshape(t.d_out, t.d_in // 2)
+    d = base.buf[t.d_off:t.d_off + d_bytes(t.d_out, t.d_in)].view(np.uint16)
+    return qs, d.reshape(t.d_out, t.d_in // QK)
+
+
+@dataclass
+class Adapter:
+    targets: list              # tensor indices into the base
+    ranks: list
+    a_off: list
+    b_off: list
+    payload: np.ndarray        # uint8
+    factors: list              # [(A fp32 [r][d_in], B fp32 [d_out][r])]
+    required_base: bytes = b"\0" * 32
+
+
+def build_adapter(base: Base, targets, ranks, factors, required_base=None) -> Adapter:
+    """Pack fp32 factors [(A, B)] for the given target tensors into one payload."""
+    off = 0
+    a_off, b_off = [], []
+    for (A, B) in factors:
+        a_off.append(off)
+        off = _align(off + A.nbytes)
+        b_off.append(off)
+        off = _align(off + B.nbytes)
+    payload = np.zeros(max(off, ALIGN), dtype=np.uint8)
+    for (A, B), ao, bo in zip(factors, a_off, b_off):
+        payload[ao:ao + A.nbytes] = np.ascontiguousarray(A, np.float32).reshape(-1).view(np.uint8)
+        payload[bo:bo + B.nbytes] = np.ascontiguousarray(B, np.float32).reshape(-1).view(np.uint8)
+    return Adapter(list(targets), list(ranks), a_off, b_off, payload,
+                   [(np.ascontiguousarray(A, np.float32), np.ascontiguousarray(B, np.float32))
+                    for A, B in factors],
+                   required_base if required_base is not None else b"\0" * 32)
+
+
+def content_digest(buf: np.ndarray) -> bytes:
+    """Declared digest of a byte buffer: SHA-256 over the concatenated SHA-256
+    digests of consecutive 64 KiB leaves (last leaf may be short).  This is the
+    value a caller declares when it hands bytes to the library."""
+    mv = memoryview(np.ascontiguousarray(buf).view(np.uint8)).cast("B")
+    top = hashlib.sha256()
+    for i in range(0, len(mv), LEAF):
+        top.update(hashlib.sha256(mv[i:i + LEAF]).digest())
+    return top.digest()
+
+
+# --------------------------------------------------------------------------
+# workloads
+# --------------------------------------------------------------------------
+def single_layer_256(seed_a: int = 0, seed_b: int = 1, quant: int = Q8_0):
+    """256x256 layer, rank-8 adapters A (rng seed 0) and B (rng seed 1), s = 2.0.
+
+    rng(0) draws W, then adapter A's A-factor, then its B-factor, then x (fp32);
+    adapter B's factors come from rng(1).
+    """
+    rng = np.random.default_rng(seed_a)
+    W = gaussian(rng, (256, 256), 0.02)
+    A1 = gaussian(rng, (8, 256), 0.01)
+    B1 = gaussian(rng, (256, 8), 0.01)
+    x = gaussian(rng, (1, 256), 1.0)
+    rng2 = np.random.default_rng(seed_b)
+    A2 = gaussian(rng2, (8, 256), 0.01)
+    B2 = gaussian(rng2, (256, 8), 0.01)
+    base = build_base(quant, [(0, 0, W)])
+    ad_a = build_adapter(base, [0], [8], [(A1, B1)])
+    ad_b = build_adapter(base, [0], [8], [(A2, B2)])
+    return base, ad_a, ad_b, x, 2.0
+
+
+def block_base(quant: int, layers=(0,), shapes=SHAPES_8B, projs=PROJ) -> Base:
+    items = []
+    for layer in layers:
+        for p in projs:
+            pi = PROJ.index(p)
+            d_out, d_in = shapes[p]
+            rng = np.random.default_rng(base_seed(layer, pi))
+            items.append((layer, pi, gaussian(rng, (d_out, d_in), 0.02)))
+    return build_base(quant, items)
+
+
+def block_adapter(base: Base, adapter: int, rank: int, which=None) -> Adapter:
+    """Rank-`rank` LoRA on every tensor of `base` (or on the indices `which`)."""
+    idx = list(range(len(base.tensors))) if which is None else list(which)
+    factors = []
+    for i in idx:
+        t = base.tensors[i]
+        rng = np.random.default_rng(adapter_seed(adapter, t.layer, t.proj))
+        A = gaussian(rng, (rank, t.d_in), 0.01)
+        B = gaussian(rng, (t.d_out, rank), 0.01)
+        factors.append((A, B))
+    return build_adapter(base, idx, [rank] * len(idx), factors)
+
+
+def activations(T: int, d_in: int, seed=None) -> np.ndarray:
+    """x ~ N(0,1) float32 [T][d_in]."""
+    rng = np.random.default_rng(x_seed(T, d_in) if seed is None else seed)
+    return gaussian(rng, (T, d_in), 1.0)
+
+
+def zipf_ids(n_requests: int = 64, n_adapters: int = 16, a: float = 1.1, seed: int = ZIPF_SEED):
+    """Finite Zipf draw of adapter ids: p_k proportional to k^-a, k = 1..n, id = k-1."""
+    k = np.arange(1, n_adapters + 1, dtype=np.float64)
+    p = k ** (-a)
+    p /= p.sum()
+    rng = np.random.default_rng(seed)
+    return rng.choice(n_adapters, size=n_requests, p=p).astype(np.int32)
+
+
+def segments(ids: np.ndarray):
+    """Group requests by adapter id (stable, ascending id).
+
+    Returns (perm, seg_offsets, seg_slot): perm[j] = original request index of
+    the j-th grouped row; segment s covers grouped rows seg_offsets[s] ..
+    seg_offsets[s+1]-1 and uses table slot seg_slot[s].
+    """
+    ids = np.asarray(ids, dtype=np.int32)
+    perm = np.argsort(ids, kind="stable").astype(np.int32)
+    sorted_ids = ids[perm]
+    slots, starts = np.unique(sorted_ids, return_index=True)
+    offsets = np.append(starts, len(ids)).astype(np.int32)
+    return perm, offsets, slots.astype(np.int32)
