@@ -1,0 +1,295 @@
+/*
+ * ovl.h — C ABI of the dual-path quantized-base + LoRA overlay library (libovl).
+ *
+ * The library evaluates the linear layers of a transformer whose base weights
+ * are an immutable block-quantized buffer, with an ordered stack of low-rank
+ * adapters applied as overlays that are never merged into the base:
+ *
+ *     y = deq(W_q) x + sum_k s_k B_k (A_k x)                        (dual path)
+ *     S = deq(W_q) + sum_k s_k B_k A_k ;  y = S x   (per-layer JIT, S discarded)
+ *
+ * Sources, cited by page title and section:
+ *   [OVR]    "We propose a content-addressed overlay system ..." report
+ *            (mikekappel.com/reports/runtime/we-propose-a-content-addressed-overlay-system/)
+ *   [DTD]    "Deep Technical Design: Exact, Atomic, Reversible Specialist Overlays on
+ *            Quantized Transformer Bases"
+ *            (mikekappel.com/reports/runtime/quantized-adapter-runtime-architecture/)
+ *   [MODELD] contenox modeld blueprint "LoRA adapters"
+ *            (contenox.com/docs/development/blueprints/modeld/lora-adapters/)
+ *
+ * Conventions for every entry point
+ *   - Returns ovl_status: 0 = OVL_OK, negative = error.  Nothing throws, aborts or
+ *     exits.  On error the library state is exactly what it was before the call
+ *     (strong guarantee; [OVR] §"Explicit Correctness and Atomicity Invariants",
+ *     Atomic Update) and ovl_last_error() describes the failure.  Errors are
+ *     deterministic for a given input ([OVR] §"Checksum Verification").
+ *   - "device pointer" = a CUDA global-memory address on the context's device,
+ *     owned by the caller and valid for the duration stated.  "host pointer" =
+ *     ordinary process memory.  Streams are cudaStream_t passed as void*
+ *     (NULL = the legacy default stream).  The library never calls cudaMalloc or
+ *     cudaFree: every byte of device memory it uses comes from the caller's
+ *     arena (ovl_create) or the caller's argument buffers.
+ *   - Work enqueued on a stream is asynchronous; a device-side failure (a bounded
+ *     wait that ran out) is latched in a status word that ovl_check_device() reads.
+ *   - Calls on one context are serialized by an internal mutex; forward calls
+ *     must be issued on one stream (or otherwise stream-ordered) because they
+ *     share the context's device workspace.
+ *
+ * Byte layouts (written format shared by every producer and consumer of the bytes)
+ *   Base buffer (device, caller-owned, never written by the library):
+ *     per tensor a qs plane at qs_off and a d plane at d_off (both multiples of 16).
+ *       q8_0: qs = int8 [d_out][d_in] row-major; weight = d * q.
+ *       q4_0: qs = uint8 [d_out][d_in/2]; byte p of a row holds element 2p in bits 0-3
+ *             and element 2p+1 in bits 4-7; codes 0..15; weight = d * (code - 8).
+ *       d   = IEEE binary16, little-endian, [d_out][d_in/32], one scale per 32 weights.
+ *     ([DTD] §5 "Quantized-Base Numerical Analysis": 32-weight blocks, one f16 scale.)
+ *     The d plane, rounded up to a multiple of 16 bytes, must lie inside the buffer.
+ *     d_in must be a multiple of 32.
+ *   Adapter payload (host, copied into the arena by ovl_stage_adapter):
+ *     per target tensor t: A_t = float32 [rank][d_in] at a_off, B_t = float32
+ *     [d_out][rank] at b_off, offsets multiples of 16 ([OVR] §"Memory, Byte, and
+ *     Latency Formulas": LoRA stores A (r x n) and B (m x r)).
+ *   Activations x: row-major [T][d_in] float32 or bfloat16.  Outputs y: float32 [T][d_out].
+ *
+ * Content digest (the "declared digest" arguments)
+ *   SHA-256 (FIPS 180-4) over the concatenation of the SHA-256 digests of
+ *   consecutive 65536-byte leaves of the bytes (the last leaf may be shorter;
+ *   zero bytes -> SHA-256 of the empty string).  ([OVR] §"Checksum Verification";
+ *   [DTD] §6 CHECKSUM VERIFICATION.)
+ *
+ * Composition identity (32 bytes, little-endian fields)
+ *   base_key    = SHA256("OVLB" | base_digest | u32 quant | u32 n_tensors |
+ *                        per tensor u32 layer,proj,d_out,d_in | u64 qs_off,d_off)
+ *   adapter_key = SHA256("OVLA" | payload_digest | u32 n_targets |
+ *                        per target u32 tensor,rank | u64 a_off,b_off)
+ *   id          = SHA256("OVLC" | runtime_tag[16] | base_key | u32 mode | u32 K |
+ *                        per entry adapter_key | u32 bits_of_float(scale))
+ *   runtime_tag = "ovl-gb300 v1" padded with zero bytes to 16; an empty stack has
+ *   mode OVL_MODE_STACK.  ([OVR] §"Composition Identity and Manifest Schema";
+ *   [DTD] §3; [MODELD] §"Runtime Identity and Cache Safety".)
+ */
+#ifndef OVL_H
+#define OVL_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct ovl_ctx ovl_ctx;
+typedef int32_t ovl_status;
+typedef uint64_t ovl_adapter_h;   /* 0 is never a valid handle */
+
+enum {
+  OVL_OK = 0,
+  OVL_E_ARG = -1,            /* bad argument / unknown handle / non-finite scale */
+  OVL_E_HASH = -2,           /* declared digest does not match the bytes */
+  OVL_E_SHAPE = -3,          /* dims, offsets, alignment or sizes inconsistent */
+  OVL_E_QUANT = -4,          /* unknown or mismatched quantization profile */
+  OVL_E_OOM = -5,            /* arena budget exceeded (all-or-nothing) */
+  OVL_E_NONFINITE = -6,      /* NaN/Inf in an adapter payload */
+  OVL_E_DUPLICATE = -7,      /* duplicate handle / duplicate target */
+  OVL_E_NOTARGET = -8,       /* adapter targets a tensor the base does not have */
+  OVL_E_BUSY = -9,           /* switch requested while forward work is in flight */
+  OVL_E_NO_PREVIOUS = -10,   /* rollback with no previous composition */
+  OVL_E_STATE = -11,         /* operation not valid in the current state */
+  OVL_E_CUDA = -12,          /* a CUDA runtime call failed */
+  OVL_E_DEVICE_TIMEOUT = -13 /* a bounded device-side wait ran out */
+};
+
+enum { OVL_Q8_0 = 1, OVL_Q4_0 = 2 };                 /* quantization profile */
+enum { OVL_F32 = 1, OVL_BF16 = 2 };                  /* activation dtype */
+enum { OVL_MODE_STACK = 1, OVL_MODE_TABLE = 2 };     /* composition mode */
+enum { OVL_PATH_DUAL = 1, OVL_PATH_JIT = 2 };        /* evaluation path */
+enum { OVL_SWITCH_REJECT = 1, OVL_SWITCH_DRAIN = 2 };/* switch vs in-flight forward */
+enum {                                                /* activation phases ([DTD] §6) */
+  OVL_PHASE_VALIDATION = 1, OVL_PHASE_ALLOCATION = 2, OVL_PHASE_STAGING = 3,
+  OVL_PHASE_CHECKSUM = 4, OVL_PHASE_SWAP = 5
+};
+
+enum {
+  OVL_MAX_STACK = 8,          /* adapters in one STACK composition */
+  OVL_MAX_TABLE = 32,         /* slots in one TABLE composition */
+  OVL_MAX_RANK = 128,         /* rank of one adapter target */
+  OVL_MAX_TOTAL_RANK = 256,   /* sum of ranks on one tensor in a STACK */
+  OVL_MAX_T = 512,            /* tokens per forward call */
+  OVL_MAX_SEGMENTS = 64       /* segments per segmented call */
+};
+
+typedef struct {
+  uint32_t layer, proj;       /* informational; part of the identity */
+  uint32_t d_out, d_in;       /* rows (outputs) and columns (inputs) */
+  uint64_t qs_off, d_off;     /* byte offsets of the two planes in the base buffer */
+} ovl_tensor_desc;
+
+typedef struct {
+  uint32_t quant;             /* OVL_Q8_0 or OVL_Q4_0 */
+  uint32_t n_tensors;
+  const ovl_tensor_desc* tensors;   /* host array of n_tensors, copied */
+} ovl_base_desc;
+
+typedef struct {
+  uint32_t n_targets;
+  const uint32_t* target_tensor;    /* host arrays of n_targets, copied */
+  const uint32_t* rank;
+  const uint64_t* a_off;
+  const uint64_t* b_off;
+  uint8_t required_base_digest[32]; /* all-zero = no requirement, else must equal the
+                                       base's content digest ([DTD] §11 AdapterManifestV0) */
+} ovl_adapter_desc;
+
+typedef struct {
+  uint8_t composition_id[32];
+  uint8_t base_digest[32];
+  uint32_t quant, mode, n_entries, has_previous;
+  uint64_t epoch;             /* number of successful swaps since ovl_load_base */
+  uint64_t arena_used, arena_bytes;
+  uint32_t n_staged, base_loaded;
+} ovl_state;
+
+typedef struct {
+  ovl_adapter_h handle;
+  uint8_t adapter_key[32];
+  float scale;
+  uint32_t total_rank;        /* sum of ranks over the adapter's targets */
+} ovl_entry;
+
+/* Create a context on CUDA device `device` over a caller-owned device arena of
+ * arena_bytes bytes (>= 16 MiB, 256-byte aligned).  The arena holds the device
+ * status word, the forward workspace, staged adapters and digest scratch; it must
+ * outlive the context.  switch_policy: OVL_SWITCH_REJECT (a switch while forward
+ * work is in flight fails with OVL_E_BUSY) or OVL_SWITCH_DRAIN (waits for it)
+ * ([OVR] §"Explicit Correctness and Atomicity Invariants", Concurrent Safety).
+ * *out receives the context; on error *out is NULL. */
+ovl_status ovl_create(ovl_ctx** out, int device, void* arena_dev, size_t arena_bytes,
+                      uint32_t switch_policy);
+
+/* Destroy the context after synchronizing its internal stream.  Frees host
+ * state only; the arena and the base remain the caller's.  NULL is a no-op. */
+ovl_status ovl_destroy(ovl_ctx* ctx);
+
+/* Register the immutable base ([OVR] §"Immutable base"; [DTD] §2 Oracle
+ * Invariant).  base_dev: device pointer to nbytes bytes laid out as described
+ * above, read-only to the library, valid until ovl_destroy.  digest: the declared
+ * content digest; the library computes the digest of the device bytes (device
+ * leaf hashing on `stream`, then synchronizes) and fails with OVL_E_HASH on
+ * mismatch.  Descriptor errors: OVL_E_QUANT, OVL_E_SHAPE.  Once per context
+ * (OVL_E_STATE otherwise).  The base-only composition becomes active. */
+ovl_status ovl_load_base(ovl_ctx* ctx, const ovl_base_desc* desc, const void* base_dev,
+                         size_t nbytes, const uint8_t digest[32], void* stream);
+
+/* Stage an adapter ([OVR] §"Proposed Activation/Deactivation State Machine";
+ * [DTD] §6 VALIDATION -> ALLOCATION -> STAGING -> CHECKSUM).  payload_host: host
+ * pointer to nbytes bytes (A/B factors at the descriptor's offsets), read during
+ * the call only.  Validation: targets exist (OVL_E_NOTARGET), no duplicate target
+ * (OVL_E_DUPLICATE), 1 <= rank <= OVL_MAX_RANK, offsets aligned and in range
+ * (OVL_E_SHAPE), required base digest (OVL_E_HASH), digest of the host bytes
+ * equals `digest` (OVL_E_HASH).  Allocation from the arena, all-or-nothing
+ * (OVL_E_OOM).  Staging: host->device copy on the library's internal stream.
+ * Checksum: the digest of the device copy must equal the host digest
+ * (OVL_E_HASH) and every factor value must be finite (OVL_E_NONFINITE).  Any
+ * failure frees the allocation and changes nothing.  *out receives the handle. */
+ovl_status ovl_stage_adapter(ovl_ctx* ctx, const ovl_adapter_desc* desc, const void* payload_host,
+                             size_t nbytes, const uint8_t digest[32], ovl_adapter_h* out);
+
+/* Release a staged adapter's arena block.  OVL_E_STATE if it is part of the
+ * active or the rollback composition; OVL_E_BUSY (REJECT policy) if forward work
+ * that read it is still in flight; OVL_E_ARG for an unknown handle. */
+ovl_status ovl_unstage_adapter(ovl_ctx* ctx, ovl_adapter_h h);
+
+/* Atomically make (h[0], scale[0]) ... (h[n-1], scale[n-1]) the active
+ * composition ([OVR] §"Proposed Activation/Deactivation State Machine",
+ * Activation Point; [DTD] §6 COMMIT/SWAP).  mode OVL_MODE_STACK: every entry is
+ * applied to every token, in order.  mode OVL_MODE_TABLE: entries are slots that
+ * ovl_segmented_forward selects per segment.  n = 0 activates the base-only
+ * composition (deactivation, [OVR] same section, Deactivation).  Re-activating
+ * the active composition is a no-op that returns its id ([OVR] Idempotency).
+ * The replaced composition becomes the rollback target.  Errors: OVL_E_ARG
+ * (unknown handle, non-finite scale, bad mode, n over the limit), OVL_E_DUPLICATE,
+ * OVL_E_SHAPE (total rank on a tensor over OVL_MAX_TOTAL_RANK), OVL_E_BUSY.
+ * composition_id_out (host, 32 bytes, may be NULL) receives the active id. */
+ovl_status ovl_activate(ovl_ctx* ctx, const ovl_adapter_h* h, const float* scale, uint32_t n,
+                        uint32_t mode, uint8_t composition_id_out[32]);
+
+/* Restore the composition that was active before the last successful swap and
+ * clear the rollback slot (one level deep; [OVR] §"Proposed Activation/
+ * Deactivation State Machine", Commit or Rollback).  OVL_E_NO_PREVIOUS if there
+ * is none; OVL_E_BUSY as for ovl_activate. */
+ovl_status ovl_rollback(ovl_ctx* ctx, uint8_t composition_id_out[32]);
+
+/* y = layer `tensor` of the active composition applied to x.
+ * x: device pointer [T][d_in] (x_dtype OVL_F32 or OVL_BF16); y: device pointer
+ * float32 [T][d_out]; both valid until the work on `stream` completes.
+ * path OVL_PATH_DUAL: fused dequant + low-rank kernel, y = deq(W) x + sum s B (A x)
+ *   with fp32 accumulation ([OVR] §"Native/WASM Kernel Implications", Direct
+ *   Low-Rank Addition; [DTD] §8 Prefill vs Decode).  scratch unused (may be NULL).
+ * path OVL_PATH_JIT: materializes S = deq(W) + sum s B A into `scratch` (device,
+ *   float32, >= d_out*d_in*4 bytes), then y = x S^T on the tensor cores (TF32
+ *   operands, fp32 accumulation); the scratch may be reused by the next layer
+ *   ([DTD] §1 Per-Layer JIT CoW Materialization; §5 Fresh-Base Oracle Definition).
+ * STACK compositions only (OVL_E_STATE for TABLE).  T = 0 is a no-op.  Errors:
+ * OVL_E_ARG (tensor index, dtype, path, T > OVL_MAX_T, null pointers, scratch too
+ * small), OVL_E_STATE (no base), OVL_E_CUDA (launch failure). */
+ovl_status ovl_linear_forward(ovl_ctx* ctx, uint32_t tensor, const void* x, uint32_t x_dtype,
+                              uint32_t T, float* y, uint32_t path, float* scratch,
+                              size_t scratch_bytes, void* stream);
+
+/* Materialize S = deq(W) + sum_k s_k B_k A_k (STACK composition, float32
+ * [d_out][d_in] row-major) into the caller's device scratch without requantizing
+ * ([DTD] §5 Fresh-Base Oracle Definition; §7 Scratch Overhead).  With an empty
+ * stack S is the exact dequantized tensor. */
+ovl_status ovl_materialize_layer(ovl_ctx* ctx, uint32_t tensor, float* scratch,
+                                 size_t scratch_bytes, void* stream);
+
+/* Multi-adapter batch over one base tensor (TABLE composition; [DTD] §1 SGMV).
+ * x: device [T][d_in]; y: device float32 [T][d_out], rows in request order.
+ * perm, seg_offsets, seg_slot: HOST arrays, copied into the launch:
+ *   perm[j] (j < T) = request row of the j-th grouped row (a permutation of 0..T-1);
+ *   segment s (s < n_seg) covers grouped rows seg_offsets[s] .. seg_offsets[s+1]-1
+ *   (seg_offsets has n_seg+1 nondecreasing entries, first 0, last T) and uses
+ *   table slot seg_slot[s] (-1 = base only).
+ * y[perm[j]] = deq(W) x[perm[j]] + s_slot B_slot (A_slot x[perm[j]]).
+ * Errors: OVL_E_STATE (not TABLE), OVL_E_ARG (bad segments or slots). */
+ovl_status ovl_segmented_forward(ovl_ctx* ctx, uint32_t tensor, const void* x, uint32_t x_dtype,
+                                 uint32_t T, const int32_t* seg_offsets, const int32_t* seg_slot,
+                                 uint32_t n_seg, const int32_t* perm, float* y, void* stream);
+
+/* Recompute the content digest of the base's device bytes now (device leaf
+ * hashing on `stream`, synchronizes).  Used to check that the base stays
+ * bit-identical across switches ([DTD] §2 Oracle Invariant). */
+ovl_status ovl_base_digest(ovl_ctx* ctx, uint8_t digest_out[32], void* stream);
+
+/* Snapshot of the observable state. */
+ovl_status ovl_get_state(ovl_ctx* ctx, ovl_state* out);
+
+/* Entry i (< n_entries) of the active composition, in order. */
+ovl_status ovl_get_entry(ovl_ctx* ctx, uint32_t i, ovl_entry* out);
+
+/* Synchronize `stream`, read and clear the device status word.  Returns OVL_OK,
+ * OVL_E_DEVICE_TIMEOUT (a bounded device wait ran out; outputs of that launch are
+ * invalid) or OVL_E_CUDA. */
+ovl_status ovl_check_device(ovl_ctx* ctx, void* stream);
+
+/* Fault injection for tests ([OVR] §"TDD and Fault-Injection Matrix"): the next
+ * stage/activate/rollback that reaches `phase` fails there with `code` (< 0),
+ * with the same cleanup as a real failure.  code 0 clears a pending injection. */
+ovl_status ovl_debug_inject(ovl_ctx* ctx, uint32_t phase, ovl_status code);
+
+/* Message of the last failed call on ctx (static storage owned by ctx; "" after
+ * success).  ctx NULL returns the message of the last failed ovl_create. */
+const char* ovl_last_error(ovl_ctx* ctx);
+
+/* Host utilities (no device needed): FIPS 180-4 SHA-256 of n bytes, and the
+ * content digest defined above, both computed by the library's own code. */
+ovl_status ovl_sha256(const void* data, size_t n, uint8_t out[32]);
+ovl_status ovl_content_digest(const void* data, size_t n, uint8_t out[32]);
+
+/* Library version string (static). */
+const char* ovl_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* OVL_H */

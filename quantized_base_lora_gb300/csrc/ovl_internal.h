@@ -1,0 +1,84 @@
+// Internal declarations of libovl: launch arguments of the kernels and the
+// launcher functions the host state machine calls.  Not part of the C ABI.
+#pragma once
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "../../include/ovl.h"
+
+namespace ovl {
+
+constexpr int kQK = 32;                 // weights per quantization block
+constexpr size_t kLeaf = 65536;         // content-digest leaf size
+
+// Device status word codes (latched by kernels, read by ovl_check_device).
+enum : uint32_t {
+  kDevOk = 0,
+  kDevTimeoutFull = 1,      // consumer gave up waiting for a staged tile
+  kDevTimeoutEmpty = 2,     // producer gave up waiting for a free stage
+  kDevTimeoutShrink = 3,    // epilogue gave up waiting for the low-rank partials
+};
+
+// One low-rank term as the kernels see it: A [r][d_in], B [d_out][r] (fp32,
+// device), applied with scale s.
+struct LoraRef {
+  const float* A;
+  const float* B;
+  uint32_t r;
+  float s;
+};
+
+// Device workspace carved from the arena at context creation.
+struct Workspace {
+  uint32_t* status;               // one status word
+  unsigned long long* counter;    // [0]: arrivals, [1]: departures (self-resetting)
+  float* partial;                 // low-rank partial sums
+  size_t partial_floats;
+};
+
+// Fused dual-path forward of one tensor over a token chunk (T <= 8).
+struct DualArgs {
+  const uint8_t* qs;      // qs plane
+  const uint8_t* dpl;     // d plane (binary16)
+  uint32_t m, n, quant;
+  const void* x;          // [T][n], fp32 or bf16
+  uint32_t xdt, T;
+  float* y;               // [T][m]
+  uint32_t nl;            // number of low-rank terms
+  uint32_t rtot;          // sum of ranks
+  LoraRef lora[OVL_MAX_STACK];
+  Workspace ws;
+};
+
+// Materialize S = deq(W) + sum_k s_k B_k A_k into fp32 scratch [m][n].
+struct MatArgs {
+  const uint8_t* qs;
+  const uint8_t* dpl;
+  uint32_t m, n, quant;
+  uint32_t nl;
+  LoraRef lora[OVL_MAX_STACK];
+  float* S;
+};
+
+cudaError_t launch_dualpath(const DualArgs& a, cudaStream_t st);
+cudaError_t launch_materialize(const MatArgs& a, cudaStream_t st);
+// Y[T][m] = X[T][n] * S[m][n]^T with TF32 tensor-core operands, fp32 accumulate.
+cudaError_t launch_jit_gemm(const float* S, const void* x, uint32_t xdt, uint32_t T, uint32_t m,
+                            uint32_t n, float* y, float* xf32_scratch, const Workspace& ws,
+                            cudaStream_t st);
+size_t jit_gemm_x_scratch_bytes(uint32_t T, uint32_t n);
+
+// Content digest helpers: SHA-256 of each 64 KiB leaf of a device buffer into
+// `leaf_digests` (device, 32 bytes per leaf).
+cudaError_t launch_leaf_digests(const uint8_t* data, size_t n, uint8_t* leaf_digests,
+                                cudaStream_t st);
+// Scan `n` fp32 values at `p`; increments *flag (device) if any is NaN/Inf.
+cudaError_t launch_finite_scan(const float* p, size_t n, uint32_t* flag, cudaStream_t st);
+
+// Host-side digests (library's own SHA-256).
+void host_sha256(const void* data, size_t n, uint8_t out[32]);
+void host_content_digest(const void* data, size_t n, uint8_t out[32]);
+void host_digest_of_leaves(const uint8_t* leaf_digests, size_t n_leaves, uint8_t out[32]);
+
+}  // namespace ovl

@@ -1,0 +1,215 @@
+"""GPU parity of the fused dual-path kernel against the fp64 oracle, through the
+C ABI: the single 256x256 layer with its switch sequence, the 8B-shape q8_0
+block, the q4_0 block with two stacked adapters at T = 1, 4, 8, ragged and
+degenerate shapes."""
+import numpy as np
+import pytest
+
+import oracle as O
+import synth as S
+from gpu_common import (adapter_tuples, assert_within_bound, deq_of, lora_terms, make_runtime, require_gpu,
+                        stage, tensor_tuples, torch, x_device)
+
+pytestmark = pytest.mark.gpu
+
+
+def fwd(rt, i, xd):
+    y = rt.forward(i, xd)
+    torch.cuda.synchronize()
+    assert rt.check_device() == 0
+    return y.cpu().numpy()
+
+
+# ----------------------------------------------------------------- single layer
+@pytest.fixture(scope="module")
+def layer256():
+    require_gpu()
+    base, ad_a, ad_b, x, s = S.single_layer_256()
+    rt = make_runtime(base)
+    return base, ad_a, ad_b, x, s, rt
+
+
+def test_single_layer_switch_sequence(layer256):
+    import quantized_base_lora_gb300 as q
+    base, ad_a, ad_b, x, s, rt = layer256
+    xd, x64 = x_device(x, "f32")
+    deq = deq_of(base, 0)
+    d0 = rt.base_digest()[1]
+    ha, hb = stage(rt, ad_a), stage(rt, ad_b)
+    outs = {}
+    for name, handles, ads in (("base", [], []), ("A", [ha], [(ad_a, s)]), ("base2", [], []),
+                               ("B", [hb], [(ad_b, s)])):
+        st, cid = rt.activate(handles, [s] * len(handles))
+        assert st == 0, q.ovl_last_error(rt.ctx)
+        y = fwd(rt, 0, xd)
+        assert_within_bound(y, deq, lora_terms(ads, 0), x64, name)
+        outs[name] = y
+        assert rt.base_digest()[1] == d0                       # base bytes untouched
+    assert np.array_equal(outs["base"].view(np.uint32), outs["base2"].view(np.uint32))
+    # reversibility: base -> A -> base -> B is bitwise base -> B in a fresh context
+    rt2 = make_runtime(base)
+    hb2 = stage(rt2, ad_b)
+    st, cid2 = rt2.activate([hb2], [s])
+    y2 = fwd(rt2, 0, xd)
+    assert np.array_equal(outs["B"].view(np.uint32), y2.view(np.uint32))
+    assert rt.state()["composition_id"] == rt2.state()["composition_id"] == cid2
+    rt2.close()
+
+
+def test_single_layer_ids_match_oracle(layer256):
+    import json, os
+    base, ad_a, ad_b, x, s, rt = layer256
+    with open(os.path.join(os.path.dirname(__file__), "golden", "config1.json")) as f:
+        g = json.load(f)
+    rt3 = make_runtime(base)
+    assert rt3.state()["composition_id"].hex() == g["ids"]["base"]
+    ha = stage(rt3, ad_a)
+    assert rt3.activate([ha], [s])[1].hex() == g["ids"]["A"]
+    hb = stage(rt3, ad_b)
+    assert rt3.activate([hb], [s])[1].hex() == g["ids"]["B"]
+    assert rt3.state()["base_digest"].hex() == g["base_digest"]
+    rt3.close()
+
+
+def test_zero_B_adapter_gives_base_output_exactly(layer256):
+    base, ad_a, ad_b, x, s, rt = layer256
+    A, B = ad_a.factors[0]
+    zb = S.build_adapter(base, [0], [8], [(A, np.zeros_like(B))])
+    xd, _ = x_device(x, "f32")
+    rt.activate([], [])
+    y0 = fwd(rt, 0, xd)
+    hz = stage(rt, zb)
+    rt.activate([hz], [s])
+    y1 = fwd(rt, 0, xd)
+    assert np.array_equal(y0, y1)                                # fp32 ==
+    assert np.array_equal(y0.view(np.uint32), y1.view(np.uint32))  # and bits (no -0 expected)
+    rt.activate([], [])
+
+
+def test_forward_is_deterministic(layer256):
+    base, ad_a, ad_b, x, s, rt = layer256
+    xd, _ = x_device(x, "f32")
+    ha = stage(rt, ad_a)
+    rt.activate([ha], [s])
+    ys = [fwd(rt, 0, xd) for _ in range(5)]
+    for y in ys[1:]:
+        assert np.array_equal(ys[0].view(np.uint32), y.view(np.uint32))
+    rt.activate([], [])
+
+
+# ----------------------------------------------------------------- 8B-shape q8_0 block
+@pytest.fixture(scope="module")
+def block_q8():
+    require_gpu()
+    base = S.block_base(S.Q8_0)
+    ad = S.block_adapter(base, adapter=0, rank=16)
+    rt = make_runtime(base, arena_bytes=512 << 20)
+    h = stage(rt, ad)
+    st, _ = rt.activate([h], [2.0])
+    assert st == 0
+    return base, ad, rt
+
+
+@pytest.mark.parametrize("proj", list(range(7)))
+def test_block_q8_decode_bf16(block_q8, proj):
+    base, ad, rt = block_q8
+    t = base.tensors[proj]
+    x = S.activations(1, t.d_in)
+    xd, x64 = x_device(x, "bf16")
+    y = fwd(rt, proj, xd)
+    assert_within_bound(y, deq_of(base, proj), lora_terms([(ad, 2.0)], proj), x64, S.PROJ[proj])
+
+
+# ----------------------------------------------------------------- q4_0 block, stacked adapters
+@pytest.fixture(scope="module")
+def block_q4():
+    require_gpu()
+    base = S.block_base(S.Q4_0)
+    a16 = S.block_adapter(base, adapter=0, rank=16)
+    a64 = S.block_adapter(base, adapter=1, rank=64)
+    rt = make_runtime(base, arena_bytes=768 << 20)
+    h16, h64 = stage(rt, a16), stage(rt, a64)
+    st, _ = rt.activate([h16, h64], [1.0, 0.5])
+    assert st == 0
+    return base, a16, a64, rt
+
+
+@pytest.mark.parametrize("T", [1, 4, 8])
+@pytest.mark.parametrize("proj", [0, 1, 4, 6])
+def test_block_q4_stacked(block_q4, proj, T):
+    base, a16, a64, rt = block_q4
+    t = base.tensors[proj]
+    x = S.activations(T, t.d_in)
+    xd, x64 = x_device(x, "bf16")
+    y = fwd(rt, proj, xd)
+    assert_within_bound(y, deq_of(base, proj), lora_terms([(a16, 1.0), (a64, 0.5)], proj), x64,
+                        f"{S.PROJ[proj]} T={T}")
+
+
+# ----------------------------------------------------------------- ragged / degenerate shapes
+RAGGED = [  # (quant, d_out, d_in, T, ranks, xdtype)
+    (S.Q8_0, 1, 32, 1, (), "f32"),
+    (S.Q8_0, 3, 96, 2, (1,), "bf16"),
+    (S.Q4_0, 1000, 288, 3, (5, 7), "f32"),
+    (S.Q8_0, 1337, 1056, 5, (16,), "bf16"),
+    (S.Q4_0, 77, 4128, 1, (3,), "bf16"),
+    (S.Q8_0, 513, 8192, 8, (32, 2), "bf16"),
+    (S.Q4_0, 257, 2048, 16, (4,), "f32"),
+    (S.Q8_0, 4096, 256, 1, (128, 128), "f32"),
+]
+
+
+@pytest.mark.parametrize("case", RAGGED, ids=[f"q{c[0]}_{c[1]}x{c[2]}_T{c[3]}_r{'-'.join(map(str, c[4]))}_{c[5]}"
+                                             for c in RAGGED])
+def test_ragged_shapes(case):
+    require_gpu()
+    quant, m, n, T, ranks, xdt = case
+    rng = np.random.default_rng(m * 7 + n)
+    W = S.gaussian(rng, (m, n), 0.02)
+    base = S.build_base(quant, [(0, 0, W)])
+    ads = []
+    for k, r in enumerate(ranks):
+        A = S.gaussian(rng, (r, n), 0.01)
+        B = S.gaussian(rng, (m, r), 0.01)
+        ads.append((S.build_adapter(base, [0], [r], [(A, B)]), [2.0, 0.5, 1.25][k % 3]))
+    rt = make_runtime(base, arena_bytes=64 << 20)
+    hs = [stage(rt, ad) for ad, _ in ads]
+    assert rt.activate(hs, [s for _, s in ads])[0] == 0
+    x = S.gaussian(rng, (T, n), 1.0)
+    xd, x64 = x_device(x, xdt)
+    y = fwd(rt, 0, xd)
+    assert y.shape == (T, m)
+    assert_within_bound(y, deq_of(base, 0), lora_terms(ads, 0), x64, str(case))
+    rt.close()
+
+
+def test_empty_token_batch_is_a_noop():
+    require_gpu()
+    import quantized_base_lora_gb300 as q
+    base, ad_a, ad_b, x, s = S.single_layer_256()
+    rt = make_runtime(base)
+    y = torch.full((1, 256), 7.0, device="cuda")
+    xd = torch.zeros((1, 256), device="cuda")
+    st = q.ovl_linear_forward(rt.ctx, 0, xd.data_ptr(), q.OVL_F32, 0, y.data_ptr())
+    torch.cuda.synchronize()
+    assert st == 0 and bool((y == 7.0).all())
+    rt.close()
+
+
+def test_activation_scale_extremes_stay_within_bound():
+    """Blocks whose activations span a wide dynamic range and all-zero blocks."""
+    require_gpu()
+    rng = np.random.default_rng(99)
+    m, n = 64, 512
+    W = S.gaussian(rng, (m, n), 0.02)
+    base = S.build_base(S.Q8_0, [(0, 0, W)])
+    rt = make_runtime(base)
+    x = S.gaussian(rng, (4, n), 1.0)
+    x[0, :32] = 0.0                                   # zero block
+    x[1, 32:64] *= np.float32(1e-30)                  # tiny block
+    x[2, 64:96] *= np.float32(1e20)                   # huge block
+    x[3, ::7] *= np.float32(1e-6)                     # mixed magnitudes inside blocks
+    xd, x64 = x_device(x, "f32")
+    y = fwd(rt, 0, xd)
+    assert_within_bound(y, deq_of(base, 0), [], x64, "extremes")
+    rt.close()
