@@ -42,12 +42,26 @@ namespace ovl {
 namespace {
 
 constexpr int kRecBytes = 112;  // per (token, block) activation record: 7 x 16 B
-constexpr int kMaxNS = 4;
+#ifndef OVL_K1_MAX_NS
+#define OVL_K1_MAX_NS 8
+#endif
+#ifndef OVL_K1_SOFT_KB
+#define OVL_K1_SOFT_KB 112
+#endif
+#ifndef OVL_K1_STAGE_BYTES
+#define OVL_K1_STAGE_BYTES 16384
+#endif
+#ifndef OVL_K1_MAX_GROUPS
+#define OVL_K1_MAX_GROUPS 4
+#endif
+constexpr int kMaxNS = OVL_K1_MAX_NS;
+constexpr int kMaxThreads = 9 * 32;    // up to 8 consumer warps + 1 producer warp
 constexpr uint32_t kRecBudget = 128 * 1024;
 constexpr uint32_t kSmemBudget = 220 * 1024;
 
 struct DualCfg {
-  uint32_t nwc;          // consumer warps
+  uint32_t nwc;          // column warps per consumer group
+  uint32_t ng;           // consumer groups (each consumes every ng-th stage)
   uint32_t bpl;          // column blocks per consumer lane
   uint32_t ns;           // pipeline depth
   uint32_t rowbytes;     // qs bytes per row
@@ -57,6 +71,9 @@ struct DualCfg {
   uint32_t rows_max;     // rows of the largest CTA slice
   uint32_t gs;           // CTAs that reduce a shrink chunk
   uint32_t off_rec, off_stage, off_red, off_v, off_tmp;
+  uint32_t off_x, off_a, off_b;  // staged activations, shrink chunk, B rows
+  uint32_t stage_x;              // 0: x read from global; 4 or 16: cp.async granule
+  uint32_t stage_a, stage_b;     // 1: operand staged in shared memory
   uint32_t smem;
 };
 
@@ -71,44 +88,99 @@ __device__ __forceinline__ float load_x(const void* x, uint32_t xdt, size_t i) {
   return static_cast<const float*>(x)[i];
 }
 
-// Activation record of one 32-block: limbs h|m|l (32 bytes each, in the order the
-// weight words are consumed), then {2^-s as f32 bits, start_h, start_m, start_l}.
+// Activation records.  Record (t, b) describes the 32-block b of token t as
+// an exact integer vector X with x_j = X_j * 2^-s (|X_j| <= 2^22), split in
+// three signed byte limbs X = 65536 h + 256 m + l with m, l in [-128, 127]
+// (balanced base-256 digits, so every dot product is a signed x signed dp4a):
+// words 0-7 = h, 8-15 = m, 16-23 = l, then {2^-s as f32 bits, start_h,
+// start_m, start_l}.  Limb word k
+// holds the four elements that weight word k consumes: elements 4k..4k+3 for
+// q8_0; for q4_0 word 2g carries the low nibbles (elements 8g, 8g+2, 8g+4, 8g+6)
+// and word 2g+1 the high nibbles (8g+1, ...).  The q4_0 starts are -8 * sum of
+// the limbs, which folds the code offset into the integer accumulators.
+//
+// One warp builds four records at a time: lane k = lane & 7 of each 8-lane
+// group produces limb word k of its block.
 template <bool Q4>
-__device__ __forceinline__ void prep_record(uint8_t* rec, const void* x, uint32_t xdt, size_t idx,
-                                            uint32_t lane) {
-  const float v = load_x(x, xdt, idx);
-  const uint32_t mx = __reduce_max_sync(0xffffffffu, __float_as_uint(fabsf(v)));
-  int X = 0;
-  float xs = 0.f;
-  if (mx != 0u) {
-    const int E = ilogbf(__uint_as_float(mx));
-    const int s = 21 - E;                 // |X| <= 2^22
-    X = __float2int_rn(ldexpf(v, s));
-    xs = ldexpf(1.0f, -s);
-  }
-  // q4_0 word i of a block carries elements 8i..8i+7 as nibbles: the low nibbles
-  // hold the even elements, the high nibbles the odd ones.
-  const uint32_t p = Q4 ? ((lane >> 3) * 8 + (lane & 1) * 4 + ((lane & 7) >> 1)) : lane;
-  const int h = X >> 16;
-  const int mm = (X >> 8) & 0xFF;
-  const int ll = X & 0xFF;
-  rec[p] = static_cast<uint8_t>(h & 0xFF);
-  rec[32 + p] = static_cast<uint8_t>(mm);
-  rec[64 + p] = static_cast<uint8_t>(ll);
-  uint32_t* meta = reinterpret_cast<uint32_t*>(rec + 96);
-  if (Q4) {
-    const int sh = __reduce_add_sync(0xffffffffu, h);
-    const int sm = __reduce_add_sync(0xffffffffu, mm);
-    const int sl = __reduce_add_sync(0xffffffffu, ll);
-    if (lane == 0) {
-      meta[1] = static_cast<uint32_t>(-8 * sh);
-      meta[2] = static_cast<uint32_t>(-8 * sm);
-      meta[3] = static_cast<uint32_t>(-8 * sl);
+__device__ __forceinline__ void prep_records(uint8_t* rec, const DualArgs& a, const void* xsrc, uint32_t nb,
+                                             uint32_t warp, uint32_t nwarps, uint32_t lane) {
+  const uint32_t k = lane & 7;
+  const uint32_t total = a.T * nb;
+  for (uint32_t base = warp * 4; base < total; base += nwarps * 4) {
+    const uint32_t ri = base + (lane >> 3);
+    const bool live = ri < total;
+    const uint32_t t = live ? ri / nb : 0, b = live ? ri - t * nb : 0;
+    float v[4];
+    const size_t row = static_cast<size_t>(t) * a.n + static_cast<size_t>(b) * 32;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const uint32_t e = Q4 ? (8 * (k >> 1) + (k & 1) + 2 * i) : (4 * k + i);
+      v[i] = live ? load_x(xsrc, a.xdt, row + e) : 0.f;
     }
-  } else if (lane == 0) {
-    meta[1] = meta[2] = meta[3] = 0u;
+    uint32_t mx = 0;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) mx = max(mx, __float_as_uint(v[i]) & 0x7FFFFFFFu);
+    mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+    mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+    mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+    int X[4] = {0, 0, 0, 0};
+    float xs = 0.f;
+    if (mx != 0u) {
+      const int E = mx >= 0x00800000u ? static_cast<int>(mx >> 23) - 127 : ilogbf(__uint_as_float(mx));
+      const int s = 21 - E;
+      if (s >= -126 && s <= 126) {
+        const float sc = __uint_as_float(static_cast<uint32_t>(s + 127) << 23);
+        xs = __uint_as_float(static_cast<uint32_t>(127 - s) << 23);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) X[i] = __float2int_rn(v[i] * sc);
+      } else {
+        xs = ldexpf(1.0f, -s);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) X[i] = __float2int_rn(ldexpf(v[i], s));
+      }
+    }
+    int H[4], M[4], Lw[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      Lw[i] = ((X[i] + 128) & 0xFF) - 128;
+      const int x1 = (X[i] - Lw[i]) >> 8;
+      M[i] = ((x1 + 128) & 0xFF) - 128;
+      H[i] = (x1 - M[i]) >> 8;
+    }
+    const uint32_t h01 = __byte_perm(static_cast<uint32_t>(H[0]), static_cast<uint32_t>(H[1]), 0x0040);
+    const uint32_t h23 = __byte_perm(static_cast<uint32_t>(H[2]), static_cast<uint32_t>(H[3]), 0x0040);
+    const uint32_t m01 = __byte_perm(static_cast<uint32_t>(M[0]), static_cast<uint32_t>(M[1]), 0x0040);
+    const uint32_t m23 = __byte_perm(static_cast<uint32_t>(M[2]), static_cast<uint32_t>(M[3]), 0x0040);
+    const uint32_t l01 = __byte_perm(static_cast<uint32_t>(Lw[0]), static_cast<uint32_t>(Lw[1]), 0x0040);
+    const uint32_t l23 = __byte_perm(static_cast<uint32_t>(Lw[2]), static_cast<uint32_t>(Lw[3]), 0x0040);
+    int sh = 0, sm = 0, sl = 0;
+    if (Q4) {
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        sh += H[i];
+        sm += M[i];
+        sl += Lw[i];
+      }
+#pragma unroll
+      for (int o = 1; o <= 4; o <<= 1) {
+        sh += __shfl_xor_sync(0xffffffffu, sh, o);
+        sm += __shfl_xor_sync(0xffffffffu, sm, o);
+        sl += __shfl_xor_sync(0xffffffffu, sl, o);
+      }
+    }
+    if (live) {
+      uint32_t* w = reinterpret_cast<uint32_t*>(rec + static_cast<size_t>(ri) * kRecBytes);
+      w[k] = __byte_perm(h01, h23, 0x5410);
+      w[8 + k] = __byte_perm(m01, m23, 0x5410);
+      w[16 + k] = __byte_perm(l01, l23, 0x5410);
+      if (k == 0) {
+        w[24] = __float_as_uint(xs);
+        w[25] = static_cast<uint32_t>(-8 * sh);
+        w[26] = static_cast<uint32_t>(-8 * sm);
+        w[27] = static_cast<uint32_t>(-8 * sl);
+      }
+    }
   }
-  if (lane == 0) meta[0] = __float_as_uint(xs);
 }
 
 __device__ __forceinline__ float limb_combine(int sh, int sm, int sl) {
@@ -123,39 +195,40 @@ __device__ __forceinline__ float dot_q8(const uint8_t* wp, const uint4 (&r)[7]) 
   sh = dp4a_ss(a.z, r[0].z, sh); sh = dp4a_ss(a.w, r[0].w, sh);
   sh = dp4a_ss(b.x, r[1].x, sh); sh = dp4a_ss(b.y, r[1].y, sh);
   sh = dp4a_ss(b.z, r[1].z, sh); sh = dp4a_ss(b.w, r[1].w, sh);
-  sm = dp4a_su(a.x, r[2].x, sm); sm = dp4a_su(a.y, r[2].y, sm);
-  sm = dp4a_su(a.z, r[2].z, sm); sm = dp4a_su(a.w, r[2].w, sm);
-  sm = dp4a_su(b.x, r[3].x, sm); sm = dp4a_su(b.y, r[3].y, sm);
-  sm = dp4a_su(b.z, r[3].z, sm); sm = dp4a_su(b.w, r[3].w, sm);
-  sl = dp4a_su(a.x, r[4].x, sl); sl = dp4a_su(a.y, r[4].y, sl);
-  sl = dp4a_su(a.z, r[4].z, sl); sl = dp4a_su(a.w, r[4].w, sl);
-  sl = dp4a_su(b.x, r[5].x, sl); sl = dp4a_su(b.y, r[5].y, sl);
-  sl = dp4a_su(b.z, r[5].z, sl); sl = dp4a_su(b.w, r[5].w, sl);
+  sm = dp4a_ss(a.x, r[2].x, sm); sm = dp4a_ss(a.y, r[2].y, sm);
+  sm = dp4a_ss(a.z, r[2].z, sm); sm = dp4a_ss(a.w, r[2].w, sm);
+  sm = dp4a_ss(b.x, r[3].x, sm); sm = dp4a_ss(b.y, r[3].y, sm);
+  sm = dp4a_ss(b.z, r[3].z, sm); sm = dp4a_ss(b.w, r[3].w, sm);
+  sl = dp4a_ss(a.x, r[4].x, sl); sl = dp4a_ss(a.y, r[4].y, sl);
+  sl = dp4a_ss(a.z, r[4].z, sl); sl = dp4a_ss(a.w, r[4].w, sl);
+  sl = dp4a_ss(b.x, r[5].x, sl); sl = dp4a_ss(b.y, r[5].y, sl);
+  sl = dp4a_ss(b.z, r[5].z, sl); sl = dp4a_ss(b.w, r[5].w, sl);
   return limb_combine(sh, sm, sl);
 }
 
+// q4_0 codes 0..15 are valid signed bytes, so the code words go straight into
+// signed dp4a; the -8 offset is in the accumulator starts of the record.
 __device__ __forceinline__ float dot_q4(const uint8_t* wp, const uint4 (&r)[7]) {
   const uint4 w = *reinterpret_cast<const uint4*>(wp);
   const uint32_t m4 = 0x0F0F0F0Fu;
-  const uint32_t l0 = w.x & m4, h0 = (w.x >> 4) & m4;
-  const uint32_t l1 = w.y & m4, h1 = (w.y >> 4) & m4;
-  const uint32_t l2 = w.z & m4, h2 = (w.z >> 4) & m4;
-  const uint32_t l3 = w.w & m4, h3 = (w.w >> 4) & m4;
-  int sh = static_cast<int>(r[6].y);
-  uint32_t sm = r[6].z, sl = r[6].w;
-  sh = dp4a_us(l0, r[0].x, sh); sh = dp4a_us(h0, r[0].y, sh);
-  sh = dp4a_us(l1, r[0].z, sh); sh = dp4a_us(h1, r[0].w, sh);
-  sh = dp4a_us(l2, r[1].x, sh); sh = dp4a_us(h2, r[1].y, sh);
-  sh = dp4a_us(l3, r[1].z, sh); sh = dp4a_us(h3, r[1].w, sh);
-  sm = dp4a_uu(l0, r[2].x, sm); sm = dp4a_uu(h0, r[2].y, sm);
-  sm = dp4a_uu(l1, r[2].z, sm); sm = dp4a_uu(h1, r[2].w, sm);
-  sm = dp4a_uu(l2, r[3].x, sm); sm = dp4a_uu(h2, r[3].y, sm);
-  sm = dp4a_uu(l3, r[3].z, sm); sm = dp4a_uu(h3, r[3].w, sm);
-  sl = dp4a_uu(l0, r[4].x, sl); sl = dp4a_uu(h0, r[4].y, sl);
-  sl = dp4a_uu(l1, r[4].z, sl); sl = dp4a_uu(h1, r[4].w, sl);
-  sl = dp4a_uu(l2, r[5].x, sl); sl = dp4a_uu(h2, r[5].y, sl);
-  sl = dp4a_uu(l3, r[5].z, sl); sl = dp4a_uu(h3, r[5].w, sl);
-  return limb_combine(sh, static_cast<int>(sm), static_cast<int>(sl));
+  const int l0 = w.x & m4, h0 = (w.x >> 4) & m4;
+  const int l1 = w.y & m4, h1 = (w.y >> 4) & m4;
+  const int l2 = w.z & m4, h2 = (w.z >> 4) & m4;
+  const int l3 = w.w & m4, h3 = (w.w >> 4) & m4;
+  int sh = static_cast<int>(r[6].y), sm = static_cast<int>(r[6].z), sl = static_cast<int>(r[6].w);
+  sh = dp4a_ss(l0, r[0].x, sh); sh = dp4a_ss(h0, r[0].y, sh);
+  sh = dp4a_ss(l1, r[0].z, sh); sh = dp4a_ss(h1, r[0].w, sh);
+  sh = dp4a_ss(l2, r[1].x, sh); sh = dp4a_ss(h2, r[1].y, sh);
+  sh = dp4a_ss(l3, r[1].z, sh); sh = dp4a_ss(h3, r[1].w, sh);
+  sm = dp4a_ss(l0, r[2].x, sm); sm = dp4a_ss(h0, r[2].y, sm);
+  sm = dp4a_ss(l1, r[2].z, sm); sm = dp4a_ss(h1, r[2].w, sm);
+  sm = dp4a_ss(l2, r[3].x, sm); sm = dp4a_ss(h2, r[3].y, sm);
+  sm = dp4a_ss(l3, r[3].z, sm); sm = dp4a_ss(h3, r[3].w, sm);
+  sl = dp4a_ss(l0, r[4].x, sl); sl = dp4a_ss(h0, r[4].y, sl);
+  sl = dp4a_ss(l1, r[4].z, sl); sl = dp4a_ss(h1, r[4].w, sl);
+  sl = dp4a_ss(l2, r[5].x, sl); sl = dp4a_ss(h2, r[5].y, sl);
+  sl = dp4a_ss(l3, r[5].z, sl); sl = dp4a_ss(h3, r[5].w, sl);
+  return limb_combine(sh, sm, sl);
 }
 
 // Sum over the 32 lanes of v[lane >> (5 - log2 N)] for all N values at once
@@ -190,31 +263,47 @@ __device__ __forceinline__ float warp_sum(float v) {
   return v;
 }
 
+// Global address of element f of the flattened [rtot][n] factor space.
+__device__ __forceinline__ const float* factor_ptr(const DualArgs& a, uint64_t f) {
+  const uint32_t rho = static_cast<uint32_t>(f / a.n);
+  uint32_t k = 0, rbase = 0;
+  while (rho >= rbase + a.lora[k].r) { rbase += a.lora[k].r; ++k; }
+  return a.lora[k].A + static_cast<size_t>(rho - rbase) * a.n + (f - static_cast<uint64_t>(rho) * a.n);
+}
+
+// This CTA's chunk [lo, hi) of the flattened factor space (contiguous chunks,
+// one per shrink CTA).
+__device__ __forceinline__ void shrink_bounds(const DualArgs& a, const DualCfg& c, uint32_t cta, uint64_t* lo,
+                                              uint64_t* hi) {
+  const uint64_t total = static_cast<uint64_t>(a.rtot) * a.n;
+  *lo = cta * total / c.gs;
+  *hi = (cta + 1) * total / c.gs;
+}
+
 // Partial shrink sums of this CTA's chunk of the flattened [rtot][n] factor
 // space: partial[(t * rtot + rho) * gs + cta] = sum_{j in chunk, row rho} A[rho][j] x[t][j].
 template <int TT>
-__device__ void shrink_chunk(const DualArgs& a, const DualCfg& c, uint32_t cta, float* tmp,
-                             uint32_t warp, uint32_t lane) {
+__device__ void shrink_chunk(const DualArgs& a, const DualCfg& c, uint32_t cta, float* tmp, const float* sA,
+                             const void* xsrc, uint32_t warp, uint32_t lane, uint32_t ncw) {
   if (cta >= c.gs) return;
-  const uint32_t nthr = c.nwc * 32;
-  const uint64_t total = static_cast<uint64_t>(a.rtot) * a.n;
-  const uint64_t lo = cta * total / c.gs, hi = (cta + 1) * total / c.gs;
+  const uint32_t nthr = ncw * 32;
+  uint64_t lo, hi;
+  shrink_bounds(a, c, cta, &lo, &hi);
   const uint32_t rho_a = static_cast<uint32_t>(lo / a.n), rho_b = static_cast<uint32_t>((hi - 1) / a.n);
   for (uint32_t rho = rho_a; rho <= rho_b; ++rho) {
-    uint32_t k = 0, rbase = 0;
-    while (rho >= rbase + a.lora[k].r) { rbase += a.lora[k].r; ++k; }
-    const float* Arow = a.lora[k].A + static_cast<size_t>(rho - rbase) * a.n;
     const uint64_t rs = static_cast<uint64_t>(rho) * a.n;
     const uint32_t j0 = static_cast<uint32_t>(max(lo, rs) - rs);
     const uint32_t j1 = static_cast<uint32_t>(min(hi, rs + a.n) - rs);
+    const float* Arow = c.stage_a ? sA + (static_cast<int64_t>(rs) - static_cast<int64_t>(lo))
+                                  : factor_ptr(a, rs);
     float acc[TT];
 #pragma unroll
     for (int t = 0; t < TT; ++t) acc[t] = 0.f;
     for (uint32_t j = j0 + threadIdx.x; j < j1; j += nthr) {
-      const float av = __ldg(Arow + j);
+      const float av = Arow[j];
 #pragma unroll
       for (int t = 0; t < TT; ++t)
-        if (t < static_cast<int>(a.T)) acc[t] = fmaf(av, load_x(a.x, a.xdt, static_cast<size_t>(t) * a.n + j), acc[t]);
+        if (t < static_cast<int>(a.T)) acc[t] = fmaf(av, load_x(xsrc, a.xdt, static_cast<size_t>(t) * a.n + j), acc[t]);
     }
 #pragma unroll
     for (int t = 0; t < TT; ++t) {
@@ -224,7 +313,7 @@ __device__ void shrink_chunk(const DualArgs& a, const DualCfg& c, uint32_t cta, 
     named_bar(1, nthr);
     if (threadIdx.x < a.T) {
       float s = 0.f;
-      for (uint32_t w = 0; w < c.nwc; ++w) s += tmp[w * TT + threadIdx.x];
+      for (uint32_t w = 0; w < ncw; ++w) s += tmp[w * TT + threadIdx.x];
       a.ws.partial[(static_cast<size_t>(threadIdx.x) * a.rtot + rho) * c.gs + cta] = s;
     }
     named_bar(1, nthr);
@@ -232,7 +321,7 @@ __device__ void shrink_chunk(const DualArgs& a, const DualCfg& c, uint32_t cta, 
 }
 
 template <int QUANT, int TT, int RG>
-__global__ void __launch_bounds__(288, 2) k_dualpath(const DualArgs a, const DualCfg c) {
+__global__ void __launch_bounds__(kMaxThreads, 2) k_dualpath(const DualArgs a, const DualCfg c) {
   constexpr bool Q4 = QUANT == OVL_Q4_0;
   constexpr int N = TT * RG;
   constexpr int LN = Log2<N>::v;
@@ -240,7 +329,7 @@ __global__ void __launch_bounds__(288, 2) k_dualpath(const DualArgs a, const Dua
   extern __shared__ __align__(1024) uint8_t sm[];
   uint64_t* full = reinterpret_cast<uint64_t*>(sm);
   uint64_t* empty = full + kMaxNS;
-  volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(sm + 64);
+  volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(sm + 2 * kMaxNS * 8);
   uint8_t* rec = sm + c.off_rec;
   uint8_t* stages = sm + c.off_stage;
   float* red = reinterpret_cast<float*>(sm + c.off_red);
@@ -248,12 +337,13 @@ __global__ void __launch_bounds__(288, 2) k_dualpath(const DualArgs a, const Dua
   float* tmp = reinterpret_cast<float*>(sm + c.off_tmp);
 
   const uint32_t warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t ncw = c.nwc * c.ng;               // consumer warps
+  const uint32_t nthr = ncw * 32;
   const uint32_t G = gridDim.x, cta = blockIdx.x;
   const uint32_t row0 = static_cast<uint32_t>((static_cast<uint64_t>(cta) * a.m) / G);
   const uint32_t row1 = static_cast<uint32_t>((static_cast<uint64_t>(cta + 1) * a.m) / G);
   const uint32_t nrows = row1 - row0;
   const uint32_t nst = (nrows + RG - 1) / RG;
-  const uint32_t nthr = c.nwc * 32;
 
   if (threadIdx.x == 0) {
     for (uint32_t i = 0; i < c.ns; ++i) {
@@ -266,9 +356,9 @@ __global__ void __launch_bounds__(288, 2) k_dualpath(const DualArgs a, const Dua
   __syncthreads();
   griddep_launch_dependents();
 
-  if (warp == c.nwc) {
-    // ---------------- producer: stream this CTA's rows (base bytes are immutable,
-    // so this may start before the preceding grid has finished).
+  if (warp == ncw) {
+    // ---------------- producer: stream this CTA's rows in order.  The base is
+    // immutable, so this starts before the preceding grid has finished.
     if (lane == 0) {
       const uint64_t pol = l2_evict_first_policy();
       uint32_t issued = 0;
@@ -300,25 +390,66 @@ __global__ void __launch_bounds__(288, 2) k_dualpath(const DualArgs a, const Dua
   }
 
   // ---------------- consumers
+  const uint32_t grp = warp / c.nwc;                // consumer group: stages grp, grp+ng, ...
+  const uint32_t cw = warp - grp * c.nwc;           // column warp inside the group
+  const uint32_t L = cw * 32 + lane;                // column lane: blocks L, L + ncol, ...
+  const uint32_t ncol = c.nwc * 32;
+  float* sA = reinterpret_cast<float*>(sm + c.off_a);
+  float* sB = reinterpret_cast<float*>(sm + c.off_b);
+  // 0. immutable low-rank operands into shared memory while the preceding grid
+  //    may still run: this CTA's B rows of every term and its shrink chunk of A.
+  if (a.nl && c.stage_b) {
+    uint32_t rb = 0;
+    for (uint32_t k = 0; k < a.nl; ++k) {
+      const uint32_t cnt = nrows * a.lora[k].r;
+      const float* src = a.lora[k].B + static_cast<size_t>(row0) * a.lora[k].r;
+      for (uint32_t e = threadIdx.x; e < cnt; e += nthr) cp_async4(sB + nrows * rb + e, src + e);
+      rb += a.lora[k].r;
+    }
+  }
+  if (a.nl && c.stage_a && cta < c.gs) {
+    uint64_t lo, hi;
+    shrink_bounds(a, c, cta, &lo, &hi);
+    for (uint64_t f = lo + threadIdx.x; f < hi; f += nthr) cp_async4(sA + (f - lo), factor_ptr(a, f));
+  }
+  cp_async_commit();
   griddep_wait();  // x, y and the workspace may be touched by the preceding grid
+  const void* xsrc = a.x;
+  if (c.stage_x) {
+    uint8_t* sX = sm + c.off_x;
+    const uint32_t xbytes = a.T * a.n * (a.xdt == OVL_BF16 ? 2u : 4u);
+    const uint8_t* gx = static_cast<const uint8_t*>(a.x);
+    if (c.stage_x == 16) {
+      for (uint32_t e = threadIdx.x * 16; e < xbytes; e += nthr * 16) cp_async16(sX + e, gx + e);
+    } else {
+      for (uint32_t e = threadIdx.x * 4; e < xbytes; e += nthr * 4) cp_async4(sX + e, gx + e);
+    }
+    cp_async_commit();
+    xsrc = sX;
+  }
+  cp_async_wait_all();
+  named_bar(1, nthr);
 
   // 1. activation records for the tokens of this launch
-  for (uint32_t rr = warp; rr < a.T * c.nb; rr += c.nwc) {
-    const uint32_t t = rr / c.nb, b = rr - t * c.nb;
-    prep_record<Q4>(rec + static_cast<size_t>(rr) * kRecBytes, a.x, a.xdt,
-                    static_cast<size_t>(t) * a.n + b * 32 + lane, lane);
-  }
+  prep_records<Q4>(rec, a, xsrc, c.nb, warp, ncw, lane);
   // 2. low-rank shrink partials, published with one arrival per CTA
-  if (a.nl) shrink_chunk<TT>(a, c, cta, tmp, warp, lane);
+  if (a.nl) shrink_chunk<TT>(a, c, cta, tmp, sA, xsrc, warp, lane, ncw);
   named_bar(1, nthr);
   if (a.nl && threadIdx.x == 0) {
     __threadfence();
     atomicAdd(&a.ws.counter[0], 1ull);
   }
+  // single-token launches keep the lane's first record in registers
+  uint4 rreg[7];
+  if (TT == 1 && L < c.nb) {
+    const uint4* rp = reinterpret_cast<const uint4*>(rec + static_cast<size_t>(L) * kRecBytes);
+#pragma unroll
+    for (int i = 0; i < 7; ++i) rreg[i] = rp[i];
+  }
 
   // 3. stream the base rows
   bool ok = true;
-  for (uint32_t s = 0; s < nst; ++s) {
+  for (uint32_t s = grp; s < nst; s += c.ng) {
     const uint32_t slot = s % c.ns;
     // warp-uniform decision: the shuffles below need every lane
     if (!__all_sync(0xffffffffu, mbar_wait_bounded(&full[slot], (s / c.ns) & 1))) {
@@ -334,8 +465,19 @@ __global__ void __launch_bounds__(288, 2) k_dualpath(const DualArgs a, const Dua
     float acc[N];
 #pragma unroll
     for (int i = 0; i < N; ++i) acc[i] = 0.f;
-    for (uint32_t k = 0; k < c.bpl; ++k) {
-      const uint32_t b = threadIdx.x + k * nthr;
+    auto block = [&](uint32_t b, const uint4 (&r)[7], int t) {
+      const float xs = __uint_as_float(r[6].x);
+#pragma unroll
+      for (int rr = 0; rr < RG; ++rr) {
+        const uint8_t* wp = sq + rr * c.rowbytes + b * kBlockBytes;
+        const float P = Q4 ? dot_q4(wp, r) : dot_q8(wp, r);
+        const float d = __half2float(sd[rr * c.nb + b]);
+        acc[t * RG + rr] = fmaf(d * xs, P, acc[t * RG + rr]);
+      }
+    };
+    if (TT == 1 && L < c.nb) block(L, rreg, 0);
+    for (uint32_t k = (TT == 1 ? 1u : 0u); k < c.bpl; ++k) {
+      const uint32_t b = L + k * ncol;
       if (b < c.nb) {
 #pragma unroll
         for (int t = 0; t < TT; ++t) {
@@ -344,14 +486,7 @@ __global__ void __launch_bounds__(288, 2) k_dualpath(const DualArgs a, const Dua
             uint4 r[7];
 #pragma unroll
             for (int i = 0; i < 7; ++i) r[i] = rp[i];
-            const float xs = __uint_as_float(r[6].x);
-#pragma unroll
-            for (int rr = 0; rr < RG; ++rr) {
-              const uint8_t* wp = sq + rr * c.rowbytes + b * kBlockBytes;
-              const float P = Q4 ? dot_q4(wp, r) : dot_q8(wp, r);
-              const float d = __half2float(sd[rr * c.nb + b]);
-              acc[t * RG + rr] = fmaf(d * xs, P, acc[t * RG + rr]);
-            }
+            block(b, r, t);
           }
         }
       }
@@ -363,7 +498,7 @@ __global__ void __launch_bounds__(288, 2) k_dualpath(const DualArgs a, const Dua
       const uint32_t idx = lane >> (5 - LN);
       const uint32_t t = idx / RG, rr = idx - t * RG;
       const uint32_t lr = s * RG + rr;
-      if (lr < nrows && t < a.T) red[(warp * TT + t) * c.rows_max + lr] = tot;
+      if (lr < nrows && t < a.T) red[(cw * TT + t) * c.rows_max + lr] = tot;
     }
   }
   named_bar(1, nthr);
@@ -391,7 +526,14 @@ __global__ void __launch_bounds__(288, 2) k_dualpath(const DualArgs a, const Dua
       if (cl > c.gs - 1) cl = c.gs - 1;
       const float* p = a.ws.partial + (static_cast<size_t>(t) * a.rtot + rho) * c.gs;
       float s = 0.f;
-      for (uint64_t q = cf; q <= cl; ++q) s += __ldcg(p + q);
+      for (uint64_t q = cf; q <= cl; q += 4) {   // four loads in flight, summed in order
+        float v4[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) v4[u] = (q + u <= cl) ? __ldcg(p + q + u) : 0.f;
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+          if (q + u <= cl) s += v4[u];
+      }
       vsm[t * a.rtot + rho] = s;
     }
     named_bar(1, nthr);
@@ -405,40 +547,31 @@ __global__ void __launch_bounds__(288, 2) k_dualpath(const DualArgs a, const Dua
     }
   }
 
-  // 5. epilogue: y = base + sum_k s_k (B_k v_k), one warp per row
+  // 5. epilogue, one output per thread: y = base + sum_k s_k (B_k v_k)
   if (!ok) return;
-  for (uint32_t lr = warp; lr < nrows; lr += c.nwc) {
+  for (uint32_t i = threadIdx.x; i < a.T * nrows; i += nthr) {
+    const uint32_t t = i / nrows, lr = i - t * nrows;
     const uint32_t row = row0 + lr;
-    float yv[TT];
-#pragma unroll
-    for (int t = 0; t < TT; ++t) {
-      float s = 0.f;
-      if (t < static_cast<int>(a.T))
-        for (uint32_t w = 0; w < c.nwc; ++w) s += red[(w * TT + t) * c.rows_max + lr];
-      yv[t] = s;
-    }
+    float yv = 0.f;
+    for (uint32_t w = 0; w < c.nwc; ++w) yv += red[(w * TT + t) * c.rows_max + lr];
     uint32_t rbase = 0;
     for (uint32_t k = 0; k < a.nl; ++k) {
       const uint32_t r = a.lora[k].r;
-      const float* Brow = a.lora[k].B + static_cast<size_t>(row) * r;
-      float part[TT];
+      const float* Brow = c.stage_b ? sB + nrows * rbase + lr * r : a.lora[k].B + static_cast<size_t>(row) * r;
+      const float* vv = vsm + t * a.rtot + rbase;
+      float dot = 0.f;
+      for (uint32_t tau = 0; tau < r; tau += 8) {   // eight loads in flight, summed in order
+        float b8[8];
 #pragma unroll
-      for (int t = 0; t < TT; ++t) part[t] = 0.f;
-      for (uint32_t tau = lane; tau < r; tau += 32) {
-        const float bv = __ldg(Brow + tau);
+        for (int u = 0; u < 8; ++u) b8[u] = (tau + u < r) ? Brow[tau + u] : 0.f;
 #pragma unroll
-        for (int t = 0; t < TT; ++t)
-          if (t < static_cast<int>(a.T)) part[t] = fmaf(bv, vsm[t * a.rtot + rbase + tau], part[t]);
+        for (int u = 0; u < 8; ++u)
+          if (tau + u < r) dot = fmaf(b8[u], vv[tau + u], dot);
       }
-#pragma unroll
-      for (int t = 0; t < TT; ++t) yv[t] = fmaf(a.lora[k].s, warp_sum(part[t]), yv[t]);
+      yv = fmaf(a.lora[k].s, dot, yv);
       rbase += r;
     }
-    if (lane == 0) {
-#pragma unroll
-      for (int t = 0; t < TT; ++t)
-        if (t < static_cast<int>(a.T)) a.y[static_cast<size_t>(t) * a.m + row] = yv[t];
-    }
+    a.y[static_cast<size_t>(t) * a.m + row] = yv;
   }
 }
 
@@ -447,9 +580,10 @@ using KernelFn = void (*)(const DualArgs, const DualCfg);
 KernelFn pick(uint32_t quant, int tt, int rg) {
 #define OVL_K(Q, T_, R_) \
   if (quant == Q && tt == T_ && rg == R_) return k_dualpath<Q, T_, R_>;
-  OVL_K(OVL_Q8_0, 1, 2) OVL_K(OVL_Q8_0, 1, 8) OVL_K(OVL_Q8_0, 2, 2) OVL_K(OVL_Q8_0, 4, 2)
-  OVL_K(OVL_Q8_0, 8, 2) OVL_K(OVL_Q4_0, 1, 2) OVL_K(OVL_Q4_0, 1, 8) OVL_K(OVL_Q4_0, 2, 2)
-  OVL_K(OVL_Q4_0, 4, 2) OVL_K(OVL_Q4_0, 8, 2)
+  OVL_K(OVL_Q8_0, 1, 1) OVL_K(OVL_Q8_0, 1, 2) OVL_K(OVL_Q8_0, 1, 4) OVL_K(OVL_Q8_0, 1, 8)
+  OVL_K(OVL_Q8_0, 2, 2) OVL_K(OVL_Q8_0, 4, 2) OVL_K(OVL_Q8_0, 8, 2)
+  OVL_K(OVL_Q4_0, 1, 1) OVL_K(OVL_Q4_0, 1, 2) OVL_K(OVL_Q4_0, 1, 4) OVL_K(OVL_Q4_0, 1, 8)
+  OVL_K(OVL_Q4_0, 2, 2) OVL_K(OVL_Q4_0, 4, 2) OVL_K(OVL_Q4_0, 8, 2)
 #undef OVL_K
   return nullptr;
 }
@@ -463,10 +597,14 @@ int device_sms() {
   return n > 0 ? n : 1;
 }
 
-// Shared-memory plan for one launch; returns false if it cannot fit.
+// Shared-memory plan for one launch; returns false if it cannot fit.  A plan
+// under kSoftBudget leaves room for a CTA of the next launch on the same SM,
+// which then prefetches its weights while this grid drains.
+constexpr uint32_t kSoftBudget = OVL_K1_SOFT_KB * 1024;
+
 bool plan(DualCfg& c, const DualArgs& a, int tt, int rg, uint32_t G) {
   c.rows_max = (a.m + G - 1) / G;
-  uint32_t off = 128;
+  uint32_t off = round_up(2 * kMaxNS * 8 + 16, 256);   // mbarriers + abort flag
   c.off_rec = off;
   off = round_up(off + tt * c.nb * kRecBytes, 128);
   c.off_red = off;
@@ -474,12 +612,27 @@ bool plan(DualCfg& c, const DualArgs& a, int tt, int rg, uint32_t G) {
   c.off_v = off;
   off = round_up(off + tt * a.rtot * 4 + 4, 128);
   c.off_tmp = off;
-  off = round_up(off + c.nwc * tt * 4, 1024);
+  off = round_up(off + c.nwc * c.ng * tt * 4, 128);
+  c.off_x = off;
+  if (c.stage_x) off = round_up(off + tt * a.n * (a.xdt == OVL_BF16 ? 2 : 4), 128);
+  c.off_a = off;
+  if (c.stage_a) off = round_up(off + (static_cast<uint32_t>(static_cast<uint64_t>(a.rtot) * a.n / std::max<uint32_t>(c.gs, 1)) + 2) * 4, 128);
+  c.off_b = off;
+  if (c.stage_b) off = round_up(off + c.rows_max * a.rtot * 4, 128);
+  off = round_up(off, 1024);
   c.stage_q = rg * c.rowbytes;
   c.stage_bytes = round_up(c.stage_q + round_up(rg * c.nb * 2, 16) + 32, 128);
   c.off_stage = off;
-  for (uint32_t ns = kMaxNS; ns >= 2; --ns) {
-    if (off + ns * c.stage_bytes <= kSmemBudget) {
+  // Group g consumes the stages s = g, g+ng, ...  With ns a multiple of ng every
+  // slot is consumed by one group only, in order, so a consumer is never more
+  // than one barrier phase ahead of its slot (the parity wait cannot alias).
+  for (uint32_t budget : {kSoftBudget, kSmemBudget}) {
+    if (off + c.stage_bytes > budget) continue;
+    const uint32_t max_ns = std::min<uint32_t>(kMaxNS, (budget - off) / c.stage_bytes);
+    const uint32_t ng = std::min<uint32_t>(c.ng, max_ns);
+    const uint32_t ns = max_ns / ng * ng;
+    if (ns >= 2 * ng || budget == kSmemBudget) {
+      c.ng = ng;
       c.ns = ns;
       c.smem = off + ns * c.stage_bytes;
       return true;
@@ -496,44 +649,65 @@ cudaError_t launch_dualpath(const DualArgs& a0, cudaStream_t st) {
   DualCfg c{};
   c.nb = a0.n / kQK;
   c.rowbytes = a0.quant == OVL_Q8_0 ? a0.n : a0.n / 2;
-  // consumer warps: fewest idle lanes, then fewest blocks per lane
+  // column warps: fewest blocks per lane, then fewest idle lanes
   uint32_t best_w = 1, best_b = 0, best_waste = ~0u;
   for (uint32_t w = 1; w <= 8; ++w) {
     const uint32_t b = (c.nb + 32 * w - 1) / (32 * w);
     const uint32_t waste = b * 32 * w - c.nb;
-    if (b < best_b || best_b == 0 || (b == best_b && waste < best_waste)) {
+    if (best_b == 0 || b < best_b || (b == best_b && waste < best_waste)) {
       best_w = w; best_b = b; best_waste = waste;
     }
   }
   c.nwc = best_w;
   c.bpl = best_b;
+  c.ng = std::max<uint32_t>(1, std::min<uint32_t>(OVL_K1_MAX_GROUPS, 8 / c.nwc));
   // token tile
   int tt = 1;
   const uint32_t Tneed = a0.T < 8 ? a0.T : 8;
   while (tt < static_cast<int>(Tneed)) tt *= 2;
   while (tt > 1 && tt * c.nb * kRecBytes > kRecBudget) tt /= 2;
-  const int rg = (tt == 1 && c.rowbytes * 8 <= 40960) ? 8 : 2;
+  int rg = 2;
+  if (tt == 1) {
+    rg = 1;
+    while (rg < 8 && 2 * rg * c.rowbytes <= OVL_K1_STAGE_BYTES) rg *= 2;
+  }
   KernelFn fn = pick(a0.quant, tt, rg);
   if (!fn) return cudaErrorInvalidValue;
-  const uint32_t threads = (c.nwc + 1) * 32;
-  // grid: co-resident CTAs, at least two rows each
-  uint32_t G = static_cast<uint32_t>(nsm) * 2;
-  G = std::min<uint32_t>(G, std::max<uint32_t>(1, a0.m / 2));
-  int occ = 0;
-  for (int iter = 0; iter < 4; ++iter) {
-    if (!plan(c, a0, tt, rg, G)) return cudaErrorInvalidConfiguration;
-    cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, c.smem);
-    if (e != cudaSuccess) return e;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, fn, threads, c.smem);
-    if (e != cudaSuccess) return e;
-    if (occ < 1) return cudaErrorInvalidConfiguration;
-    const uint32_t cap = static_cast<uint32_t>(nsm) * static_cast<uint32_t>(occ);
-    if (G <= cap) break;
-    G = cap;
-  }
-  if (!plan(c, a0, tt, rg, G)) return cudaErrorInvalidConfiguration;
+  const uint32_t G = std::min<uint32_t>(static_cast<uint32_t>(nsm), a0.m);
   c.gs = a0.nl ? static_cast<uint32_t>(std::min<uint64_t>(G, static_cast<uint64_t>(a0.rtot) * a0.n)) : 0;
   if (a0.nl && static_cast<size_t>(tt) * a0.rtot * c.gs > a0.ws.partial_floats) return cudaErrorInvalidValue;
+  // operands staged in shared memory when small (immutable ones before the
+  // grid dependency resolves, activations right after)
+  const uint32_t esz_x = a0.xdt == OVL_BF16 ? 2 : 4;
+  const uintptr_t xa = reinterpret_cast<uintptr_t>(a0.x);
+  const bool x_small = static_cast<uint64_t>(tt) * a0.n * esz_x <= 32768;
+  c.stage_x = !x_small ? 0 : (xa % 16 == 0 ? 16 : (xa % 4 == 0 ? 4 : 0));
+  const uint32_t rows_max = (a0.m + G - 1) / G;
+  c.stage_b = a0.nl && static_cast<uint64_t>(rows_max) * a0.rtot * 4 <= 32768;
+  c.stage_a = a0.nl && (static_cast<uint64_t>(a0.rtot) * a0.n / std::max<uint32_t>(c.gs, 1) + 2) * 4 <= 32768;
+  if (!plan(c, a0, tt, rg, G)) return cudaErrorInvalidConfiguration;
+  if (c.ns % c.ng != 0 || c.ns > static_cast<uint32_t>(kMaxNS)) return cudaErrorInvalidConfiguration;
+  const uint32_t threads = (c.nwc * c.ng + 1) * 32;
+  // one attribute / occupancy query per (kernel, shared-memory size)
+  struct Seen { KernelFn fn; uint32_t smem; int occ; };
+  static std::mutex mu;
+  static Seen seen[64];
+  static int nseen = 0;
+  int occ = -1;
+  {
+    std::lock_guard<std::mutex> lk(mu);
+    for (int i = 0; i < nseen; ++i)
+      if (seen[i].fn == fn && seen[i].smem == c.smem) occ = seen[i].occ;
+    if (occ < 0) {
+      cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBudget);
+      if (e != cudaSuccess) return e;
+      e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, fn, threads, c.smem);
+      if (e != cudaSuccess) return e;
+      if (nseen < 64) seen[nseen++] = {fn, c.smem, occ};
+    }
+  }
+  if (occ < 1) return cudaErrorInvalidConfiguration;
+  cudaError_t e = cudaSuccess;
 
   const size_t esz = a0.xdt == OVL_BF16 ? 2 : 4;
   for (uint32_t t0 = 0; t0 < a0.T; t0 += tt) {
@@ -551,7 +725,7 @@ cudaError_t launch_dualpath(const DualArgs& a0, cudaStream_t st) {
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    cudaError_t e = cudaLaunchKernelEx(&cfg, fn, a, c);
+    e = cudaLaunchKernelEx(&cfg, fn, a, c);
     if (e != cudaSuccess) return e;
   }
   return cudaSuccess;

@@ -110,8 +110,7 @@ struct Adapter {
   uint8_t digest[32];
   uint8_t key[32];
   uint32_t total_rank = 0;
-  cudaEvent_t last_use = nullptr;
-  bool used = false;
+  bool used = false;        // read by at least one forward call
 };
 
 struct Entry {
@@ -169,7 +168,12 @@ struct DeviceGuard {
   bool ok = false;
   explicit DeviceGuard(int dev) {
     if (cudaGetDevice(&prev) != cudaSuccess) prev = -1;
-    ok = cudaSetDevice(dev) == cudaSuccess;
+    if (prev == dev) {
+      prev = -1;   // already current: nothing to restore
+      ok = true;
+    } else {
+      ok = cudaSetDevice(dev) == cudaSuccess;
+    }
   }
   ~DeviceGuard() {
     if (prev >= 0) cudaSetDevice(prev);
@@ -372,11 +376,6 @@ ovl_status ovl_destroy(ovl_ctx* ctx) {
   {
     DeviceGuard g(ctx->device);
     cudaStreamSynchronize(ctx->stream);
-    for (auto& kv : ctx->staged)
-      if (kv.second.last_use) {
-        cudaEventSynchronize(kv.second.last_use);
-        cudaEventDestroy(kv.second.last_use);
-      }
     if (ctx->fwd_recorded) cudaEventSynchronize(ctx->fwd_done);
     cudaEventDestroy(ctx->fwd_done);
     cudaStreamDestroy(ctx->stream);
@@ -492,8 +491,6 @@ ovl_status ovl_stage_adapter(ovl_ctx* ctx, const ovl_adapter_desc* desc, const v
   if (e == cudaSuccess) e = cudaStreamSynchronize(ctx->stream);
   if (e != cudaSuccess) return release(cuda_fail(ctx, e, "finite scan"));
   if (bad) return release(fail(ctx, OVL_E_NONFINITE, "adapter payload holds NaN or Inf"));
-  e = cudaEventCreateWithFlags(&ad.last_use, cudaEventDisableTiming);
-  if (e != cudaSuccess) return release(cuda_fail(ctx, e, "event"));
   compute_adapter_key(ad);
   ad.h = ctx->next_h++;
   *out = ad.h;
@@ -512,15 +509,14 @@ ovl_status ovl_unstage_adapter(ovl_ctx* ctx, ovl_adapter_h h) {
         if (e.h == h) return fail(ctx, OVL_E_STATE, "adapter is part of the active or rollback composition");
   DeviceGuard g(ctx->device);
   Adapter& a = it->second;
-  if (a.used) {
+  if (a.used && ctx->fwd_recorded) {
     if (ctx->policy == OVL_SWITCH_DRAIN) {
-      cudaEventSynchronize(a.last_use);
+      cudaEventSynchronize(ctx->fwd_done);
     } else {
-      cudaError_t q = cudaEventQuery(a.last_use);
+      cudaError_t q = cudaEventQuery(ctx->fwd_done);
       if (q == cudaErrorNotReady) return fail(ctx, OVL_E_BUSY, "forward work reading the adapter is in flight");
     }
   }
-  cudaEventDestroy(a.last_use);
   ctx->alloc.release(a.off);
   ctx->staged.erase(it);
   return ok(ctx);
@@ -609,15 +605,13 @@ uint32_t stack_terms(ovl_ctx* c, const Composition& comp, uint32_t tensor, LoraR
   return nl;
 }
 
+// One event per forward call: forward work on a context is stream-ordered, so
+// once the latest record has completed every earlier forward has too.
 ovl_status record_use(ovl_ctx* c, const std::vector<Adapter*>& used, cudaStream_t st) {
   cudaError_t e = cudaEventRecord(c->fwd_done, st);
   if (e != cudaSuccess) return cuda_fail(c, e, "event record");
   c->fwd_recorded = true;
-  for (Adapter* a : used) {
-    e = cudaEventRecord(a->last_use, st);
-    if (e != cudaSuccess) return cuda_fail(c, e, "event record");
-    a->used = true;
-  }
+  for (Adapter* a : used) a->used = true;
   return OVL_OK;
 }
 
