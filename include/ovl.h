@@ -256,6 +256,36 @@ ovl_status ovl_segmented_forward(ovl_ctx* ctx, uint32_t tensor, const void* x, u
                                  uint32_t T, const int32_t* seg_offsets, const int32_t* seg_slot,
                                  uint32_t n_seg, const int32_t* perm, float* y, void* stream);
 
+/* Allocation-free dual-path forward.  No counterpart in the source pages: it
+ * serves callers that can neither lend an arena (ovl_create) nor allocate device
+ * memory at call time -- code running while a stream capture is in progress in
+ * the global capture mode, where cudaMalloc is refused, or an embedder whose
+ * device memory belongs entirely to its own pooled allocator.
+ *   y = deq(W) x + sum_k scale[k] B[k] (A[k] x), exactly the computation of
+ *   ovl_linear_forward on the dual path for the STACK composition (B[0..n), ...).
+ * qs, d: device pointers to one tensor's planes in the layout above (16-byte
+ * aligned; the d plane readable up to the next multiple of 16 bytes).  A, B,
+ * rank, scale: HOST arrays of n_terms entries; A[k] float32 [rank][d_in] and
+ * B[k] float32 [d_out][rank] are device pointers.  x, y as in
+ * ovl_linear_forward.  Runs on the current device, on `stream`.
+ * Scratch: a file-scope device array of 2 MiB per device (held by every GPU
+ * that loads the library until the process exits) instead of cudaMalloc; the
+ * call allocates nothing and calls no allocating routine.  The first call on a
+ * device looks up the array's address and clears it (synchronizing the device),
+ * so make that first call before any stream capture.  Every call clears the
+ * array's status word and counters on `stream` and then reuses its contents;
+ * calls that overlap on the GPU (different streams, or other threads) race on
+ * the array and must be serialized by the caller.
+ * Errors: OVL_E_QUANT, OVL_E_SHAPE (d_in, alignment, rank, total rank), OVL_E_ARG
+ * (null pointers, dtype, T > OVL_MAX_T, n_terms > OVL_MAX_STACK, non-finite
+ * scale), OVL_E_OOM (the low-rank partial sums would need more than the 2 MiB
+ * array), OVL_E_CUDA.  T = 0 is a no-op.  Device-side timeouts are latched in
+ * the array's status word only. */
+ovl_status ovl_dualpath_forward_noalloc(const void* qs, const void* d, uint32_t quant, uint32_t d_out,
+                                        uint32_t d_in, const float* const* A, const float* const* B,
+                                        const uint32_t* rank, const float* scale, uint32_t n_terms,
+                                        const void* x, uint32_t x_dtype, uint32_t T, float* y, void* stream);
+
 /* Recompute the content digest of the base's device bytes now (device leaf
  * hashing on `stream`, synchronizes).  Used to check that the base stays
  * bit-identical across switches ([DTD] §2 Oracle Invariant). */

@@ -2,8 +2,8 @@
 
 Argument marshalling only: every step of the computation runs in the CUDA
 library.  Importing this package loads ``libovl.so`` from this directory and
-raises ImportError if it has not been built (``python -m
-quantized_base_lora_gb300.build``); there is no fallback implementation.
+raises ImportError if it has not been built (``python
+quantized_base_lora_gb300/build.py``); there is no fallback implementation.
 
 Device buffers and streams are passed as integers (e.g. ``tensor.data_ptr()``
 and ``torch.cuda.current_stream().cuda_stream``).  Functions keep the C names
@@ -72,7 +72,7 @@ class ovl_entry(C.Structure):
 
 def _load():
     if not os.path.exists(LIB_PATH):
-        raise ImportError(f"libovl.so is not built ({LIB_PATH}); run python -m quantized_base_lora_gb300.build")
+        raise ImportError(f"libovl.so is not built ({LIB_PATH}); run python quantized_base_lora_gb300/build.py")
     lib = C.CDLL(LIB_PATH)
     P, U32, U64, I32, SZ = C.c_void_p, C.c_uint32, C.c_uint64, C.c_int32, C.c_size_t
     B32 = C.POINTER(C.c_uint8)
@@ -97,6 +97,8 @@ def _load():
         "ovl_sha256": ([P, SZ, B32], I32),
         "ovl_content_digest": ([P, SZ, B32], I32),
         "ovl_version": ([], C.c_char_p),
+        "ovl_dualpath_forward_noalloc": ([P, P, U32, U32, U32, C.POINTER(P), C.POINTER(P), C.POINTER(U32),
+                                          C.POINTER(C.c_float), U32, P, U32, U32, P, P], I32),
     }
     for name, (args, res) in sig.items():
         fn = getattr(lib, name)
@@ -110,7 +112,7 @@ EXPORTED = ("ovl_create", "ovl_destroy", "ovl_load_base", "ovl_stage_adapter", "
             "ovl_activate", "ovl_rollback", "ovl_linear_forward", "ovl_materialize_layer",
             "ovl_segmented_forward", "ovl_base_digest", "ovl_get_state", "ovl_get_entry",
             "ovl_check_device", "ovl_debug_inject", "ovl_last_error", "ovl_sha256",
-            "ovl_content_digest", "ovl_version")
+            "ovl_content_digest", "ovl_version", "ovl_dualpath_forward_noalloc")
 
 
 class OvlError(RuntimeError):
@@ -270,3 +272,16 @@ def ovl_check_device(ctx, stream: int = 0) -> int:
 
 def ovl_debug_inject(ctx, phase: int, code: int) -> int:
     return lib.ovl_debug_inject(ctx, int(phase), int(code))
+
+
+def ovl_dualpath_forward_noalloc(qs_ptr: int, d_ptr: int, quant: int, d_out: int, d_in: int, A_ptrs, B_ptrs,
+                                 ranks, scales, x_ptr: int, x_dtype: int, T: int, y_ptr: int,
+                                 stream: int = 0) -> int:
+    """Allocation-free dual-path forward (see include/ovl.h); factor pointers are device addresses."""
+    n = len(ranks)
+    Ap = (C.c_void_p * max(n, 1))(*[C.c_void_p(p) for p in A_ptrs])
+    Bp = (C.c_void_p * max(n, 1))(*[C.c_void_p(p) for p in B_ptrs])
+    return lib.ovl_dualpath_forward_noalloc(C.c_void_p(qs_ptr), C.c_void_p(d_ptr), int(quant), int(d_out), int(d_in),
+                                            Ap, Bp, _u32s(ranks) if n else None,
+                                            (C.c_float * n)(*scales) if n else None, n, C.c_void_p(x_ptr),
+                                            int(x_dtype), int(T), C.c_void_p(y_ptr), C.c_void_p(stream))

@@ -2,7 +2,7 @@
 
 Each translation unit under csrc/ is compiled in its own process, in parallel,
 then linked into quantized_base_lora_gb300/libovl.so against the shared CUDA
-runtime.  Usage: python -m quantized_base_lora_gb300.build
+runtime.  Usage: python quantized_base_lora_gb300/build.py  (runs without importing the package)
 """
 from __future__ import annotations
 

@@ -1,0 +1,137 @@
+// Allocation-free variant of the dual-path forward.
+//
+// The regular entry point (ovl_linear_forward) takes its kernel scratch -- the
+// low-rank partial sums, the grid arrival counters and the device status word
+// -- from the arena that the caller lent to ovl_create.  Some callers have no
+// arena to lend and cannot allocate device memory when they call: code that
+// runs while a stream capture is in progress in the global capture mode (where
+// cudaMalloc is refused), or an embedder whose device memory is owned entirely
+// by its own pooled allocator.  For them this file keeps the scratch in one
+// file-scope device array, sized once at load time, so a call needs nothing but
+// the caller's inputs and outputs.
+//
+// There is no counterpart to this entry point in the source pages; it is an
+// interface convenience around the same kernel (k_dualpath) and computes
+// exactly what ovl_linear_forward computes for a STACK composition.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cmath>
+#include <mutex>
+
+#include "ovl_internal.h"
+
+namespace ovl {
+namespace {
+
+// 2 MiB of scratch per device: 256 B status word, 256 B arrival counters, the
+// rest low-rank partial sums (T-tile x total rank x shrink CTAs floats).  Every
+// GPU that loads the library keeps this array until the process exits.
+constexpr size_t kNoAllocBytes = 2u << 20;
+constexpr size_t kNoAllocStatus = 0;
+constexpr size_t kNoAllocCounter = 256;
+constexpr size_t kNoAllocPartial = 512;
+constexpr int kMaxDevices = 64;
+
+static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocBytes];
+
+std::mutex g_setup_mu;
+uint8_t* g_scratch_addr[kMaxDevices] = {};
+
+// Device address of the array on the current device, looked up (and the array
+// cleared) on the first call for that device.  In host code the array's name is
+// only a host-side stand-in, so the kernel receives this looked-up address.
+cudaError_t scratch_for_current_device(uint8_t** out, int* dev_out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  *dev_out = dev;
+  std::lock_guard<std::mutex> lk(g_setup_mu);
+  if (!g_scratch_addr[dev]) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess) return e;
+    e = cudaMemset(p, 0, kNoAllocBytes);
+    if (e == cudaSuccess) e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) return e;
+    g_scratch_addr[dev] = static_cast<uint8_t*>(p);
+  }
+  *out = g_scratch_addr[dev];
+  return cudaSuccess;
+}
+
+}  // namespace
+}  // namespace ovl
+
+extern "C" ovl_status ovl_dualpath_forward_noalloc(const void* qs, const void* d, uint32_t quant, uint32_t d_out,
+                                                   uint32_t d_in, const float* const* A, const float* const* B,
+                                                   const uint32_t* rank, const float* scale, uint32_t n_terms,
+                                                   const void* x, uint32_t x_dtype, uint32_t T, float* y,
+                                                   void* stream) {
+  using namespace ovl;
+  if (quant != OVL_Q8_0 && quant != OVL_Q4_0) return OVL_E_QUANT;
+  if (d_out == 0 || d_in == 0 || d_in % kQK != 0) return OVL_E_SHAPE;
+  if (x_dtype != OVL_F32 && x_dtype != OVL_BF16) return OVL_E_ARG;
+  if (T > OVL_MAX_T) return OVL_E_ARG;
+  if (n_terms > OVL_MAX_STACK) return OVL_E_ARG;
+  if (n_terms && (!A || !B || !rank || !scale)) return OVL_E_ARG;
+  if (!qs || !d || (T && (!x || !y))) return OVL_E_ARG;
+  if ((reinterpret_cast<uintptr_t>(qs) & 15) || (reinterpret_cast<uintptr_t>(d) & 15))
+    return OVL_E_SHAPE;
+  DualArgs a{};
+  uint32_t rtot = 0;
+  for (uint32_t k = 0; k < n_terms; ++k) {
+    if (!A[k] || !B[k]) return OVL_E_ARG;
+    if (rank[k] == 0 || rank[k] > OVL_MAX_RANK) return OVL_E_SHAPE;
+    if (!std::isfinite(scale[k])) return OVL_E_ARG;
+    a.lora[k] = LoraRef{A[k], B[k], rank[k], scale[k]};
+    rtot += rank[k];
+  }
+  if (rtot > OVL_MAX_TOTAL_RANK) return OVL_E_SHAPE;
+  if (T == 0) return OVL_OK;
+
+  uint8_t* scratch = nullptr;
+  int dev = 0;
+  cudaError_t e = scratch_for_current_device(&scratch, &dev);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return OVL_E_CUDA;
+  }
+  // Largest partial-sum demand of any launch of this call: a token tile of at
+  // most 8, the total rank, and at most one shrink chunk per SM.
+  int nsm = 0;
+  cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev);
+  const uint64_t shrink_ctas = std::min<uint64_t>(static_cast<uint64_t>(nsm > 0 ? nsm : 1),
+                                                  static_cast<uint64_t>(rtot) * d_in);
+  const uint64_t need = kNoAllocPartial + 4ull * 8 * rtot * shrink_ctas;
+  if (n_terms && need > kNoAllocBytes) return OVL_E_OOM;   // more scratch than the static array holds
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  // The status word and the arrival counters must start at zero.
+  e = cudaMemsetAsync(scratch, 0, kNoAllocPartial, st);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return OVL_E_CUDA;
+  }
+  a.qs = static_cast<const uint8_t*>(qs);
+  a.dpl = static_cast<const uint8_t*>(d);
+  a.m = d_out;
+  a.n = d_in;
+  a.quant = quant;
+  a.x = x;
+  a.xdt = x_dtype;
+  a.T = T;
+  a.y = y;
+  a.nl = n_terms;
+  a.rtot = rtot;
+  a.ws.status = reinterpret_cast<uint32_t*>(scratch + kNoAllocStatus);
+  a.ws.counter = reinterpret_cast<unsigned long long*>(scratch + kNoAllocCounter);
+  a.ws.partial = reinterpret_cast<float*>(scratch + kNoAllocPartial);
+  a.ws.partial_floats = (kNoAllocBytes - kNoAllocPartial) / sizeof(float);
+  e = launch_dualpath(a, st);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return OVL_E_CUDA;
+  }
+  return OVL_OK;
+}
