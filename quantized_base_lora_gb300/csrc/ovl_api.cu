@@ -687,7 +687,7 @@ ovl_status ovl_linear_forward(ovl_ctx* ctx, uint32_t tensor, const void* x, uint
   } else {
     const size_t need = size_t(td.d_out) * td.d_in * 4;
     const size_t xneed = jit_gemm_x_scratch_bytes(T, td.d_in);
-    if (!scratch || (reinterpret_cast<uintptr_t>(scratch) & 127) || scratch_bytes < need + xneed)
+    if (!scratch || (reinterpret_cast<uintptr_t>(scratch) & 127) || scratch_bytes < (need + 127) / 128 * 128 + xneed)
       return fail(ctx, OVL_E_ARG, "JIT scratch must be 128-byte aligned and hold the layer plus the widened activations");
     MatArgs m{};
     m.qs = ctx->base + td.qs_off;

@@ -97,6 +97,9 @@ __device__ __forceinline__ uint32_t dp4a_uu(uint32_t a, uint32_t b, uint32_t c) 
   return d;
 }
 
+// Latch the first device-side failure code into a status word.
+__device__ __forceinline__ void latch_status(uint32_t* status, uint32_t code) { atomicCAS(status, 0u, code); }
+
 __device__ __forceinline__ unsigned long long ld_acquire_u64(const unsigned long long* p) {
   unsigned long long v;
   asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
