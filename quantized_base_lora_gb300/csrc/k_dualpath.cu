@@ -557,6 +557,10 @@ __global__ void __launch_bounds__(kMaxThreads, 2) k_dualpath(const DualArgs a, c
     uint32_t rbase = 0;
     for (uint32_t k = 0; k < a.nl; ++k) {
       const uint32_t r = a.lora[k].r;
+      if (a.tok_sel && a.tok_term[t] != static_cast<int>(k)) {   // segmented: one term per token
+        rbase += r;
+        continue;
+      }
       const float* Brow = c.stage_b ? sB + nrows * rbase + lr * r : a.lora[k].B + static_cast<size_t>(row) * r;
       const float* vv = vsm + t * a.rtot + rbase;
       float dot = 0.f;
@@ -715,6 +719,8 @@ cudaError_t launch_dualpath(const DualArgs& a0, cudaStream_t st) {
     a.T = std::min<uint32_t>(tt, a0.T - t0);
     a.x = static_cast<const uint8_t*>(a0.x) + static_cast<size_t>(t0) * a0.n * esz;
     a.y = a0.y + static_cast<size_t>(t0) * a0.m;
+    if (a0.tok_sel)
+      for (uint32_t t = 0; t < 8; ++t) a.tok_term[t] = (t0 + t < a0.T) ? a0.tok_host[t0 + t] : -1;
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = dim3(G);
     cfg.blockDim = dim3(threads);

@@ -40,6 +40,7 @@ constexpr size_t kPartialOff = 1024;
 constexpr size_t kPartialBytes = 8u << 20;
 constexpr size_t kReservedEnd = kPartialOff + kPartialBytes;
 constexpr size_t kMinArena = 16u << 20;
+constexpr uint32_t kMaxTableRank = 1024;   // sum of ranks of a TABLE composition on one tensor
 constexpr char kRuntimeTag[16] = {'o', 'v', 'l', '-', 'g', 'b', '3', '0', '0', ' ', 'v', '1', 0, 0, 0, 0};
 
 // First-fit sub-allocator over [kReservedEnd, arena_bytes) of the caller's arena.
@@ -713,9 +714,70 @@ ovl_status ovl_segmented_forward(ovl_ctx* ctx, uint32_t tensor, const void* x, u
                                  const int32_t* perm, float* y, void* stream) {
   if (!ctx) return OVL_E_ARG;
   std::lock_guard<std::mutex> lk(ctx->mu);
-  (void)tensor; (void)x; (void)x_dtype; (void)T; (void)seg_offsets; (void)seg_slot; (void)n_seg;
-  (void)perm; (void)y; (void)stream;
-  return fail(ctx, OVL_E_STATE, "segmented forward is not available in this build");
+  if (!ctx->base_loaded) return fail(ctx, OVL_E_STATE, "no base loaded");
+  if (ctx->active->mode != OVL_MODE_TABLE) return fail(ctx, OVL_E_STATE, "segmented forward needs a TABLE composition");
+  if (tensor >= ctx->tensors.size()) return fail(ctx, OVL_E_ARG, "no such tensor");
+  if (x_dtype != OVL_F32 && x_dtype != OVL_BF16) return fail(ctx, OVL_E_ARG, "unknown activation dtype");
+  if (T > OVL_MAX_T) return fail(ctx, OVL_E_ARG, "T exceeds OVL_MAX_T");
+  if (n_seg > OVL_MAX_SEGMENTS) return fail(ctx, OVL_E_ARG, "too many segments");
+  if (T == 0) return ok(ctx);
+  if (!x || !y || !seg_offsets || !seg_slot || !perm || n_seg == 0) return fail(ctx, OVL_E_ARG, "null argument");
+  // segments: offsets nondecreasing from 0 to T; perm a permutation; slots valid
+  const Composition& comp = *ctx->active;
+  const int32_t n_slots = static_cast<int32_t>(comp.entries.size());
+  if (seg_offsets[0] != 0 || seg_offsets[n_seg] != static_cast<int32_t>(T))
+    return fail(ctx, OVL_E_ARG, "segment offsets must run from 0 to T");
+  for (uint32_t s = 0; s < n_seg; ++s) {
+    if (seg_offsets[s + 1] < seg_offsets[s]) return fail(ctx, OVL_E_ARG, "segment offsets must not decrease");
+    if (seg_slot[s] < -1 || seg_slot[s] >= n_slots) return fail(ctx, OVL_E_ARG, "segment slot out of range");
+  }
+  std::vector<uint8_t> seen(T, 0);
+  for (uint32_t j = 0; j < T; ++j) {
+    if (perm[j] < 0 || perm[j] >= static_cast<int32_t>(T) || seen[perm[j]]) return fail(ctx, OVL_E_ARG, "perm is not a permutation");
+    seen[perm[j]] = 1;
+  }
+  // low-rank terms: every table slot that targets this tensor
+  const ovl_tensor_desc& td = ctx->tensors[tensor];
+  DualArgs a{};
+  std::vector<int> slot_term(n_slots, -1);
+  std::vector<Adapter*> used;
+  for (int32_t sl = 0; sl < n_slots; ++sl) {
+    Adapter& ad = ctx->staged.at(comp.entries[sl].h);
+    const Target* tg = target_for(ad, tensor);
+    if (!tg) continue;
+    slot_term[sl] = static_cast<int>(a.nl);
+    a.lora[a.nl].A = reinterpret_cast<const float*>(ctx->arena + ad.off + tg->a_off);
+    a.lora[a.nl].B = reinterpret_cast<const float*>(ctx->arena + ad.off + tg->b_off);
+    a.lora[a.nl].r = tg->rank;
+    a.lora[a.nl].s = comp.entries[sl].s;
+    a.rtot += tg->rank;
+    ++a.nl;
+    used.push_back(&ad);
+  }
+  if (a.rtot > kMaxTableRank) return fail(ctx, OVL_E_SHAPE, "total rank of the table on this tensor exceeds the limit");
+  // request r (row r of x and y) uses the slot of the segment holding it
+  std::vector<int8_t> tok(T, -1);
+  for (uint32_t s = 0; s < n_seg; ++s)
+    for (int32_t j = seg_offsets[s]; j < seg_offsets[s + 1]; ++j)
+      tok[perm[j]] = static_cast<int8_t>(seg_slot[s] >= 0 ? slot_term[seg_slot[s]] : -1);
+  DeviceGuard g(ctx->device);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  a.qs = ctx->base + td.qs_off;
+  a.dpl = ctx->base + td.d_off;
+  a.m = td.d_out;
+  a.n = td.d_in;
+  a.quant = ctx->quant;
+  a.x = x;
+  a.xdt = x_dtype;
+  a.T = T;
+  a.y = y;
+  a.tok_sel = 1;
+  a.tok_host = tok.data();
+  a.ws = ctx->ws;
+  cudaError_t e = launch_dualpath(a, st);
+  if (e != cudaSuccess) return cuda_fail(ctx, e, "segmented launch");
+  if (ovl_status s = record_use(ctx, used, st)) return s;
+  return ok(ctx);
 }
 
 ovl_status ovl_base_digest(ovl_ctx* ctx, uint8_t digest_out[32], void* stream) {

@@ -47,7 +47,12 @@ struct DualArgs {
   float* y;               // [T][m]
   uint32_t nl;            // number of low-rank terms
   uint32_t rtot;          // sum of ranks
-  LoraRef lora[OVL_MAX_STACK];
+  LoraRef lora[OVL_MAX_TABLE];
+  // Per-token term selection (segmented batches): when tok_sel is set, token t
+  // of the launch receives only term tok_term[t] (-1: base only).
+  uint32_t tok_sel;
+  int8_t tok_term[8];           // this launch's slice (filled by the launcher)
+  const int8_t* tok_host;       // host array of T entries (launcher only)
   Workspace ws;
 };
 
