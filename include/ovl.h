@@ -236,6 +236,17 @@ ovl_status ovl_linear_forward(ovl_ctx* ctx, uint32_t tensor, const void* x, uint
                               uint32_t T, float* y, uint32_t path, float* scratch,
                               size_t scratch_bytes, void* stream);
 
+/* Dual path for up to 4 tensors that read the same activations -- the q, k and
+ * v projections of a block, or gate and up -- in one launch ([DTD] §8: decode is
+ * memory-bandwidth bound, so one pass streams every weight once and the fixed
+ * per-launch latency is paid once).  tensors: host array of n tensor indices,
+ * all with the same d_in; ys: host array of n device pointers, ys[i] float32
+ * [T][d_out of tensors[i]].  Each output equals ovl_linear_forward(tensors[i],
+ * path OVL_PATH_DUAL).  STACK compositions only.  Errors as ovl_linear_forward,
+ * plus OVL_E_SHAPE when the d_in differ and OVL_E_ARG for n = 0 or n > 4. */
+ovl_status ovl_linear_forward_multi(ovl_ctx* ctx, uint32_t n, const uint32_t* tensors, const void* x,
+                                    uint32_t x_dtype, uint32_t T, float* const* ys, void* stream);
+
 /* Materialize S = deq(W) + sum_k s_k B_k A_k (STACK composition, float32
  * [d_out][d_in] row-major) into the caller's device scratch without requantizing
  * ([DTD] §5 Fresh-Base Oracle Definition; §7 Scratch Overhead).  With an empty

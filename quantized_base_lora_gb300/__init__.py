@@ -86,6 +86,7 @@ def _load():
         "ovl_rollback": ([P, B32], I32),
         "ovl_linear_forward": ([P, U32, P, U32, U32, P, U32, P, SZ, P], I32),
         "ovl_materialize_layer": ([P, U32, P, SZ, P], I32),
+        "ovl_linear_forward_multi": ([P, U32, C.POINTER(U32), P, U32, U32, C.POINTER(P), P], I32),
         "ovl_segmented_forward": ([P, U32, P, U32, U32, C.POINTER(I32), C.POINTER(I32), U32,
                                    C.POINTER(I32), P, P], I32),
         "ovl_base_digest": ([P, B32, P], I32),
@@ -109,7 +110,7 @@ def _load():
 
 lib = _load()
 EXPORTED = ("ovl_create", "ovl_destroy", "ovl_load_base", "ovl_stage_adapter", "ovl_unstage_adapter",
-            "ovl_activate", "ovl_rollback", "ovl_linear_forward", "ovl_materialize_layer",
+            "ovl_activate", "ovl_rollback", "ovl_linear_forward", "ovl_linear_forward_multi", "ovl_materialize_layer",
             "ovl_segmented_forward", "ovl_base_digest", "ovl_get_state", "ovl_get_entry",
             "ovl_check_device", "ovl_debug_inject", "ovl_last_error", "ovl_sha256",
             "ovl_content_digest", "ovl_version", "ovl_dualpath_forward_noalloc")
@@ -229,6 +230,13 @@ def ovl_linear_forward(ctx, tensor: int, x_ptr: int, x_dtype: int, T: int, y_ptr
                        stream: int = 0) -> int:
     return lib.ovl_linear_forward(ctx, int(tensor), C.c_void_p(x_ptr), int(x_dtype), int(T), C.c_void_p(y_ptr),
                                   int(path), C.c_void_p(scratch_ptr), int(scratch_bytes), C.c_void_p(stream))
+
+
+def ovl_linear_forward_multi(ctx, tensors, x_ptr: int, x_dtype: int, T: int, y_ptrs, stream: int = 0) -> int:
+    n = len(tensors)
+    ys = (C.c_void_p * max(n, 1))(*[C.c_void_p(p) for p in y_ptrs])
+    return lib.ovl_linear_forward_multi(ctx, n, _u32s(tensors), C.c_void_p(x_ptr), int(x_dtype), int(T), ys,
+                                        C.c_void_p(stream))
 
 
 def ovl_materialize_layer(ctx, tensor: int, scratch_ptr: int, scratch_bytes: int, stream: int = 0) -> int:

@@ -51,11 +51,27 @@ constexpr int kRecBytes = 112;  // per (token, block) activation record: 7 x 16 
 #ifndef OVL_K1_STAGE_BYTES
 #define OVL_K1_STAGE_BYTES 16384
 #endif
+#ifndef OVL_K1_PDL
+#define OVL_K1_PDL 1
+#endif
 #ifndef OVL_K1_MAX_GROUPS
 #define OVL_K1_MAX_GROUPS 4
 #endif
 constexpr int kMaxNS = OVL_K1_MAX_NS;
-constexpr int kMaxThreads = 9 * 32;    // up to 8 consumer warps + 1 producer warp
+constexpr int kMaxThreads = 10 * 32;       // up to 8 consumer warps + producer + helper
+constexpr int kMaxThreadsWide = 16 * 32;   // wide rows: up to 14 consumer warps, one CTA per SM
+
+// Variants that stream at most two rows per stage serve wide rows (d_in >= 8K
+// for q8_0): they run one CTA per SM with more warps and keep two activation
+// records per lane in registers.  The others run two CTAs per SM, so the next
+// launch's CTA can be resident (and prefetching) while this one drains.
+template <int TT, int RG>
+struct K1Shape {
+  static constexpr bool wide = RG <= 2;
+  static constexpr int threads = wide ? kMaxThreadsWide : kMaxThreads;
+  static constexpr int min_blocks = wide ? 1 : 2;
+  static constexpr int reg_records = (wide && TT == 1) ? 2 : 1;
+};
 constexpr uint32_t kRecBudget = 128 * 1024;
 constexpr uint32_t kSmemBudget = 220 * 1024;
 
@@ -74,6 +90,7 @@ struct DualCfg {
   uint32_t off_x, off_a, off_b;  // staged activations, shrink chunk, B rows
   uint32_t stage_x;              // 0: x read from global; 4 or 16: cp.async granule
   uint32_t stage_a, stage_b;     // 1: operand staged in shared memory
+  uint32_t div32;                // 1: rtot * n * gs < 2^32, chunk arithmetic fits 32 bits
   uint32_t smem;
 };
 
@@ -90,96 +107,196 @@ __device__ __forceinline__ float load_x(const void* x, uint32_t xdt, size_t i) {
 
 // Activation records.  Record (t, b) describes the 32-block b of token t as
 // an exact integer vector X with x_j = X_j * 2^-s (|X_j| <= 2^22), split in
-// three signed byte limbs X = 65536 h + 256 m + l with m, l in [-128, 127]
-// (balanced base-256 digits, so every dot product is a signed x signed dp4a):
-// words 0-7 = h, 8-15 = m, 16-23 = l, then {2^-s as f32 bits, start_h,
-// start_m, start_l}.  Limb word k
-// holds the four elements that weight word k consumes: elements 4k..4k+3 for
-// q8_0; for q4_0 word 2g carries the low nibbles (elements 8g, 8g+2, 8g+4, 8g+6)
-// and word 2g+1 the high nibbles (8g+1, ...).  The q4_0 starts are -8 * sum of
-// the limbs, which folds the code offset into the integer accumulators.
-//
-// One warp builds four records at a time: lane k = lane & 7 of each 8-lane
-// group produces limb word k of its block.
+// three byte limbs X = 65536 h + 256 m + l with h signed (byte 2 of X) and m, l
+// unsigned (bytes 1 and 0): words 0-7 = h, 8-15 = m, 16-23 = l, then
+// {2^-s as f32 bits, start_h, start_m, start_l}.  Limb word k holds the four
+// elements that weight word k consumes: elements 4k..4k+3 for q8_0; for q4_0
+// word 2g carries the low nibbles (elements 8g, 8g+2, 8g+4, 8g+6) and word
+// 2g+1 the high nibbles (8g+1, ...).  The q4_0 starts are -8 * sum of the limbs,
+// which folds the code offset into the integer accumulators.
+// Block exponent of a record: x_j = X_j * 2^-s with |X_j| <= 2^22.  Blocks
+// whose largest magnitude is below 2^-104 (including subnormal-only blocks) are
+// flushed to zero: their whole contribution is below 2^-104 * 127 * 32 *
+// max|d|, far under the absolute 1e-5 term of the output bound.  Finite fp32
+// inputs cannot need a downward shift beyond the normal range.
+struct BlockScale {
+  float sc;   // 2^s
+  float xs;   // 2^-s (0 for a flushed block)
+};
+__device__ __forceinline__ BlockScale block_scale(uint32_t mx) {
+  const int E = static_cast<int>(mx >> 23) - 127;   // mx >= 2^-104 is normal
+  const int s = 21 - E;
+  if (mx < 0x0B800000u) return BlockScale{0.f, 0.f};  // 2^-104: flush
+  return BlockScale{__uint_as_float(static_cast<uint32_t>(s + 127) << 23),
+                    __uint_as_float(static_cast<uint32_t>(127 - s) << 23)};
+}
+
+// Exact round-to-nearest-even of v * 2^s to an integer, |result| <= 2^22:
+// adding 1.5 * 2^23 leaves the integer in the low mantissa bits.
+__device__ __forceinline__ int round_scaled(float v, float sc) {
+  return __float_as_int(fmaf(v, sc, 12582912.0f)) - 0x4B400000;
+}
+
+// Limb words of four rounded integers: h (byte 2), m (byte 1), l (byte 0).
+__device__ __forceinline__ void limb_words(const int (&X)[4], uint32_t& hw, uint32_t& mw, uint32_t& lw) {
+  const uint32_t x0 = static_cast<uint32_t>(X[0]), x1 = static_cast<uint32_t>(X[1]);
+  const uint32_t x2 = static_cast<uint32_t>(X[2]), x3 = static_cast<uint32_t>(X[3]);
+  hw = __byte_perm(__byte_perm(x0, x1, 0x0062), __byte_perm(x2, x3, 0x0062), 0x5410);
+  mw = __byte_perm(__byte_perm(x0, x1, 0x0051), __byte_perm(x2, x3, 0x0051), 0x5410);
+  lw = __byte_perm(__byte_perm(x0, x1, 0x0040), __byte_perm(x2, x3, 0x0040), 0x5410);
+}
+
+// One warp builds four records per batch and two batches at a time: lane
+// k = lane & 7 of each 8-lane group produces limb word k of its record.
+// Activations staged in shared memory are read with one vector load per lane.
+
+// The four activation values that limb word k of block `row` consumes.
 template <bool Q4>
-__device__ __forceinline__ void prep_records(uint8_t* rec, const DualArgs& a, const void* xsrc, uint32_t nb,
-                                             uint32_t warp, uint32_t nwarps, uint32_t lane) {
-  const uint32_t k = lane & 7;
-  const uint32_t total = a.T * nb;
-  for (uint32_t base = warp * 4; base < total; base += nwarps * 4) {
-    const uint32_t ri = base + (lane >> 3);
-    const bool live = ri < total;
-    const uint32_t t = live ? ri / nb : 0, b = live ? ri - t * nb : 0;
-    float v[4];
-    const size_t row = static_cast<size_t>(t) * a.n + static_cast<size_t>(b) * 32;
+__device__ __forceinline__ void load_word_inputs(const void* xsrc, uint32_t xdt, bool vec, size_t row, uint32_t k,
+                                                 float (&v)[4]) {
+  if (vec && xdt == OVL_BF16) {
+    const uint16_t* xb = static_cast<const uint16_t*>(xsrc);
+    if (!Q4) {
+      const uint2 w = *reinterpret_cast<const uint2*>(xb + row + 4 * k);
+      v[0] = __uint_as_float(w.x << 16); v[1] = __uint_as_float(w.x & 0xFFFF0000u);
+      v[2] = __uint_as_float(w.y << 16); v[3] = __uint_as_float(w.y & 0xFFFF0000u);
+    } else {
+      const uint4 w = *reinterpret_cast<const uint4*>(xb + row + 8 * (k >> 1));
+      const bool odd = k & 1;
+      v[0] = __uint_as_float(odd ? (w.x & 0xFFFF0000u) : (w.x << 16));
+      v[1] = __uint_as_float(odd ? (w.y & 0xFFFF0000u) : (w.y << 16));
+      v[2] = __uint_as_float(odd ? (w.z & 0xFFFF0000u) : (w.z << 16));
+      v[3] = __uint_as_float(odd ? (w.w & 0xFFFF0000u) : (w.w << 16));
+    }
+  } else if (vec) {
+    const float* xf = static_cast<const float*>(xsrc);
+    if (!Q4) {
+      const float4 w = *reinterpret_cast<const float4*>(xf + row + 4 * k);
+      v[0] = w.x; v[1] = w.y; v[2] = w.z; v[3] = w.w;
+    } else {
+      const float4 w0 = *reinterpret_cast<const float4*>(xf + row + 8 * (k >> 1));
+      const float4 w1 = *reinterpret_cast<const float4*>(xf + row + 8 * (k >> 1) + 4);
+      const bool odd = k & 1;
+      v[0] = odd ? w0.y : w0.x; v[1] = odd ? w0.w : w0.z;
+      v[2] = odd ? w1.y : w1.x; v[3] = odd ? w1.w : w1.z;
+    }
+  } else {
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
       const uint32_t e = Q4 ? (8 * (k >> 1) + (k & 1) + 2 * i) : (4 * k + i);
-      v[i] = live ? load_x(xsrc, a.xdt, row + e) : 0.f;
+      v[i] = load_x(xsrc, xdt, row + e);
     }
-    uint32_t mx = 0;
+  }
+}
+
+template <bool Q4>
+__device__ __forceinline__ void build_record(uint8_t* rec, uint32_t ri, bool live, uint32_t k, const float (&v)[4]) {
+  uint32_t mx = 0;
 #pragma unroll
-    for (int i = 0; i < 4; ++i) mx = max(mx, __float_as_uint(v[i]) & 0x7FFFFFFFu);
-    mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-    mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-    mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
-    int X[4] = {0, 0, 0, 0};
-    float xs = 0.f;
-    if (mx != 0u) {
-      const int E = mx >= 0x00800000u ? static_cast<int>(mx >> 23) - 127 : ilogbf(__uint_as_float(mx));
-      const int s = 21 - E;
-      if (s >= -126 && s <= 126) {
-        const float sc = __uint_as_float(static_cast<uint32_t>(s + 127) << 23);
-        xs = __uint_as_float(static_cast<uint32_t>(127 - s) << 23);
+  for (int i = 0; i < 4; ++i) mx = max(mx, __float_as_uint(v[i]) & 0x7FFFFFFFu);
+  mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+  mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+  mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+  const BlockScale bs = block_scale(mx);
+  const float xs = bs.xs;
+  int X[4];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) X[i] = __float2int_rn(v[i] * sc);
-      } else {
-        xs = ldexpf(1.0f, -s);
+  for (int i = 0; i < 4; ++i) X[i] = round_scaled(v[i], bs.sc);
+  uint32_t hw, mw, lw;
+  limb_words(X, hw, mw, lw);
+  int sh = 0, sm = 0, sl = 0;
+  if (Q4) {
+    sh = dp4a_ss(static_cast<int>(hw), 0x01010101, 0);
+    sm = static_cast<int>(dp4a_uu(mw, 0x01010101u, 0u));
+    sl = static_cast<int>(dp4a_uu(lw, 0x01010101u, 0u));
 #pragma unroll
-        for (int i = 0; i < 4; ++i) X[i] = __float2int_rn(ldexpf(v[i], s));
-      }
+    for (int o = 1; o <= 4; o <<= 1) {
+      sh += __shfl_xor_sync(0xffffffffu, sh, o);
+      sm += __shfl_xor_sync(0xffffffffu, sm, o);
+      sl += __shfl_xor_sync(0xffffffffu, sl, o);
     }
-    int H[4], M[4], Lw[4];
+  }
+  if (live) {
+    uint32_t* w = reinterpret_cast<uint32_t*>(rec + static_cast<size_t>(ri) * kRecBytes);
+    w[k] = hw;
+    w[8 + k] = mw;
+    w[16 + k] = lw;
+    if (k == 0) *reinterpret_cast<uint4*>(w + 24) = make_uint4(__float_as_uint(xs), static_cast<uint32_t>(-8 * sh),
+                                                                static_cast<uint32_t>(-8 * sm),
+                                                                static_cast<uint32_t>(-8 * sl));
+  }
+}
+
+// The record of one block built by a single lane straight into registers
+// (single-token launches) from activations staged in shared memory.
+template <bool Q4>
+__device__ __forceinline__ void lane_record(uint4 (&r)[7], const void* xsrc, uint32_t xdt, bool vec, size_t row) {
+  float v[32];
+  if (vec && xdt == OVL_BF16) {
+    const uint4* p = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(xsrc) + row);
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      Lw[i] = ((X[i] + 128) & 0xFF) - 128;
-      const int x1 = (X[i] - Lw[i]) >> 8;
-      M[i] = ((x1 + 128) & 0xFF) - 128;
-      H[i] = (x1 - M[i]) >> 8;
+    for (int q = 0; q < 4; ++q) {
+      const uint4 w = p[q];
+      v[8 * q + 0] = __uint_as_float(w.x << 16); v[8 * q + 1] = __uint_as_float(w.x & 0xFFFF0000u);
+      v[8 * q + 2] = __uint_as_float(w.y << 16); v[8 * q + 3] = __uint_as_float(w.y & 0xFFFF0000u);
+      v[8 * q + 4] = __uint_as_float(w.z << 16); v[8 * q + 5] = __uint_as_float(w.z & 0xFFFF0000u);
+      v[8 * q + 6] = __uint_as_float(w.w << 16); v[8 * q + 7] = __uint_as_float(w.w & 0xFFFF0000u);
     }
-    const uint32_t h01 = __byte_perm(static_cast<uint32_t>(H[0]), static_cast<uint32_t>(H[1]), 0x0040);
-    const uint32_t h23 = __byte_perm(static_cast<uint32_t>(H[2]), static_cast<uint32_t>(H[3]), 0x0040);
-    const uint32_t m01 = __byte_perm(static_cast<uint32_t>(M[0]), static_cast<uint32_t>(M[1]), 0x0040);
-    const uint32_t m23 = __byte_perm(static_cast<uint32_t>(M[2]), static_cast<uint32_t>(M[3]), 0x0040);
-    const uint32_t l01 = __byte_perm(static_cast<uint32_t>(Lw[0]), static_cast<uint32_t>(Lw[1]), 0x0040);
-    const uint32_t l23 = __byte_perm(static_cast<uint32_t>(Lw[2]), static_cast<uint32_t>(Lw[3]), 0x0040);
-    int sh = 0, sm = 0, sl = 0;
+  } else if (vec) {
+    const float4* p = reinterpret_cast<const float4*>(static_cast<const float*>(xsrc) + row);
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      const float4 w = p[q];
+      v[4 * q + 0] = w.x; v[4 * q + 1] = w.y; v[4 * q + 2] = w.z; v[4 * q + 3] = w.w;
+    }
+  } else {
+#pragma unroll
+    for (int j = 0; j < 32; ++j) v[j] = load_x(xsrc, xdt, row + j);
+  }
+  uint32_t mx = 0;
+#pragma unroll
+  for (int j = 0; j < 32; ++j) mx = max(mx, __float_as_uint(v[j]) & 0x7FFFFFFFu);
+  const BlockScale bs = block_scale(mx);
+  int sh = 0, sm = 0, sl = 0;
+  uint32_t hw[8], mw[8], lw[8];
+#pragma unroll
+  for (int w = 0; w < 8; ++w) {
+    int X[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) X[i] = round_scaled(v[Q4 ? (8 * (w >> 1) + (w & 1) + 2 * i) : (4 * w + i)], bs.sc);
+    limb_words(X, hw[w], mw[w], lw[w]);
     if (Q4) {
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        sh += H[i];
-        sm += M[i];
-        sl += Lw[i];
-      }
-#pragma unroll
-      for (int o = 1; o <= 4; o <<= 1) {
-        sh += __shfl_xor_sync(0xffffffffu, sh, o);
-        sm += __shfl_xor_sync(0xffffffffu, sm, o);
-        sl += __shfl_xor_sync(0xffffffffu, sl, o);
-      }
+      sh = dp4a_ss(static_cast<int>(hw[w]), 0x01010101, sh);
+      sm = static_cast<int>(dp4a_uu(mw[w], 0x01010101u, static_cast<uint32_t>(sm)));
+      sl = static_cast<int>(dp4a_uu(lw[w], 0x01010101u, static_cast<uint32_t>(sl)));
     }
-    if (live) {
-      uint32_t* w = reinterpret_cast<uint32_t*>(rec + static_cast<size_t>(ri) * kRecBytes);
-      w[k] = __byte_perm(h01, h23, 0x5410);
-      w[8 + k] = __byte_perm(m01, m23, 0x5410);
-      w[16 + k] = __byte_perm(l01, l23, 0x5410);
-      if (k == 0) {
-        w[24] = __float_as_uint(xs);
-        w[25] = static_cast<uint32_t>(-8 * sh);
-        w[26] = static_cast<uint32_t>(-8 * sm);
-        w[27] = static_cast<uint32_t>(-8 * sl);
-      }
-    }
+  }
+  r[0] = make_uint4(hw[0], hw[1], hw[2], hw[3]);
+  r[1] = make_uint4(hw[4], hw[5], hw[6], hw[7]);
+  r[2] = make_uint4(mw[0], mw[1], mw[2], mw[3]);
+  r[3] = make_uint4(mw[4], mw[5], mw[6], mw[7]);
+  r[4] = make_uint4(lw[0], lw[1], lw[2], lw[3]);
+  r[5] = make_uint4(lw[4], lw[5], lw[6], lw[7]);
+  r[6] = Q4 ? make_uint4(__float_as_uint(bs.xs), static_cast<uint32_t>(-8 * sh), static_cast<uint32_t>(-8 * sm),
+                         static_cast<uint32_t>(-8 * sl))
+            : make_uint4(__float_as_uint(bs.xs), 0u, 0u, 0u);
+}
+
+template <bool Q4>
+__device__ __forceinline__ void prep_records(uint8_t* rec, const DualArgs& a, const void* xsrc, bool vec, uint32_t nb,
+                                             uint32_t warp, uint32_t nwarps, uint32_t lane) {
+  const uint32_t k = lane & 7;
+  const uint32_t total = a.T * nb;
+  for (uint32_t base = warp * 8; base < total; base += nwarps * 8) {
+    const uint32_t ri0 = base + (lane >> 3), ri1 = ri0 + 4;
+    const bool live0 = ri0 < total, live1 = ri1 < total;
+    const uint32_t t0 = live0 ? ri0 / nb : 0, b0 = live0 ? ri0 - t0 * nb : 0;
+    const uint32_t t1 = live1 ? ri1 / nb : 0, b1 = live1 ? ri1 - t1 * nb : 0;
+    float v0[4] = {0.f, 0.f, 0.f, 0.f}, v1[4] = {0.f, 0.f, 0.f, 0.f};
+    if (live0) load_word_inputs<Q4>(xsrc, a.xdt, vec, static_cast<size_t>(t0) * a.n + static_cast<size_t>(b0) * 32, k, v0);
+    if (live1) load_word_inputs<Q4>(xsrc, a.xdt, vec, static_cast<size_t>(t1) * a.n + static_cast<size_t>(b1) * 32, k, v1);
+    build_record<Q4>(rec, ri0, live0, k, v0);
+    build_record<Q4>(rec, ri1, live1, k, v1);
   }
 }
 
@@ -195,40 +312,41 @@ __device__ __forceinline__ float dot_q8(const uint8_t* wp, const uint4 (&r)[7]) 
   sh = dp4a_ss(a.z, r[0].z, sh); sh = dp4a_ss(a.w, r[0].w, sh);
   sh = dp4a_ss(b.x, r[1].x, sh); sh = dp4a_ss(b.y, r[1].y, sh);
   sh = dp4a_ss(b.z, r[1].z, sh); sh = dp4a_ss(b.w, r[1].w, sh);
-  sm = dp4a_ss(a.x, r[2].x, sm); sm = dp4a_ss(a.y, r[2].y, sm);
-  sm = dp4a_ss(a.z, r[2].z, sm); sm = dp4a_ss(a.w, r[2].w, sm);
-  sm = dp4a_ss(b.x, r[3].x, sm); sm = dp4a_ss(b.y, r[3].y, sm);
-  sm = dp4a_ss(b.z, r[3].z, sm); sm = dp4a_ss(b.w, r[3].w, sm);
-  sl = dp4a_ss(a.x, r[4].x, sl); sl = dp4a_ss(a.y, r[4].y, sl);
-  sl = dp4a_ss(a.z, r[4].z, sl); sl = dp4a_ss(a.w, r[4].w, sl);
-  sl = dp4a_ss(b.x, r[5].x, sl); sl = dp4a_ss(b.y, r[5].y, sl);
-  sl = dp4a_ss(b.z, r[5].z, sl); sl = dp4a_ss(b.w, r[5].w, sl);
+  sm = dp4a_su(a.x, r[2].x, sm); sm = dp4a_su(a.y, r[2].y, sm);
+  sm = dp4a_su(a.z, r[2].z, sm); sm = dp4a_su(a.w, r[2].w, sm);
+  sm = dp4a_su(b.x, r[3].x, sm); sm = dp4a_su(b.y, r[3].y, sm);
+  sm = dp4a_su(b.z, r[3].z, sm); sm = dp4a_su(b.w, r[3].w, sm);
+  sl = dp4a_su(a.x, r[4].x, sl); sl = dp4a_su(a.y, r[4].y, sl);
+  sl = dp4a_su(a.z, r[4].z, sl); sl = dp4a_su(a.w, r[4].w, sl);
+  sl = dp4a_su(b.x, r[5].x, sl); sl = dp4a_su(b.y, r[5].y, sl);
+  sl = dp4a_su(b.z, r[5].z, sl); sl = dp4a_su(b.w, r[5].w, sl);
   return limb_combine(sh, sm, sl);
 }
 
-// q4_0 codes 0..15 are valid signed bytes, so the code words go straight into
-// signed dp4a; the -8 offset is in the accumulator starts of the record.
+// q4_0: unsigned codes 0..15 against the limbs; the -8 offset is in the
+// accumulator starts of the record.
 __device__ __forceinline__ float dot_q4(const uint8_t* wp, const uint4 (&r)[7]) {
   const uint4 w = *reinterpret_cast<const uint4*>(wp);
   const uint32_t m4 = 0x0F0F0F0Fu;
-  const int l0 = w.x & m4, h0 = (w.x >> 4) & m4;
-  const int l1 = w.y & m4, h1 = (w.y >> 4) & m4;
-  const int l2 = w.z & m4, h2 = (w.z >> 4) & m4;
-  const int l3 = w.w & m4, h3 = (w.w >> 4) & m4;
-  int sh = static_cast<int>(r[6].y), sm = static_cast<int>(r[6].z), sl = static_cast<int>(r[6].w);
-  sh = dp4a_ss(l0, r[0].x, sh); sh = dp4a_ss(h0, r[0].y, sh);
-  sh = dp4a_ss(l1, r[0].z, sh); sh = dp4a_ss(h1, r[0].w, sh);
-  sh = dp4a_ss(l2, r[1].x, sh); sh = dp4a_ss(h2, r[1].y, sh);
-  sh = dp4a_ss(l3, r[1].z, sh); sh = dp4a_ss(h3, r[1].w, sh);
-  sm = dp4a_ss(l0, r[2].x, sm); sm = dp4a_ss(h0, r[2].y, sm);
-  sm = dp4a_ss(l1, r[2].z, sm); sm = dp4a_ss(h1, r[2].w, sm);
-  sm = dp4a_ss(l2, r[3].x, sm); sm = dp4a_ss(h2, r[3].y, sm);
-  sm = dp4a_ss(l3, r[3].z, sm); sm = dp4a_ss(h3, r[3].w, sm);
-  sl = dp4a_ss(l0, r[4].x, sl); sl = dp4a_ss(h0, r[4].y, sl);
-  sl = dp4a_ss(l1, r[4].z, sl); sl = dp4a_ss(h1, r[4].w, sl);
-  sl = dp4a_ss(l2, r[5].x, sl); sl = dp4a_ss(h2, r[5].y, sl);
-  sl = dp4a_ss(l3, r[5].z, sl); sl = dp4a_ss(h3, r[5].w, sl);
-  return limb_combine(sh, sm, sl);
+  const uint32_t l0 = w.x & m4, h0 = (w.x >> 4) & m4;
+  const uint32_t l1 = w.y & m4, h1 = (w.y >> 4) & m4;
+  const uint32_t l2 = w.z & m4, h2 = (w.z >> 4) & m4;
+  const uint32_t l3 = w.w & m4, h3 = (w.w >> 4) & m4;
+  int sh = static_cast<int>(r[6].y);
+  uint32_t sm = r[6].z, sl = r[6].w;
+  sh = dp4a_us(l0, r[0].x, sh); sh = dp4a_us(h0, r[0].y, sh);
+  sh = dp4a_us(l1, r[0].z, sh); sh = dp4a_us(h1, r[0].w, sh);
+  sh = dp4a_us(l2, r[1].x, sh); sh = dp4a_us(h2, r[1].y, sh);
+  sh = dp4a_us(l3, r[1].z, sh); sh = dp4a_us(h3, r[1].w, sh);
+  sm = dp4a_uu(l0, r[2].x, sm); sm = dp4a_uu(h0, r[2].y, sm);
+  sm = dp4a_uu(l1, r[2].z, sm); sm = dp4a_uu(h1, r[2].w, sm);
+  sm = dp4a_uu(l2, r[3].x, sm); sm = dp4a_uu(h2, r[3].y, sm);
+  sm = dp4a_uu(l3, r[3].z, sm); sm = dp4a_uu(h3, r[3].w, sm);
+  sl = dp4a_uu(l0, r[4].x, sl); sl = dp4a_uu(h0, r[4].y, sl);
+  sl = dp4a_uu(l1, r[4].z, sl); sl = dp4a_uu(h1, r[4].w, sl);
+  sl = dp4a_uu(l2, r[5].x, sl); sl = dp4a_uu(h2, r[5].y, sl);
+  sl = dp4a_uu(l3, r[5].z, sl); sl = dp4a_uu(h3, r[5].w, sl);
+  return limb_combine(sh, static_cast<int>(sm), static_cast<int>(sl));
 }
 
 // Sum over the 32 lanes of v[lane >> (5 - log2 N)] for all N values at once
@@ -275,18 +393,43 @@ __device__ __forceinline__ const float* factor_ptr(const DualArgs& a, uint64_t f
 // one per shrink CTA).
 __device__ __forceinline__ void shrink_bounds(const DualArgs& a, const DualCfg& c, uint32_t cta, uint64_t* lo,
                                               uint64_t* hi) {
-  const uint64_t total = static_cast<uint64_t>(a.rtot) * a.n;
-  *lo = cta * total / c.gs;
-  *hi = (cta + 1) * total / c.gs;
+  if (c.div32) {
+    const uint32_t total = a.rtot * a.n;
+    *lo = cta * total / c.gs;
+    *hi = (cta + 1) * total / c.gs;
+  } else {
+    const uint64_t total = static_cast<uint64_t>(a.rtot) * a.n;
+    *lo = cta * total / c.gs;
+    *hi = (cta + 1) * total / c.gs;
+  }
+}
+
+// Range [cf, cl] of shrink CTAs whose chunk overlaps factor row rho.
+__device__ __forceinline__ void partial_range(const DualArgs& a, const DualCfg& c, uint32_t rho, uint32_t* cf,
+                                              uint32_t* cl) {
+  uint32_t f, l;
+  if (c.div32) {
+    const uint32_t total = a.rtot * a.n;
+    f = ((rho * a.n + 1) * c.gs + total - 1) / total;
+    l = ((rho + 1) * a.n * c.gs + total - 1) / total;
+  } else {
+    const uint64_t total = static_cast<uint64_t>(a.rtot) * a.n;
+    f = static_cast<uint32_t>(((static_cast<uint64_t>(rho) * a.n + 1) * c.gs + total - 1) / total);
+    l = static_cast<uint32_t>(((static_cast<uint64_t>(rho + 1) * a.n) * c.gs + total - 1) / total);
+  }
+  f = f ? f - 1 : 0;
+  l = l ? l - 1 : 0;
+  *cf = f;
+  *cl = l > c.gs - 1 ? c.gs - 1 : l;
 }
 
 // Partial shrink sums of this CTA's chunk of the flattened [rtot][n] factor
-// space: partial[(t * rtot + rho) * gs + cta] = sum_{j in chunk, row rho} A[rho][j] x[t][j].
+// space, computed by one warp: partial[(t * rtot + rho) * gs + cta] =
+// sum_{j in chunk, row rho} A[rho][j] x[t][j] (lane-strided, fixed-order
+// warp reduction).
 template <int TT>
-__device__ void shrink_chunk(const DualArgs& a, const DualCfg& c, uint32_t cta, float* tmp, const float* sA,
-                             const void* xsrc, uint32_t warp, uint32_t lane, uint32_t ncw) {
-  if (cta >= c.gs) return;
-  const uint32_t nthr = ncw * 32;
+__device__ void shrink_chunk_warp(const DualArgs& a, const DualCfg& c, uint32_t cta, const float* sA,
+                                  const void* xsrc, uint32_t lane) {
   uint64_t lo, hi;
   shrink_bounds(a, c, cta, &lo, &hi);
   const uint32_t rho_a = static_cast<uint32_t>(lo / a.n), rho_b = static_cast<uint32_t>((hi - 1) / a.n);
@@ -294,12 +437,11 @@ __device__ void shrink_chunk(const DualArgs& a, const DualCfg& c, uint32_t cta, 
     const uint64_t rs = static_cast<uint64_t>(rho) * a.n;
     const uint32_t j0 = static_cast<uint32_t>(max(lo, rs) - rs);
     const uint32_t j1 = static_cast<uint32_t>(min(hi, rs + a.n) - rs);
-    const float* Arow = c.stage_a ? sA + (static_cast<int64_t>(rs) - static_cast<int64_t>(lo))
-                                  : factor_ptr(a, rs);
+    const float* Arow = c.stage_a ? sA + (static_cast<int64_t>(rs) - static_cast<int64_t>(lo)) : factor_ptr(a, rs);
     float acc[TT];
 #pragma unroll
     for (int t = 0; t < TT; ++t) acc[t] = 0.f;
-    for (uint32_t j = j0 + threadIdx.x; j < j1; j += nthr) {
+    for (uint32_t j = j0 + lane; j < j1; j += 32) {
       const float av = Arow[j];
 #pragma unroll
       for (int t = 0; t < TT; ++t)
@@ -307,21 +449,16 @@ __device__ void shrink_chunk(const DualArgs& a, const DualCfg& c, uint32_t cta, 
     }
 #pragma unroll
     for (int t = 0; t < TT; ++t) {
-      const float s = warp_sum(acc[t]);
-      if (lane == 0) tmp[warp * TT + t] = s;
+      const float v = warp_sum(acc[t]);
+      if (lane == 0 && t < static_cast<int>(a.T)) a.ws.partial[(static_cast<size_t>(t) * a.rtot + rho) * c.gs + cta] = v;
     }
-    named_bar(1, nthr);
-    if (threadIdx.x < a.T) {
-      float s = 0.f;
-      for (uint32_t w = 0; w < ncw; ++w) s += tmp[w * TT + threadIdx.x];
-      a.ws.partial[(static_cast<size_t>(threadIdx.x) * a.rtot + rho) * c.gs + cta] = s;
-    }
-    named_bar(1, nthr);
   }
 }
 
 template <int QUANT, int TT, int RG>
-__global__ void __launch_bounds__(kMaxThreads, 2) k_dualpath(const DualArgs a, const DualCfg c) {
+__global__ void __launch_bounds__(K1Shape<TT, RG>::threads, K1Shape<TT, RG>::min_blocks)
+    k_dualpath(const DualArgs a, const DualCfg c) {
+  constexpr int NREG = K1Shape<TT, RG>::reg_records;
   constexpr bool Q4 = QUANT == OVL_Q4_0;
   constexpr int N = TT * RG;
   constexpr int LN = Log2<N>::v;
@@ -329,19 +466,27 @@ __global__ void __launch_bounds__(kMaxThreads, 2) k_dualpath(const DualArgs a, c
   extern __shared__ __align__(1024) uint8_t sm[];
   uint64_t* full = reinterpret_cast<uint64_t*>(sm);
   uint64_t* empty = full + kMaxNS;
-  volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(sm + 2 * kMaxNS * 8);
+  uint64_t* vbar = empty + kMaxNS;                  // low-rank vector ready
+  volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(vbar + 1);
   uint8_t* rec = sm + c.off_rec;
   uint8_t* stages = sm + c.off_stage;
   float* red = reinterpret_cast<float*>(sm + c.off_red);
   float* vsm = reinterpret_cast<float*>(sm + c.off_v);
   float* tmp = reinterpret_cast<float*>(sm + c.off_tmp);
+  float* sA = reinterpret_cast<float*>(sm + c.off_a);
+  float* sB = reinterpret_cast<float*>(sm + c.off_b);
 
   const uint32_t warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t ncw = c.nwc * c.ng;               // consumer warps
   const uint32_t nthr = ncw * 32;
   const uint32_t G = gridDim.x, cta = blockIdx.x;
-  const uint32_t row0 = static_cast<uint32_t>((static_cast<uint64_t>(cta) * a.m) / G);
-  const uint32_t row1 = static_cast<uint32_t>((static_cast<uint64_t>(cta + 1) * a.m) / G);
+  // this CTA's tensor and its contiguous row slice of that tensor
+  uint32_t si = 0;
+  while (si + 1 < a.nseg && cta >= a.seg[si + 1].g0) ++si;
+  const DualSeg& sg = a.seg[si];
+  const uint32_t lc = cta - sg.g0;
+  const uint32_t row0 = static_cast<uint32_t>((static_cast<uint64_t>(lc) * sg.m) / sg.gn);
+  const uint32_t row1 = static_cast<uint32_t>((static_cast<uint64_t>(lc + 1) * sg.m) / sg.gn);
   const uint32_t nrows = row1 - row0;
   const uint32_t nst = (nrows + RG - 1) / RG;
 
@@ -350,6 +495,7 @@ __global__ void __launch_bounds__(kMaxThreads, 2) k_dualpath(const DualArgs a, c
       mbar_init(&full[i], 1);
       mbar_init(&empty[i], c.nwc);
     }
+    mbar_init(vbar, 1);
     *abort_flag = 0u;
     mbar_fence_init();
   }
@@ -357,9 +503,9 @@ __global__ void __launch_bounds__(kMaxThreads, 2) k_dualpath(const DualArgs a, c
   griddep_launch_dependents();
 
   if (warp == ncw) {
-    // ---------------- producer: stream this CTA's rows in order.  The base is
-    // immutable, so this starts before the preceding grid has finished.
     if (lane == 0) {
+      // ---------------- producer: stream this CTA's rows in order.  The base is
+      // immutable, so this starts before the preceding grid has finished.
       const uint64_t pol = l2_evict_first_policy();
       uint32_t issued = 0;
       for (uint32_t s = 0; s < nst; ++s) {
@@ -378,13 +524,89 @@ __global__ void __launch_bounds__(kMaxThreads, 2) k_dualpath(const DualArgs a, c
         uint8_t* dst = stages + static_cast<size_t>(slot) * c.stage_bytes;
         const uint32_t bq = rows * c.rowbytes;
         mbar_arrive_expect_tx(&full[slot], bq + static_cast<uint32_t>(d1 - d0));
-        bulk_g2s(dst, a.qs + static_cast<size_t>(r0) * c.rowbytes, bq, &full[slot], pol);
-        bulk_g2s(dst + c.stage_q, a.dpl + d0, static_cast<uint32_t>(d1 - d0), &full[slot], pol);
+        bulk_g2s(dst, sg.qs + static_cast<size_t>(r0) * c.rowbytes, bq, &full[slot], pol);
+        bulk_g2s(dst + c.stage_q, sg.dpl + d0, static_cast<uint32_t>(d1 - d0), &full[slot], pol);
         ++issued;
       }
       // Do not leave while copies into this CTA's shared memory may be in flight.
       const uint32_t first = issued > c.ns ? issued - c.ns : 0;
       for (uint32_t s = first; s < issued; ++s) mbar_wait_bounded(&full[s % c.ns], (s / c.ns) & 1);
+    }
+    return;
+  }
+  if (warp == ncw + 1) {
+    // ---------------- helper warp: the low-rank side product, off the critical
+    // path.  Stage this CTA's shrink chunk of A and its B rows, reduce the chunk
+    // against the staged activations, publish the partials with one release
+    // arrival, wait (bounded) for every CTA's arrival, sum the partials in a
+    // fixed order into v and release the epilogue.
+    if (!a.nl) return;
+    if (c.stage_b) {
+      uint32_t rb = 0;
+      for (uint32_t k = sg.k0; k < sg.k1; ++k) {
+        const uint32_t cnt = nrows * a.lora[k].r;
+        const float* src = a.lora[k].B + static_cast<size_t>(row0) * a.lora[k].r;
+        for (uint32_t e = lane; e < cnt; e += 32) cp_async4(sB + nrows * rb + e, src + e);
+        rb += a.lora[k].r;
+      }
+    }
+    if (c.stage_a && cta < c.gs) {
+      uint64_t lo, hi;
+      shrink_bounds(a, c, cta, &lo, &hi);
+      const uint32_t rho_a = static_cast<uint32_t>(lo / a.n), rho_b = static_cast<uint32_t>((hi - 1) / a.n);
+      for (uint32_t rho = rho_a; rho <= rho_b; ++rho) {
+        const uint64_t rs = static_cast<uint64_t>(rho) * a.n;
+        const uint32_t j0 = static_cast<uint32_t>(max(lo, rs) - rs);
+        const uint32_t j1 = static_cast<uint32_t>(min(hi, rs + a.n) - rs);
+        const float* Arow = factor_ptr(a, rs);
+        float* dstA = sA + (static_cast<int64_t>(rs) - static_cast<int64_t>(lo));
+        for (uint32_t j = j0 + lane; j < j1; j += 32) cp_async4(dstA + j, Arow + j);
+      }
+    }
+    cp_async_commit();
+    griddep_wait();
+    cp_async_wait_all();
+    named_bar(2, nthr + 32);                        // the consumers have staged x
+    const void* xsrc = c.stage_x ? static_cast<const void*>(sm + c.off_x) : a.x;
+    if (cta < c.gs) shrink_chunk_warp<TT>(a, c, cta, sA, xsrc, lane);
+    __syncwarp();
+    if (lane == 0) {
+      asm volatile("red.release.gpu.global.add.u64 [%0], 1;" ::"l"(&a.ws.counter[0]) : "memory");
+      uint32_t it = 0;
+      while (ld_acquire_u64(&a.ws.counter[0]) < G) {
+        if (++it > (1u << 22)) {
+          latch(a.ws.status, kDevTimeoutShrink);
+          break;
+        }
+        __nanosleep(32);
+      }
+    }
+    __syncwarp();
+    for (uint32_t i = lane; i < a.T * a.rtot; i += 32) {
+      const uint32_t t = i / a.rtot, rho = i - t * a.rtot;
+      uint32_t cf, cl;
+      partial_range(a, c, rho, &cf, &cl);
+      const float* p = a.ws.partial + (static_cast<size_t>(t) * a.rtot + rho) * c.gs;
+      float sum = 0.f;
+      for (uint32_t q = cf; q <= cl; q += 4) {   // four loads in flight, summed in order
+        float v4[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) v4[u] = (q + u <= cl) ? __ldcg(p + q + u) : 0.f;
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+          if (q + u <= cl) sum += v4[u];
+      }
+      vsm[t * a.rtot + rho] = sum;
+    }
+    __syncwarp();
+    if (lane == 0) {
+      mbar_arrive(vbar);
+      // Last CTA out resets the arrival counters for the next launch.
+      const unsigned long long old = atomicAdd(&a.ws.counter[1], 1ull);
+      if (old == G - 1) {
+        atomicExch(&a.ws.counter[0], 0ull);
+        atomicExch(&a.ws.counter[1], 0ull);
+      }
     }
     return;
   }
@@ -394,25 +616,6 @@ __global__ void __launch_bounds__(kMaxThreads, 2) k_dualpath(const DualArgs a, c
   const uint32_t cw = warp - grp * c.nwc;           // column warp inside the group
   const uint32_t L = cw * 32 + lane;                // column lane: blocks L, L + ncol, ...
   const uint32_t ncol = c.nwc * 32;
-  float* sA = reinterpret_cast<float*>(sm + c.off_a);
-  float* sB = reinterpret_cast<float*>(sm + c.off_b);
-  // 0. immutable low-rank operands into shared memory while the preceding grid
-  //    may still run: this CTA's B rows of every term and its shrink chunk of A.
-  if (a.nl && c.stage_b) {
-    uint32_t rb = 0;
-    for (uint32_t k = 0; k < a.nl; ++k) {
-      const uint32_t cnt = nrows * a.lora[k].r;
-      const float* src = a.lora[k].B + static_cast<size_t>(row0) * a.lora[k].r;
-      for (uint32_t e = threadIdx.x; e < cnt; e += nthr) cp_async4(sB + nrows * rb + e, src + e);
-      rb += a.lora[k].r;
-    }
-  }
-  if (a.nl && c.stage_a && cta < c.gs) {
-    uint64_t lo, hi;
-    shrink_bounds(a, c, cta, &lo, &hi);
-    for (uint64_t f = lo + threadIdx.x; f < hi; f += nthr) cp_async4(sA + (f - lo), factor_ptr(a, f));
-  }
-  cp_async_commit();
   griddep_wait();  // x, y and the workspace may be touched by the preceding grid
   const void* xsrc = a.x;
   if (c.stage_x) {
@@ -425,26 +628,26 @@ __global__ void __launch_bounds__(kMaxThreads, 2) k_dualpath(const DualArgs a, c
       for (uint32_t e = threadIdx.x * 4; e < xbytes; e += nthr * 4) cp_async4(sX + e, gx + e);
     }
     cp_async_commit();
+    cp_async_wait_all();
     xsrc = sX;
   }
-  cp_async_wait_all();
-  named_bar(1, nthr);
+  named_bar(2, nthr + (a.nl ? 32u : 0u));          // x staged (the helper warp reads it too)
 
-  // 1. activation records for the tokens of this launch
-  prep_records<Q4>(rec, a, xsrc, c.nb, warp, ncw, lane);
-  // 2. low-rank shrink partials, published with one arrival per CTA
-  if (a.nl) shrink_chunk<TT>(a, c, cta, tmp, sA, xsrc, warp, lane, ncw);
-  named_bar(1, nthr);
-  if (a.nl && threadIdx.x == 0) {
-    __threadfence();
-    atomicAdd(&a.ws.counter[0], 1ull);
+  // 1. activation records.  Single-token launches build each lane's first NREG
+  //    records in registers; any further blocks (and multi-token launches) use
+  //    records built cooperatively in shared memory.
+  if (TT > 1 || c.bpl > static_cast<uint32_t>(NREG)) {
+    prep_records<Q4>(rec, a, xsrc, c.stage_x != 0, c.nb, warp, ncw, lane);
+    named_bar(1, nthr);
   }
-  // single-token launches keep the lane's first record in registers
-  uint4 rreg[7];
-  if (TT == 1 && L < c.nb) {
-    const uint4* rp = reinterpret_cast<const uint4*>(rec + static_cast<size_t>(L) * kRecBytes);
+  uint4 rreg[NREG][7];
+  if (TT == 1) {
 #pragma unroll
-    for (int i = 0; i < 7; ++i) rreg[i] = rp[i];
+    for (int k = 0; k < NREG; ++k) {
+      const uint32_t b = L + k * ncol;
+      if (k < static_cast<int>(c.bpl) && b < c.nb)
+        lane_record<Q4>(rreg[k], xsrc, a.xdt, c.stage_x != 0, static_cast<size_t>(b) * 32);
+    }
   }
 
   // 3. stream the base rows
@@ -475,8 +678,14 @@ __global__ void __launch_bounds__(kMaxThreads, 2) k_dualpath(const DualArgs a, c
         acc[t * RG + rr] = fmaf(d * xs, P, acc[t * RG + rr]);
       }
     };
-    if (TT == 1 && L < c.nb) block(L, rreg, 0);
-    for (uint32_t k = (TT == 1 ? 1u : 0u); k < c.bpl; ++k) {
+    if (TT == 1) {
+#pragma unroll
+      for (int k = 0; k < NREG; ++k) {
+        const uint32_t b = L + k * ncol;
+        if (k < static_cast<int>(c.bpl) && b < c.nb) block(b, rreg[k], 0);
+      }
+    }
+    for (uint32_t k = (TT == 1 ? static_cast<uint32_t>(NREG) : 0u); k < c.bpl; ++k) {
       const uint32_t b = L + k * ncol;
       if (b < c.nb) {
 #pragma unroll
@@ -502,49 +711,10 @@ __global__ void __launch_bounds__(kMaxThreads, 2) k_dualpath(const DualArgs a, c
     }
   }
   named_bar(1, nthr);
-
-  // 4. low-rank vector v = A x (sum of the published partials, fixed order)
-  if (a.nl) {
-    if (threadIdx.x == 0) {
-      uint32_t it = 0;
-      while (ld_acquire_u64(&a.ws.counter[0]) < G) {
-        if (++it > (1u << 22)) {
-          latch(a.ws.status, kDevTimeoutShrink);
-          break;
-        }
-        __nanosleep(64);
-      }
-    }
-    named_bar(1, nthr);
-    const uint64_t total = static_cast<uint64_t>(a.rtot) * a.n;
-    for (uint32_t i = threadIdx.x; i < a.T * a.rtot; i += nthr) {
-      const uint32_t t = i / a.rtot, rho = i - t * a.rtot;
-      uint64_t cf = ((static_cast<uint64_t>(rho) * a.n + 1) * c.gs + total - 1) / total;
-      uint64_t cl = ((static_cast<uint64_t>(rho + 1) * a.n) * c.gs + total - 1) / total;
-      cf = cf ? cf - 1 : 0;
-      cl = cl ? cl - 1 : 0;
-      if (cl > c.gs - 1) cl = c.gs - 1;
-      const float* p = a.ws.partial + (static_cast<size_t>(t) * a.rtot + rho) * c.gs;
-      float s = 0.f;
-      for (uint64_t q = cf; q <= cl; q += 4) {   // four loads in flight, summed in order
-        float v4[4];
-#pragma unroll
-        for (int u = 0; u < 4; ++u) v4[u] = (q + u <= cl) ? __ldcg(p + q + u) : 0.f;
-#pragma unroll
-        for (int u = 0; u < 4; ++u)
-          if (q + u <= cl) s += v4[u];
-      }
-      vsm[t * a.rtot + rho] = s;
-    }
-    named_bar(1, nthr);
-    if (threadIdx.x == 0) {
-      // Last CTA out resets the arrival counters for the next launch.
-      const unsigned long long old = atomicAdd(&a.ws.counter[1], 1ull);
-      if (old == G - 1) {
-        atomicExch(&a.ws.counter[0], 0ull);
-        atomicExch(&a.ws.counter[1], 0ull);
-      }
-    }
+  // 4. the low-rank vector from the producer warp (bounded wait)
+  if (a.nl && !mbar_wait_bounded(vbar, 0)) {
+    latch(a.ws.status, kDevTimeoutShrink);
+    ok = false;
   }
 
   // 5. epilogue, one output per thread: y = base + sum_k s_k (B_k v_k)
@@ -554,14 +724,15 @@ __global__ void __launch_bounds__(kMaxThreads, 2) k_dualpath(const DualArgs a, c
     const uint32_t row = row0 + lr;
     float yv = 0.f;
     for (uint32_t w = 0; w < c.nwc; ++w) yv += red[(w * TT + t) * c.rows_max + lr];
-    uint32_t rbase = 0;
-    for (uint32_t k = 0; k < a.nl; ++k) {
+    uint32_t rbase = sg.rb0, rbl = 0;   // global and tensor-local rank offsets
+    for (uint32_t k = sg.k0; k < sg.k1; ++k) {
       const uint32_t r = a.lora[k].r;
       if (a.tok_sel && a.tok_term[t] != static_cast<int>(k)) {   // segmented: one term per token
         rbase += r;
+        rbl += r;
         continue;
       }
-      const float* Brow = c.stage_b ? sB + nrows * rbase + lr * r : a.lora[k].B + static_cast<size_t>(row) * r;
+      const float* Brow = c.stage_b ? sB + nrows * rbl + lr * r : a.lora[k].B + static_cast<size_t>(row) * r;
       const float* vv = vsm + t * a.rtot + rbase;
       float dot = 0.f;
       for (uint32_t tau = 0; tau < r; tau += 8) {   // eight loads in flight, summed in order
@@ -574,8 +745,9 @@ __global__ void __launch_bounds__(kMaxThreads, 2) k_dualpath(const DualArgs a, c
       }
       yv = fmaf(a.lora[k].s, dot, yv);
       rbase += r;
+      rbl += r;
     }
-    a.y[static_cast<size_t>(t) * a.m + row] = yv;
+    sg.y[static_cast<size_t>(t) * sg.m + row] = yv;
   }
 }
 
@@ -584,9 +756,9 @@ using KernelFn = void (*)(const DualArgs, const DualCfg);
 KernelFn pick(uint32_t quant, int tt, int rg) {
 #define OVL_K(Q, T_, R_) \
   if (quant == Q && tt == T_ && rg == R_) return k_dualpath<Q, T_, R_>;
-  OVL_K(OVL_Q8_0, 1, 1) OVL_K(OVL_Q8_0, 1, 2) OVL_K(OVL_Q8_0, 1, 4) OVL_K(OVL_Q8_0, 1, 8)
+  OVL_K(OVL_Q8_0, 1, 2) OVL_K(OVL_Q8_0, 1, 4) OVL_K(OVL_Q8_0, 1, 8)
   OVL_K(OVL_Q8_0, 2, 2) OVL_K(OVL_Q8_0, 4, 2) OVL_K(OVL_Q8_0, 8, 2)
-  OVL_K(OVL_Q4_0, 1, 1) OVL_K(OVL_Q4_0, 1, 2) OVL_K(OVL_Q4_0, 1, 4) OVL_K(OVL_Q4_0, 1, 8)
+  OVL_K(OVL_Q4_0, 1, 2) OVL_K(OVL_Q4_0, 1, 4) OVL_K(OVL_Q4_0, 1, 8)
   OVL_K(OVL_Q4_0, 2, 2) OVL_K(OVL_Q4_0, 4, 2) OVL_K(OVL_Q4_0, 8, 2)
 #undef OVL_K
   return nullptr;
@@ -606,9 +778,9 @@ int device_sms() {
 // which then prefetches its weights while this grid drains.
 constexpr uint32_t kSoftBudget = OVL_K1_SOFT_KB * 1024;
 
-bool plan(DualCfg& c, const DualArgs& a, int tt, int rg, uint32_t G) {
-  c.rows_max = (a.m + G - 1) / G;
-  uint32_t off = round_up(2 * kMaxNS * 8 + 16, 256);   // mbarriers + abort flag
+bool plan(DualCfg& c, const DualArgs& a, int tt, int rg, uint32_t rows_max) {
+  c.rows_max = rows_max;
+  uint32_t off = round_up(2 * kMaxNS * 8 + 8 + 16, 256);   // mbarriers + abort flag
   c.off_rec = off;
   off = round_up(off + tt * c.nb * kRecBytes, 128);
   c.off_red = off;
@@ -616,7 +788,7 @@ bool plan(DualCfg& c, const DualArgs& a, int tt, int rg, uint32_t G) {
   c.off_v = off;
   off = round_up(off + tt * a.rtot * 4 + 4, 128);
   c.off_tmp = off;
-  off = round_up(off + c.nwc * c.ng * tt * 4, 128);
+  off = round_up(off + c.nwc * c.ng * 4 * tt * 4, 128);
   c.off_x = off;
   if (c.stage_x) off = round_up(off + tt * a.n * (a.xdt == OVL_BF16 ? 2 : 4), 128);
   c.off_a = off;
@@ -647,8 +819,14 @@ bool plan(DualCfg& c, const DualArgs& a, int tt, int rg, uint32_t G) {
 
 }  // namespace
 
-cudaError_t launch_dualpath(const DualArgs& a0, cudaStream_t st) {
-  if (a0.T == 0 || a0.m == 0) return cudaSuccess;
+cudaError_t launch_dualpath(const DualArgs& a_in, cudaStream_t st) {
+  if (a_in.T == 0 || a_in.m == 0) return cudaSuccess;
+  DualArgs a0 = a_in;
+  if (a0.nseg == 0) {
+    a0.nseg = 1;
+    a0.seg[0] = DualSeg{a0.qs, a0.dpl, a0.y, a0.m, 0, 0, 0, a0.nl, 0};
+  }
+  if (a0.nseg > static_cast<uint32_t>(kMaxMulti)) return cudaErrorInvalidValue;
   static int nsm = device_sms();
   DualCfg c{};
   c.nb = a0.n / kQK;
@@ -664,21 +842,42 @@ cudaError_t launch_dualpath(const DualArgs& a0, cudaStream_t st) {
   }
   c.nwc = best_w;
   c.bpl = best_b;
-  c.ng = std::max<uint32_t>(1, std::min<uint32_t>(OVL_K1_MAX_GROUPS, 8 / c.nwc));
+
   // token tile
   int tt = 1;
   const uint32_t Tneed = a0.T < 8 ? a0.T : 8;
   while (tt < static_cast<int>(Tneed)) tt *= 2;
   while (tt > 1 && tt * c.nb * kRecBytes > kRecBudget) tt /= 2;
   int rg = 2;
-  if (tt == 1) {
-    rg = 1;
+  if (tt == 1)
     while (rg < 8 && 2 * rg * c.rowbytes <= OVL_K1_STAGE_BYTES) rg *= 2;
-  }
+  const uint32_t max_cw = rg <= 2 ? kMaxThreadsWide / 32 - 2 : kMaxThreads / 32 - 2;
+  c.ng = std::max<uint32_t>(1, std::min<uint32_t>(OVL_K1_MAX_GROUPS, max_cw / c.nwc));
   KernelFn fn = pick(a0.quant, tt, rg);
   if (!fn) return cudaErrorInvalidValue;
   const uint32_t G = std::min<uint32_t>(static_cast<uint32_t>(nsm), a0.m);
-  c.gs = a0.nl ? static_cast<uint32_t>(std::min<uint64_t>(G, static_cast<uint64_t>(a0.rtot) * a0.n)) : 0;
+  if (G < a0.nseg) return cudaErrorInvalidValue;
+  // CTAs per tensor in proportion to its rows (at least one, at most one per row)
+  {
+    uint32_t left = G;
+    for (uint32_t i = 0; i < a0.nseg; ++i) {
+      const uint32_t rest = a0.nseg - 1 - i;
+      uint32_t gn = static_cast<uint32_t>((static_cast<uint64_t>(G) * a0.seg[i].m + a0.m / 2) / a0.m);
+      gn = std::max<uint32_t>(1, std::min<uint32_t>(gn, a0.seg[i].m));
+      gn = std::min<uint32_t>(gn, left - rest);
+      if (i + 1 == a0.nseg) gn = std::min<uint32_t>(left, a0.seg[i].m);
+      a0.seg[i].g0 = G - left;
+      a0.seg[i].gn = gn;
+      left -= gn;
+    }
+  }
+  uint32_t G_used = 0, rows_max = 1;
+  for (uint32_t i = 0; i < a0.nseg; ++i) {
+    G_used += a0.seg[i].gn;
+    rows_max = std::max<uint32_t>(rows_max, (a0.seg[i].m + a0.seg[i].gn - 1) / a0.seg[i].gn);
+  }
+  c.gs = a0.nl ? static_cast<uint32_t>(std::min<uint64_t>(G_used, static_cast<uint64_t>(a0.rtot) * a0.n)) : 0;
+  c.div32 = static_cast<uint64_t>(a0.rtot) * a0.n * (static_cast<uint64_t>(c.gs) + 1) < (1ull << 32);
   if (a0.nl && static_cast<size_t>(tt) * a0.rtot * c.gs > a0.ws.partial_floats) return cudaErrorInvalidValue;
   // operands staged in shared memory when small (immutable ones before the
   // grid dependency resolves, activations right after)
@@ -686,12 +885,11 @@ cudaError_t launch_dualpath(const DualArgs& a0, cudaStream_t st) {
   const uintptr_t xa = reinterpret_cast<uintptr_t>(a0.x);
   const bool x_small = static_cast<uint64_t>(tt) * a0.n * esz_x <= 32768;
   c.stage_x = !x_small ? 0 : (xa % 16 == 0 ? 16 : (xa % 4 == 0 ? 4 : 0));
-  const uint32_t rows_max = (a0.m + G - 1) / G;
   c.stage_b = a0.nl && static_cast<uint64_t>(rows_max) * a0.rtot * 4 <= 32768;
   c.stage_a = a0.nl && (static_cast<uint64_t>(a0.rtot) * a0.n / std::max<uint32_t>(c.gs, 1) + 2) * 4 <= 32768;
-  if (!plan(c, a0, tt, rg, G)) return cudaErrorInvalidConfiguration;
+  if (!plan(c, a0, tt, rg, rows_max)) return cudaErrorInvalidConfiguration;
   if (c.ns % c.ng != 0 || c.ns > static_cast<uint32_t>(kMaxNS)) return cudaErrorInvalidConfiguration;
-  const uint32_t threads = (c.nwc * c.ng + 1) * 32;
+  const uint32_t threads = (c.nwc * c.ng + 2) * 32;   // consumers + producer + helper
   // one attribute / occupancy query per (kernel, shared-memory size)
   struct Seen { KernelFn fn; uint32_t smem; int occ; };
   static std::mutex mu;
@@ -718,11 +916,11 @@ cudaError_t launch_dualpath(const DualArgs& a0, cudaStream_t st) {
     DualArgs a = a0;
     a.T = std::min<uint32_t>(tt, a0.T - t0);
     a.x = static_cast<const uint8_t*>(a0.x) + static_cast<size_t>(t0) * a0.n * esz;
-    a.y = a0.y + static_cast<size_t>(t0) * a0.m;
+    for (uint32_t i = 0; i < a0.nseg; ++i) a.seg[i].y = a0.seg[i].y + static_cast<size_t>(t0) * a0.seg[i].m;
     if (a0.tok_sel)
       for (uint32_t t = 0; t < 8; ++t) a.tok_term[t] = (t0 + t < a0.T) ? a0.tok_host[t0 + t] : -1;
     cudaLaunchConfig_t cfg{};
-    cfg.gridDim = dim3(G);
+    cfg.gridDim = dim3(G_used);
     cfg.blockDim = dim3(threads);
     cfg.dynamicSmemBytes = c.smem;
     cfg.stream = st;
@@ -730,7 +928,7 @@ cudaError_t launch_dualpath(const DualArgs& a0, cudaStream_t st) {
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = OVL_K1_PDL;
     e = cudaLaunchKernelEx(&cfg, fn, a, c);
     if (e != cudaSuccess) return e;
   }

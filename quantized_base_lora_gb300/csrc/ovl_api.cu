@@ -709,6 +709,57 @@ ovl_status ovl_linear_forward(ovl_ctx* ctx, uint32_t tensor, const void* x, uint
   return ok(ctx);
 }
 
+ovl_status ovl_linear_forward_multi(ovl_ctx* ctx, uint32_t n, const uint32_t* tensors, const void* x,
+                                    uint32_t x_dtype, uint32_t T, float* const* ys, void* stream) {
+  if (!ctx) return OVL_E_ARG;
+  std::lock_guard<std::mutex> lk(ctx->mu);
+  if (!ctx->base_loaded) return fail(ctx, OVL_E_STATE, "no base loaded");
+  if (n == 0 || n > static_cast<uint32_t>(kMaxMulti) || !tensors || !ys) return fail(ctx, OVL_E_ARG, "need 1 to 4 tensors");
+  if (x_dtype != OVL_F32 && x_dtype != OVL_BF16) return fail(ctx, OVL_E_ARG, "unknown activation dtype");
+  if (T > OVL_MAX_T) return fail(ctx, OVL_E_ARG, "T exceeds OVL_MAX_T");
+  if (ctx->active->mode != OVL_MODE_STACK) return fail(ctx, OVL_E_STATE, "TABLE composition: use ovl_segmented_forward");
+  for (uint32_t i = 0; i < n; ++i) {
+    if (tensors[i] >= ctx->tensors.size()) return fail(ctx, OVL_E_ARG, "no such tensor");
+    if (ctx->tensors[tensors[i]].d_in != ctx->tensors[tensors[0]].d_in)
+      return fail(ctx, OVL_E_SHAPE, "tensors of one launch must share d_in");
+    if (T && !ys[i]) return fail(ctx, OVL_E_ARG, "null output");
+  }
+  if (T == 0) return ok(ctx);
+  if (!x) return fail(ctx, OVL_E_ARG, "null activation");
+  DeviceGuard g(ctx->device);
+  DualArgs a{};
+  std::vector<Adapter*> used;
+  for (uint32_t i = 0; i < n; ++i) {
+    const ovl_tensor_desc& td = ctx->tensors[tensors[i]];
+    LoraRef terms[OVL_MAX_STACK];
+    uint32_t rt;
+    const uint32_t nl = stack_terms(ctx, *ctx->active, tensors[i], terms, &rt, &used);
+    DualSeg& sgm = a.seg[i];
+    sgm.qs = ctx->base + td.qs_off;
+    sgm.dpl = ctx->base + td.d_off;
+    sgm.y = ys[i];
+    sgm.m = td.d_out;
+    sgm.k0 = a.nl;
+    sgm.rb0 = a.rtot;
+    for (uint32_t k = 0; k < nl; ++k) a.lora[a.nl++] = terms[k];
+    sgm.k1 = a.nl;
+    a.rtot += rt;
+    a.m += td.d_out;
+  }
+  a.nseg = n;
+  a.n = ctx->tensors[tensors[0]].d_in;
+  a.quant = ctx->quant;
+  a.x = x;
+  a.xdt = x_dtype;
+  a.T = T;
+  a.ws = ctx->ws;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e = launch_dualpath(a, st);
+  if (e != cudaSuccess) return cuda_fail(ctx, e, "multi-tensor launch");
+  if (ovl_status s = record_use(ctx, used, st)) return s;
+  return ok(ctx);
+}
+
 ovl_status ovl_segmented_forward(ovl_ctx* ctx, uint32_t tensor, const void* x, uint32_t x_dtype, uint32_t T,
                                  const int32_t* seg_offsets, const int32_t* seg_slot, uint32_t n_seg,
                                  const int32_t* perm, float* y, void* stream) {

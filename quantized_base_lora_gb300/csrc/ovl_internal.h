@@ -37,7 +37,24 @@ struct Workspace {
   size_t partial_floats;
 };
 
-// Fused dual-path forward of one tensor over a token chunk (T <= 8).
+// One tensor of a (multi-tensor) dual-path launch.  All tensors of a launch
+// share d_in and the activations; CTAs [g0, g0 + gn) of the grid serve this
+// tensor, and its low-rank terms are lora[k0, k1) (rank offset rb0 in the
+// flattened shrink space).  Filled by the launcher.
+struct DualSeg {
+  const uint8_t* qs;
+  const uint8_t* dpl;
+  float* y;
+  uint32_t m;
+  uint32_t g0, gn;
+  uint32_t k0, k1, rb0;
+};
+
+constexpr int kMaxMulti = 4;
+
+// Fused dual-path forward over a token chunk (T <= 8).  Single-tensor callers
+// fill qs/dpl/m/y; multi-tensor callers fill nseg and seg[] (qs, dpl, y, m,
+// k0, k1, rb0) and leave m = total rows.
 struct DualArgs {
   const uint8_t* qs;      // qs plane
   const uint8_t* dpl;     // d plane (binary16)
@@ -53,6 +70,8 @@ struct DualArgs {
   uint32_t tok_sel;
   int8_t tok_term[8];           // this launch's slice (filled by the launcher)
   const int8_t* tok_host;       // host array of T entries (launcher only)
+  uint32_t nseg;                // 0: single tensor (qs/dpl/m/y); else seg[0..nseg)
+  DualSeg seg[kMaxMulti];
   Workspace ws;
 };
 

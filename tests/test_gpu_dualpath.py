@@ -209,7 +209,37 @@ def test_activation_scale_extremes_stay_within_bound():
     x[1, 32:64] *= np.float32(1e-30)                  # tiny block
     x[2, 64:96] *= np.float32(1e20)                   # huge block
     x[3, ::7] *= np.float32(1e-6)                     # mixed magnitudes inside blocks
+    x[3, 96:128] *= np.float32(1e-35)                 # below 2^-104: the block is flushed to zero
     xd, x64 = x_device(x, "f32")
     y = fwd(rt, 0, xd)
     assert_within_bound(y, deq_of(base, 0), [], x64, "extremes")
     rt.close()
+
+
+# ----------------------------------------------------------------- multi-tensor launches
+@pytest.mark.parametrize("T", [1, 3])
+def test_multi_tensor_launch_qkv_and_gate_up(block_q8, T):
+    import quantized_base_lora_gb300 as q
+    base, ad, rt = block_q8
+    for group in ([0, 1, 2], [4, 5]):
+        x = S.activations(T, 4096, seed=5000 + T)
+        xd, x64 = x_device(x, "bf16")
+        ys = [torch.full((T, base.tensors[i].d_out), float("nan"), device="cuda") for i in group]
+        st = q.ovl_linear_forward_multi(rt.ctx, group, xd.data_ptr(), q.OVL_BF16, T, [y.data_ptr() for y in ys],
+                                        int(torch.cuda.current_stream().cuda_stream))
+        torch.cuda.synchronize()
+        assert st == 0 and rt.check_device() == 0
+        for i, y in zip(group, ys):
+            assert_within_bound(y.cpu().numpy(), deq_of(base, i), lora_terms([(ad, 2.0)], i), x64,
+                                f"multi {S.PROJ[i]} T={T}")
+
+
+def test_multi_tensor_launch_rejects_mixed_d_in(block_q8):
+    import quantized_base_lora_gb300 as q
+    base, ad, rt = block_q8
+    xd = torch.zeros((1, 4096), device="cuda")
+    ys = [torch.zeros((1, 4096), device="cuda") for _ in range(2)]
+    st = q.ovl_linear_forward_multi(rt.ctx, [0, 6], xd.data_ptr(), q.OVL_F32, 1, [y.data_ptr() for y in ys])
+    assert st == q.OVL_E_SHAPE
+    st = q.ovl_linear_forward_multi(rt.ctx, [0, 1, 2, 3, 4], xd.data_ptr(), q.OVL_F32, 1, [ys[0].data_ptr()] * 5)
+    assert st == q.OVL_E_ARG
