@@ -284,7 +284,7 @@ ovl_status ovl_segmented_forward(ovl_ctx* ctx, uint32_t tensor, const void* x, u
  * call allocates nothing and calls no allocating routine.  The first call on a
  * device looks up the array's address and clears it (synchronizing the device),
  * so make that first call before any stream capture.  Every call clears the
- * array's status word and counters on `stream` and then reuses its contents;
+ * array's status word on `stream` and then reuses its contents;
  * calls that overlap on the GPU (different streams, or other threads) race on
  * the array and must be serialized by the caller.
  * Errors: OVL_E_QUANT, OVL_E_SHAPE (d_in, alignment, rank, total rank), OVL_E_ARG

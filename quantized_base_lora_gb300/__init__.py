@@ -228,15 +228,14 @@ def ovl_rollback(ctx):
 def ovl_linear_forward(ctx, tensor: int, x_ptr: int, x_dtype: int, T: int, y_ptr: int,
                        path: int = OVL_PATH_DUAL, scratch_ptr: int = 0, scratch_bytes: int = 0,
                        stream: int = 0) -> int:
-    return lib.ovl_linear_forward(ctx, int(tensor), C.c_void_p(x_ptr), int(x_dtype), int(T), C.c_void_p(y_ptr),
-                                  int(path), C.c_void_p(scratch_ptr), int(scratch_bytes), C.c_void_p(stream))
+    return lib.ovl_linear_forward(ctx, int(tensor), int(x_ptr), int(x_dtype), int(T), int(y_ptr), int(path),
+                                  int(scratch_ptr), int(scratch_bytes), int(stream))
 
 
 def ovl_linear_forward_multi(ctx, tensors, x_ptr: int, x_dtype: int, T: int, y_ptrs, stream: int = 0) -> int:
     n = len(tensors)
-    ys = (C.c_void_p * max(n, 1))(*[C.c_void_p(p) for p in y_ptrs])
-    return lib.ovl_linear_forward_multi(ctx, n, _u32s(tensors), C.c_void_p(x_ptr), int(x_dtype), int(T), ys,
-                                        C.c_void_p(stream))
+    return lib.ovl_linear_forward_multi(ctx, n, (C.c_uint32 * n)(*tensors), int(x_ptr), int(x_dtype), int(T),
+                                        (C.c_void_p * n)(*map(int, y_ptrs)), int(stream))
 
 
 def ovl_materialize_layer(ctx, tensor: int, scratch_ptr: int, scratch_bytes: int, stream: int = 0) -> int:

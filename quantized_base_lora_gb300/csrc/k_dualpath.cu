@@ -45,8 +45,8 @@ constexpr int kRecBytes = 112;  // per (token, block) activation record: 7 x 16 
 #ifndef OVL_K1_MAX_NS
 #define OVL_K1_MAX_NS 8
 #endif
-#ifndef OVL_K1_SOFT_KB
-#define OVL_K1_SOFT_KB 112
+#ifndef OVL_K1_SOFT_BYTES
+#define OVL_K1_SOFT_BYTES (113 * 1024)
 #endif
 #ifndef OVL_K1_STAGE_BYTES
 #define OVL_K1_STAGE_BYTES 16384
@@ -59,19 +59,19 @@ constexpr int kRecBytes = 112;  // per (token, block) activation record: 7 x 16 
 #endif
 constexpr int kMaxNS = OVL_K1_MAX_NS;
 constexpr int kMaxThreads = 10 * 32;       // up to 8 consumer warps + producer + helper
-constexpr int kMaxThreadsWide = 16 * 32;   // wide rows: up to 14 consumer warps, one CTA per SM
 
-// Variants that stream at most two rows per stage serve wide rows (d_in >= 8K
-// for q8_0): they run one CTA per SM with more warps and keep two activation
-// records per lane in registers.  The others run two CTAs per SM, so the next
-// launch's CTA can be resident (and prefetching) while this one drains.
+// Every variant fits two CTAs per SM (registers, and shared memory for the
+// plans under the soft budget), so a CTA of the next launch is resident and
+// streaming its weights while this grid drains.  Variants that stream at most
+// two rows per stage serve wide rows (d_in >= 8K for q8_0) and keep two
+// activation records per lane in registers.
 template <int TT, int RG>
 struct K1Shape {
-  static constexpr bool wide = RG <= 2;
-  static constexpr int threads = wide ? kMaxThreadsWide : kMaxThreads;
-  static constexpr int min_blocks = wide ? 1 : 2;
-  static constexpr int reg_records = (wide && TT == 1) ? 2 : 1;
+  static constexpr int threads = kMaxThreads;
+  static constexpr int min_blocks = 2;
+  static constexpr int reg_records = (RG <= 2 && TT == 1) ? 2 : 1;
 };
+constexpr uint32_t reg_records_of(int tt, int rg) { return (rg <= 2 && tt == 1) ? 2u : 1u; }
 constexpr uint32_t kRecBudget = 128 * 1024;
 constexpr uint32_t kSmemBudget = 220 * 1024;
 
@@ -86,10 +86,13 @@ struct DualCfg {
   uint32_t stage_bytes;  // stride between stages
   uint32_t rows_max;     // rows of the largest CTA slice
   uint32_t gs;           // CTAs that reduce a shrink chunk
-  uint32_t off_rec, off_stage, off_red, off_v, off_tmp;
-  uint32_t off_x, off_a, off_b;  // staged activations, shrink chunk, B rows
+  uint32_t off_rec, off_stage, off_red, off_v, off_ep;
+  uint32_t off_x, off_a, off_xw;  // staged activations, shrink chunk of A, x window
   uint32_t stage_x;              // 0: x read from global; 4 or 16: cp.async granule
-  uint32_t stage_a, stage_b;     // 1: operand staged in shared memory
+  uint32_t xvec;                 // 1: x (staged or global) allows 16-byte vector loads
+  uint32_t stage_a;              // 1: the shrink chunk of A is staged in shared memory
+  uint32_t xwin;                 // >0: the helper stages the x window of its chunk (capacity, elements)
+  uint32_t b_ring;               // 1: B rows arrive as one ring stage after the last base stage
   uint32_t div32;                // 1: rtot * n * gs < 2^32, chunk arithmetic fits 32 bits
   uint32_t smem;
 };
@@ -423,15 +426,48 @@ __device__ __forceinline__ void partial_range(const DualArgs& a, const DualCfg& 
   *cl = l > c.gs - 1 ? c.gs - 1 : l;
 }
 
+// The part of x that a shrink chunk [lo, hi) of the flattened factor space
+// touches (x index j = f mod n), widened to 16-byte granules of g elements:
+// piece 1 = x[w0, w1), then, when the chunk wraps past the end of a row,
+// piece 2 = x[0, w2).  A chunk of n or more elements takes the whole of x.
+struct XWindow {
+  uint32_t w0, w1, w2;
+};
+__device__ __forceinline__ XWindow x_window(uint64_t lo, uint64_t hi, uint32_t n, uint32_t g) {
+  if (hi - lo >= n) return XWindow{0u, n, 0u};
+  const uint32_t j0 = static_cast<uint32_t>(lo % n);
+  const uint32_t je = j0 + static_cast<uint32_t>(hi - lo);
+  const uint32_t w0 = j0 / g * g;
+  if (je <= n) return XWindow{w0, min(n, (je + g - 1) / g * g), 0u};
+  return XWindow{w0, n, (je - n + g - 1) / g * g};
+}
+__device__ __forceinline__ uint32_t x_window_index(const XWindow& w, uint32_t j) {
+  return j >= w.w0 ? j - w.w0 : (w.w1 - w.w0) + j;
+}
+
+// One low-rank term of this CTA's tensor, copied from the kernel parameters
+// into shared memory at the start so that the B stage and the epilogue do not
+// wait on constant-cache misses.  `here` = byte offset of this CTA's first B
+// row inside the B stage.
+struct EpTerm {
+  const float* B;
+  uint32_t r;
+  float s;
+  uint32_t here;
+  uint32_t pad;
+};
+
 // Partial shrink sums of this CTA's chunk of the flattened [rtot][n] factor
-// space, computed by one warp: partial[(t * rtot + rho) * gs + cta] =
-// sum_{j in chunk, row rho} A[rho][j] x[t][j] (lane-strided, fixed-order
-// warp reduction).
+// space, computed by one warp: slot (t * rtot + rho) * gs + cta receives
+// sum_{j in chunk, row rho} A[rho][j] x[t][j] (lane-strided, fixed-order warp
+// reduction), tagged with the launch epoch in one 64-bit store.  With `xw`
+// set, x comes from the staged window (single token) instead of `xsrc`.
 template <int TT>
 __device__ void shrink_chunk_warp(const DualArgs& a, const DualCfg& c, uint32_t cta, const float* sA,
-                                  const void* xsrc, uint32_t lane) {
+                                  const void* xsrc, const void* xw, const XWindow& win, uint32_t lane) {
   uint64_t lo, hi;
   shrink_bounds(a, c, cta, &lo, &hi);
+  unsigned long long* slots = reinterpret_cast<unsigned long long*>(a.ws.partial);
   const uint32_t rho_a = static_cast<uint32_t>(lo / a.n), rho_b = static_cast<uint32_t>((hi - 1) / a.n);
   for (uint32_t rho = rho_a; rho <= rho_b; ++rho) {
     const uint64_t rs = static_cast<uint64_t>(rho) * a.n;
@@ -441,18 +477,110 @@ __device__ void shrink_chunk_warp(const DualArgs& a, const DualCfg& c, uint32_t 
     float acc[TT];
 #pragma unroll
     for (int t = 0; t < TT; ++t) acc[t] = 0.f;
-    for (uint32_t j = j0 + lane; j < j1; j += 32) {
-      const float av = Arow[j];
+    if (TT == 1) {
+      // eight independent chains, combined in a fixed order
+      float c8[8];
 #pragma unroll
-      for (int t = 0; t < TT; ++t)
-        if (t < static_cast<int>(a.T)) acc[t] = fmaf(av, load_x(xsrc, a.xdt, static_cast<size_t>(t) * a.n + j), acc[t]);
+      for (int u = 0; u < 8; ++u) c8[u] = 0.f;
+      for (uint32_t j = j0 + lane; j < j1; j += 256) {
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const uint32_t jj = j + 32 * u;
+          if (jj < j1) {
+            const float xv = xw ? load_x(xw, a.xdt, x_window_index(win, jj)) : load_x(xsrc, a.xdt, jj);
+            c8[u] = fmaf(Arow[jj], xv, c8[u]);
+          }
+        }
+      }
+      acc[0] = ((c8[0] + c8[1]) + (c8[2] + c8[3])) + ((c8[4] + c8[5]) + (c8[6] + c8[7]));
+    } else {
+      for (uint32_t j = j0 + lane; j < j1; j += 32) {
+        const float av = Arow[j];
+#pragma unroll
+        for (int t = 0; t < TT; ++t)
+          if (t < static_cast<int>(a.T)) acc[t] = fmaf(av, load_x(xsrc, a.xdt, static_cast<size_t>(t) * a.n + j), acc[t]);
+      }
     }
 #pragma unroll
     for (int t = 0; t < TT; ++t) {
       const float v = warp_sum(acc[t]);
-      if (lane == 0 && t < static_cast<int>(a.T)) a.ws.partial[(static_cast<size_t>(t) * a.rtot + rho) * c.gs + cta] = v;
+      if (lane == 0 && t < static_cast<int>(a.T))
+        st_relaxed_u64(slots + (static_cast<size_t>(t) * a.rtot + rho) * c.gs + cta,
+                       (static_cast<unsigned long long>(a.epoch) << 32) | __float_as_uint(v));
     }
   }
+}
+
+// v[t][rho] for NP factor rows per lane (pairs base + lane + 32 h): every
+// shrink slot of a row, PER slots per row and round, all loads of a round in
+// flight together; a round is repeated (bounded) until each slot carries this
+// launch's epoch.  Each row is summed over its slots in CTA order.
+template <int NP, int PER>
+__device__ __forceinline__ void gather_rows(const DualArgs& a, const DualCfg& c, float* vsm, uint32_t base,
+                                            uint32_t lane) {
+  const unsigned long long* slots = reinterpret_cast<const unsigned long long*>(a.ws.partial);
+  const uint32_t npairs = a.T * a.rtot;
+  uint32_t cf[NP], cl[NP];
+  bool live[NP];
+  const unsigned long long* pp[NP];
+  float sum[NP];
+#pragma unroll
+  for (int h = 0; h < NP; ++h) {
+    const uint32_t i = base + lane + 32 * h;
+    live[h] = i < npairs;
+    const uint32_t t = live[h] ? i / a.rtot : 0, rho = live[h] ? i - t * a.rtot : 0;
+    partial_range(a, c, rho, &cf[h], &cl[h]);
+    pp[h] = slots + (static_cast<size_t>(t) * a.rtot + rho) * c.gs;
+    sum[h] = 0.f;
+  }
+  for (uint32_t q = 0;; q += PER) {
+    bool more = false;
+#pragma unroll
+    for (int h = 0; h < NP; ++h) more = more || (live[h] && cf[h] + q <= cl[h]);
+    if (!more) break;
+    unsigned long long v[NP][PER];
+    for (uint32_t it = 0;; ++it) {
+      bool all = true;
+#pragma unroll
+      for (int h = 0; h < NP; ++h) {
+#pragma unroll
+        for (int u = 0; u < PER; ++u) {
+          const uint32_t qq = cf[h] + q + u;
+          const bool use = live[h] && qq <= cl[h];
+          v[h][u] = use ? ld_relaxed_u64(pp[h] + qq) : 0ull;
+          all = all && (!use || static_cast<uint32_t>(v[h][u] >> 32) == a.epoch);
+        }
+      }
+      if (all) break;
+      if (it > (1u << 21)) {
+        latch(a.ws.status, kDevTimeoutShrink);
+        break;
+      }
+      __nanosleep(64);
+    }
+#pragma unroll
+    for (int h = 0; h < NP; ++h)
+#pragma unroll
+      for (int u = 0; u < PER; ++u)
+        if (live[h] && cf[h] + q + u <= cl[h]) sum[h] += __uint_as_float(static_cast<uint32_t>(v[h][u]));
+  }
+#pragma unroll
+  for (int h = 0; h < NP; ++h)
+    if (live[h]) vsm[base + lane + 32 * h] = sum[h];
+}
+
+// The B rows [row0, row0 + nrows) of one low-rank term as a 16-byte aligned
+// byte span (bulk-copy granularity); `skew` = offset of the first row in it.
+struct BSpan {
+  const uint8_t* lo;
+  uint32_t bytes, skew;
+};
+__device__ __forceinline__ BSpan b_span(const float* B, uint32_t r, uint32_t row0, uint32_t nrows) {
+  const uintptr_t s = reinterpret_cast<uintptr_t>(B + static_cast<size_t>(row0) * r);
+  const uintptr_t e = s + static_cast<uintptr_t>(nrows) * r * 4u;
+  const uintptr_t lo = s & ~static_cast<uintptr_t>(15);
+  return BSpan{reinterpret_cast<const uint8_t*>(lo), static_cast<uint32_t>(((e + 15) & ~static_cast<uintptr_t>(15)) - lo),
+               static_cast<uint32_t>(s - lo)};
 }
 
 template <int QUANT, int TT, int RG>
@@ -472,14 +600,13 @@ __global__ void __launch_bounds__(K1Shape<TT, RG>::threads, K1Shape<TT, RG>::min
   uint8_t* stages = sm + c.off_stage;
   float* red = reinterpret_cast<float*>(sm + c.off_red);
   float* vsm = reinterpret_cast<float*>(sm + c.off_v);
-  float* tmp = reinterpret_cast<float*>(sm + c.off_tmp);
+  EpTerm* ep = reinterpret_cast<EpTerm*>(sm + c.off_ep);
   float* sA = reinterpret_cast<float*>(sm + c.off_a);
-  float* sB = reinterpret_cast<float*>(sm + c.off_b);
 
   const uint32_t warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t ncw = c.nwc * c.ng;               // consumer warps
   const uint32_t nthr = ncw * 32;
-  const uint32_t G = gridDim.x, cta = blockIdx.x;
+  const uint32_t cta = blockIdx.x;
   // this CTA's tensor and its contiguous row slice of that tensor
   uint32_t si = 0;
   while (si + 1 < a.nseg && cta >= a.seg[si + 1].g0) ++si;
@@ -499,6 +626,23 @@ __global__ void __launch_bounds__(K1Shape<TT, RG>::threads, K1Shape<TT, RG>::min
     *abort_flag = 0u;
     mbar_fence_init();
   }
+  if (warp == 1 % (ncw + 2) && a.nl) {
+    // this tensor's low-rank terms (B stage layout: one 16-byte span per term)
+    const uint32_t nt = sg.k1 - sg.k0;
+    for (uint32_t k = lane; k < nt; k += 32) {
+      const LoraRef L = a.lora[sg.k0 + k];
+      ep[k] = EpTerm{L.B, L.r, L.s, 0u, 0u};
+    }
+    __syncwarp();
+    if (lane == 0) {
+      uint32_t off = 0;
+      for (uint32_t k = 0; k < nt; ++k) {
+        const BSpan sp = b_span(ep[k].B, ep[k].r, row0, nrows);
+        ep[k].here = off + sp.skew;
+        off += sp.bytes;
+      }
+    }
+  }
   __syncthreads();
   griddep_launch_dependents();
 
@@ -507,6 +651,13 @@ __global__ void __launch_bounds__(K1Shape<TT, RG>::threads, K1Shape<TT, RG>::min
       // ---------------- producer: stream this CTA's rows in order.  The base is
       // immutable, so this starts before the preceding grid has finished.
       const uint64_t pol = l2_evict_first_policy();
+      // The B rows are copied in only after the last base stage: bring them
+      // into L2 now so that copy does not wait on HBM.
+      if (c.b_ring)
+        for (uint32_t k = 0; k < sg.k1 - sg.k0; ++k) {
+          const BSpan sp = b_span(ep[k].B, ep[k].r, row0, nrows);
+          bulk_prefetch_l2(sp.lo, sp.bytes);
+        }
       uint32_t issued = 0;
       for (uint32_t s = 0; s < nst; ++s) {
         const uint32_t slot = s % c.ns;
@@ -528,6 +679,24 @@ __global__ void __launch_bounds__(K1Shape<TT, RG>::threads, K1Shape<TT, RG>::min
         bulk_g2s(dst + c.stage_q, sg.dpl + d0, static_cast<uint32_t>(d1 - d0), &full[slot], pol);
         ++issued;
       }
+      // B rows of this CTA's low-rank terms: one more stage, read by the epilogue.
+      if (c.b_ring && sg.k1 > sg.k0 && issued == nst && !*abort_flag) {
+        const uint32_t s = nst, slot = s % c.ns;
+        if (s >= c.ns && !mbar_wait_bounded(&empty[slot], ((s / c.ns) - 1) & 1)) {
+          latch(a.ws.status, kDevTimeoutEmpty);
+          *abort_flag = 1u;
+        } else {
+          const uint32_t nt = sg.k1 - sg.k0;
+          const BSpan last = b_span(ep[nt - 1].B, ep[nt - 1].r, row0, nrows);
+          mbar_arrive_expect_tx(&full[slot], ep[nt - 1].here - last.skew + last.bytes);
+          uint8_t* dst = stages + static_cast<size_t>(slot) * c.stage_bytes;
+          for (uint32_t k = 0; k < nt; ++k) {
+            const BSpan sp = b_span(ep[k].B, ep[k].r, row0, nrows);
+            bulk_g2s(dst + ep[k].here - sp.skew, sp.lo, sp.bytes, &full[slot], pol);
+          }
+          ++issued;
+        }
+      }
       // Do not leave while copies into this CTA's shared memory may be in flight.
       const uint32_t first = issued > c.ns ? issued - c.ns : 0;
       for (uint32_t s = first; s < issued; ++s) mbar_wait_bounded(&full[s % c.ns], (s / c.ns) & 1);
@@ -536,23 +705,15 @@ __global__ void __launch_bounds__(K1Shape<TT, RG>::threads, K1Shape<TT, RG>::min
   }
   if (warp == ncw + 1) {
     // ---------------- helper warp: the low-rank side product, off the critical
-    // path.  Stage this CTA's shrink chunk of A and its B rows, reduce the chunk
-    // against the staged activations, publish the partials with one release
-    // arrival, wait (bounded) for every CTA's arrival, sum the partials in a
-    // fixed order into v and release the epilogue.
+    // path.  Stage this CTA's shrink chunk of A (before the grid dependency
+    // resolves: the factors are immutable) and, after it, the x window of the
+    // chunk; reduce the chunk, publish the epoch-tagged partial sums, then
+    // gather every partial of every factor row (bounded polling on the epochs),
+    // sum them in a fixed order into v and release the epilogue.
     if (!a.nl) return;
-    if (c.stage_b) {
-      uint32_t rb = 0;
-      for (uint32_t k = sg.k0; k < sg.k1; ++k) {
-        const uint32_t cnt = nrows * a.lora[k].r;
-        const float* src = a.lora[k].B + static_cast<size_t>(row0) * a.lora[k].r;
-        for (uint32_t e = lane; e < cnt; e += 32) cp_async4(sB + nrows * rb + e, src + e);
-        rb += a.lora[k].r;
-      }
-    }
+    uint64_t lo = 0, hi = 0;
+    if (cta < c.gs) shrink_bounds(a, c, cta, &lo, &hi);
     if (c.stage_a && cta < c.gs) {
-      uint64_t lo, hi;
-      shrink_bounds(a, c, cta, &lo, &hi);
       const uint32_t rho_a = static_cast<uint32_t>(lo / a.n), rho_b = static_cast<uint32_t>((hi - 1) / a.n);
       for (uint32_t rho = rho_a; rho <= rho_b; ++rho) {
         const uint64_t rs = static_cast<uint64_t>(rho) * a.n;
@@ -565,49 +726,31 @@ __global__ void __launch_bounds__(K1Shape<TT, RG>::threads, K1Shape<TT, RG>::min
     }
     cp_async_commit();
     griddep_wait();
+    XWindow win{0u, 0u, 0u};
+    const void* xw = nullptr;
+    if (c.xwin && cta < c.gs) {
+      const uint32_t esz = a.xdt == OVL_BF16 ? 2u : 4u, g = 16u / esz;
+      win = x_window(lo, hi, a.n, g);
+      uint8_t* sXw = sm + c.off_xw;
+      const uint8_t* gx = static_cast<const uint8_t*>(a.x);
+      const uint32_t n1 = (win.w1 - win.w0) / g, n2 = win.w2 / g;
+      for (uint32_t e = lane; e < n1; e += 32) cp_async16(sXw + e * 16, gx + static_cast<size_t>(win.w0) * esz + e * 16);
+      for (uint32_t e = lane; e < n2; e += 32) cp_async16(sXw + (n1 + e) * 16, gx + e * 16);
+      cp_async_commit();
+      xw = sXw;
+    }
     cp_async_wait_all();
-    named_bar(2, nthr + 32);                        // the consumers have staged x
+    __syncwarp();
+    if (c.stage_x) named_bar(2, nthr + 32);         // the consumers have staged x
     const void* xsrc = c.stage_x ? static_cast<const void*>(sm + c.off_x) : a.x;
-    if (cta < c.gs) shrink_chunk_warp<TT>(a, c, cta, sA, xsrc, lane);
-    __syncwarp();
-    if (lane == 0) {
-      asm volatile("red.release.gpu.global.add.u64 [%0], 1;" ::"l"(&a.ws.counter[0]) : "memory");
-      uint32_t it = 0;
-      while (ld_acquire_u64(&a.ws.counter[0]) < G) {
-        if (++it > (1u << 22)) {
-          latch(a.ws.status, kDevTimeoutShrink);
-          break;
-        }
-        __nanosleep(32);
-      }
+    if (cta < c.gs) shrink_chunk_warp<TT>(a, c, cta, sA, xsrc, xw, win, lane);
+    // v[t][rho] = sum over the shrink CTAs covering row rho, in CTA order.
+    for (uint32_t base = 0; base < a.T * a.rtot; base += 64) {
+      if (a.T * a.rtot - base > 32) gather_rows<2, 6>(a, c, vsm, base, lane);
+      else gather_rows<1, 16>(a, c, vsm, base, lane);
     }
     __syncwarp();
-    for (uint32_t i = lane; i < a.T * a.rtot; i += 32) {
-      const uint32_t t = i / a.rtot, rho = i - t * a.rtot;
-      uint32_t cf, cl;
-      partial_range(a, c, rho, &cf, &cl);
-      const float* p = a.ws.partial + (static_cast<size_t>(t) * a.rtot + rho) * c.gs;
-      float sum = 0.f;
-      for (uint32_t q = cf; q <= cl; q += 4) {   // four loads in flight, summed in order
-        float v4[4];
-#pragma unroll
-        for (int u = 0; u < 4; ++u) v4[u] = (q + u <= cl) ? __ldcg(p + q + u) : 0.f;
-#pragma unroll
-        for (int u = 0; u < 4; ++u)
-          if (q + u <= cl) sum += v4[u];
-      }
-      vsm[t * a.rtot + rho] = sum;
-    }
-    __syncwarp();
-    if (lane == 0) {
-      mbar_arrive(vbar);
-      // Last CTA out resets the arrival counters for the next launch.
-      const unsigned long long old = atomicAdd(&a.ws.counter[1], 1ull);
-      if (old == G - 1) {
-        atomicExch(&a.ws.counter[0], 0ull);
-        atomicExch(&a.ws.counter[1], 0ull);
-      }
-    }
+    if (lane == 0) mbar_arrive(vbar);
     return;
   }
 
@@ -630,14 +773,17 @@ __global__ void __launch_bounds__(K1Shape<TT, RG>::threads, K1Shape<TT, RG>::min
     cp_async_commit();
     cp_async_wait_all();
     xsrc = sX;
+    // x staged: tell the helper warp (which reads it too) without waiting for
+    // it, then make every consumer's copies visible to the others
+    if (a.nl) named_bar_arrive(2, nthr + 32);
+    named_bar(1, nthr);
   }
-  named_bar(2, nthr + (a.nl ? 32u : 0u));          // x staged (the helper warp reads it too)
 
   // 1. activation records.  Single-token launches build each lane's first NREG
   //    records in registers; any further blocks (and multi-token launches) use
   //    records built cooperatively in shared memory.
   if (TT > 1 || c.bpl > static_cast<uint32_t>(NREG)) {
-    prep_records<Q4>(rec, a, xsrc, c.stage_x != 0, c.nb, warp, ncw, lane);
+    prep_records<Q4>(rec, a, xsrc, c.xvec != 0, c.nb, warp, ncw, lane);
     named_bar(1, nthr);
   }
   uint4 rreg[NREG][7];
@@ -646,7 +792,7 @@ __global__ void __launch_bounds__(K1Shape<TT, RG>::threads, K1Shape<TT, RG>::min
     for (int k = 0; k < NREG; ++k) {
       const uint32_t b = L + k * ncol;
       if (k < static_cast<int>(c.bpl) && b < c.nb)
-        lane_record<Q4>(rreg[k], xsrc, a.xdt, c.stage_x != 0, static_cast<size_t>(b) * 32);
+        lane_record<Q4>(rreg[k], xsrc, a.xdt, c.xvec != 0, static_cast<size_t>(b) * 32);
     }
   }
 
@@ -710,10 +856,19 @@ __global__ void __launch_bounds__(K1Shape<TT, RG>::threads, K1Shape<TT, RG>::min
       if (lr < nrows && t < a.T) red[(cw * TT + t) * c.rows_max + lr] = tot;
     }
   }
+  // Every base stage has been consumed (so the B stage's barrier is on the
+  // phase of the B copy itself).
   named_bar(1, nthr);
-  // 4. the low-rank vector from the producer warp (bounded wait)
+  // 4. the low-rank vector from the helper warp and the B rows from the
+  //    producer (bounded waits)
   if (a.nl && !mbar_wait_bounded(vbar, 0)) {
     latch(a.ws.status, kDevTimeoutShrink);
+    ok = false;
+  }
+  const bool b_staged = c.b_ring && sg.k1 > sg.k0;
+  const uint8_t* sBst = stages + static_cast<size_t>(nst % c.ns) * c.stage_bytes;
+  if (ok && b_staged && !mbar_wait_bounded(&full[nst % c.ns], (nst / c.ns) & 1)) {
+    latch(a.ws.status, kDevTimeoutFull);
     ok = false;
   }
 
@@ -724,28 +879,37 @@ __global__ void __launch_bounds__(K1Shape<TT, RG>::threads, K1Shape<TT, RG>::min
     const uint32_t row = row0 + lr;
     float yv = 0.f;
     for (uint32_t w = 0; w < c.nwc; ++w) yv += red[(w * TT + t) * c.rows_max + lr];
-    uint32_t rbase = sg.rb0, rbl = 0;   // global and tensor-local rank offsets
+    uint32_t rbase = sg.rb0;   // global rank offset of the term
     for (uint32_t k = sg.k0; k < sg.k1; ++k) {
-      const uint32_t r = a.lora[k].r;
+      const EpTerm e = ep[k - sg.k0];
+      const uint32_t r = e.r;
       if (a.tok_sel && a.tok_term[t] != static_cast<int>(k)) {   // segmented: one term per token
         rbase += r;
-        rbl += r;
         continue;
       }
-      const float* Brow = c.stage_b ? sB + nrows * rbl + lr * r : a.lora[k].B + static_cast<size_t>(row) * r;
+      const float* Brow = b_staged ? reinterpret_cast<const float*>(sBst + e.here) + lr * r
+                                   : e.B + static_cast<size_t>(row) * r;
       const float* vv = vsm + t * a.rtot + rbase;
+      // Each row starts its dot product at a rotation of its own (lr mod r), so
+      // the lanes of a warp, whose B rows are r words apart, read different
+      // shared-memory banks.  The order is fixed per row: deterministic.
+      const uint32_t rot = lr % r;
       float dot = 0.f;
       for (uint32_t tau = 0; tau < r; tau += 8) {   // eight loads in flight, summed in order
-        float b8[8];
+        float b8[8], v8[8];
 #pragma unroll
-        for (int u = 0; u < 8; ++u) b8[u] = (tau + u < r) ? Brow[tau + u] : 0.f;
+        for (int u = 0; u < 8; ++u) {
+          uint32_t j = tau + u + rot;
+          j = j >= r ? j - r : j;
+          b8[u] = (tau + u < r) ? Brow[j] : 0.f;
+          v8[u] = (tau + u < r) ? vv[j] : 0.f;
+        }
 #pragma unroll
         for (int u = 0; u < 8; ++u)
-          if (tau + u < r) dot = fmaf(b8[u], vv[tau + u], dot);
+          if (tau + u < r) dot = fmaf(b8[u], v8[u], dot);
       }
-      yv = fmaf(a.lora[k].s, dot, yv);
+      yv = fmaf(e.s, dot, yv);
       rbase += r;
-      rbl += r;
     }
     sg.y[static_cast<size_t>(t) * sg.m + row] = yv;
   }
@@ -776,28 +940,29 @@ int device_sms() {
 // Shared-memory plan for one launch; returns false if it cannot fit.  A plan
 // under kSoftBudget leaves room for a CTA of the next launch on the same SM,
 // which then prefetches its weights while this grid drains.
-constexpr uint32_t kSoftBudget = OVL_K1_SOFT_KB * 1024;
+// Two CTAs of 113 KB plus the 1 KB the SM reserves per CTA fill its 228 KB.
+constexpr uint32_t kSoftBudget = OVL_K1_SOFT_BYTES;
 
-bool plan(DualCfg& c, const DualArgs& a, int tt, int rg, uint32_t rows_max) {
+bool plan(DualCfg& c, const DualArgs& a, int tt, int rg, uint32_t rows_max, uint32_t b_need) {
   c.rows_max = rows_max;
   uint32_t off = round_up(2 * kMaxNS * 8 + 8 + 16, 256);   // mbarriers + abort flag
   c.off_rec = off;
-  off = round_up(off + tt * c.nb * kRecBytes, 128);
+  if (tt > 1 || c.bpl > reg_records_of(tt, rg)) off = round_up(off + tt * c.nb * kRecBytes, 128);
   c.off_red = off;
   off = round_up(off + c.nwc * tt * c.rows_max * 4, 128);
   c.off_v = off;
   off = round_up(off + tt * a.rtot * 4 + 4, 128);
-  c.off_tmp = off;
-  off = round_up(off + c.nwc * c.ng * 4 * tt * 4, 128);
+  c.off_ep = off;
+  off = round_up(off + a.nl * static_cast<uint32_t>(sizeof(EpTerm)), 128);
   c.off_x = off;
   if (c.stage_x) off = round_up(off + tt * a.n * (a.xdt == OVL_BF16 ? 2 : 4), 128);
   c.off_a = off;
   if (c.stage_a) off = round_up(off + (static_cast<uint32_t>(static_cast<uint64_t>(a.rtot) * a.n / std::max<uint32_t>(c.gs, 1)) + 2) * 4, 128);
-  c.off_b = off;
-  if (c.stage_b) off = round_up(off + c.rows_max * a.rtot * 4, 128);
-  off = round_up(off, 1024);
+  c.off_xw = off;
+  if (c.xwin) off = round_up(off + c.xwin * (a.xdt == OVL_BF16 ? 2 : 4), 128);
   c.stage_q = rg * c.rowbytes;
   c.stage_bytes = round_up(c.stage_q + round_up(rg * c.nb * 2, 16) + 32, 128);
+  c.b_ring = a.nl && a.b_pad && b_need > 0 && b_need <= c.stage_bytes;
   c.off_stage = off;
   // Group g consumes the stages s = g, g+ng, ...  With ns a multiple of ng every
   // slot is consumed by one group only, in order, so a consumer is never more
@@ -851,7 +1016,7 @@ cudaError_t launch_dualpath(const DualArgs& a_in, cudaStream_t st) {
   int rg = 2;
   if (tt == 1)
     while (rg < 8 && 2 * rg * c.rowbytes <= OVL_K1_STAGE_BYTES) rg *= 2;
-  const uint32_t max_cw = rg <= 2 ? kMaxThreadsWide / 32 - 2 : kMaxThreads / 32 - 2;
+  const uint32_t max_cw = kMaxThreads / 32 - 2;
   c.ng = std::max<uint32_t>(1, std::min<uint32_t>(OVL_K1_MAX_GROUPS, max_cw / c.nwc));
   KernelFn fn = pick(a0.quant, tt, rg);
   if (!fn) return cudaErrorInvalidValue;
@@ -876,18 +1041,44 @@ cudaError_t launch_dualpath(const DualArgs& a_in, cudaStream_t st) {
     G_used += a0.seg[i].gn;
     rows_max = std::max<uint32_t>(rows_max, (a0.seg[i].m + a0.seg[i].gn - 1) / a0.seg[i].gn);
   }
-  c.gs = a0.nl ? static_cast<uint32_t>(std::min<uint64_t>(G_used, static_cast<uint64_t>(a0.rtot) * a0.n)) : 0;
+  // shrink CTAs: at most one per CTA, per factor element, and per free slot
+  c.gs = 0;
+  if (a0.nl) {
+    const uint64_t slots = a0.ws.partial_floats / 2 / (static_cast<uint64_t>(tt) * a0.rtot);
+    c.gs = static_cast<uint32_t>(std::min<uint64_t>({G_used, static_cast<uint64_t>(a0.rtot) * a0.n, slots}));
+    if (c.gs == 0) return cudaErrorInvalidValue;
+  }
   c.div32 = static_cast<uint64_t>(a0.rtot) * a0.n * (static_cast<uint64_t>(c.gs) + 1) < (1ull << 32);
-  if (a0.nl && static_cast<size_t>(tt) * a0.rtot * c.gs > a0.ws.partial_floats) return cudaErrorInvalidValue;
+  if (a0.nl && static_cast<size_t>(tt) * a0.rtot * c.gs > a0.ws.partial_floats / 2) return cudaErrorInvalidValue;
+  if (a0.nl && !a0.ws.epoch_counter) return cudaErrorInvalidValue;
   // operands staged in shared memory when small (immutable ones before the
   // grid dependency resolves, activations right after)
   const uint32_t esz_x = a0.xdt == OVL_BF16 ? 2 : 4;
   const uintptr_t xa = reinterpret_cast<uintptr_t>(a0.x);
   const bool x_small = static_cast<uint64_t>(tt) * a0.n * esz_x <= 32768;
-  c.stage_x = !x_small ? 0 : (xa % 16 == 0 ? 16 : (xa % 4 == 0 ? 4 : 0));
-  c.stage_b = a0.nl && static_cast<uint64_t>(rows_max) * a0.rtot * 4 <= 32768;
+  // Records built per lane in registers read x once, straight from global.
+  const bool reg_only = tt == 1 && c.bpl <= reg_records_of(tt, rg);
+  c.stage_x = (reg_only || !x_small) ? 0 : (xa % 16 == 0 ? 16 : (xa % 4 == 0 ? 4 : 0));
+  c.xvec = c.stage_x ? 1 : (xa % 16 == 0 ? 1 : 0);
   c.stage_a = a0.nl && (static_cast<uint64_t>(a0.rtot) * a0.n / std::max<uint32_t>(c.gs, 1) + 2) * 4 <= 32768;
-  if (!plan(c, a0, tt, rg, rows_max)) return cudaErrorInvalidConfiguration;
+  // Single-token launches with x left in global memory: the helper warp stages
+  // the x window of its shrink chunk (16-byte copies) when it is small.
+  if (a0.nl && tt == 1 && !c.stage_x && c.xvec) {
+    const uint32_t g = 16 / esz_x;
+    const uint64_t chunk = (static_cast<uint64_t>(a0.rtot) * a0.n + c.gs - 1) / c.gs;
+    // pieces: at most chunk + 2g elements, and at most n + g when the chunk wraps
+    const uint64_t cap = std::min<uint64_t>(static_cast<uint64_t>(a0.n) + g, chunk + 2 * g);
+    c.xwin = cap * esz_x <= 8192 ? static_cast<uint32_t>(cap) : 0;
+  }
+  // Bytes of the B stage of the largest CTA slice (16-byte spans per term).
+  uint32_t b_need = 0;
+  for (uint32_t i = 0; a0.nl && i < a0.nseg; ++i) {
+    const uint64_t rows = (a0.seg[i].m + a0.seg[i].gn - 1) / a0.seg[i].gn;
+    uint64_t need = 0;
+    for (uint32_t k = a0.seg[i].k0; k < a0.seg[i].k1; ++k) need += (rows * a0.lora[k].r * 4 + 15) / 16 * 16 + 16;
+    b_need = static_cast<uint32_t>(std::min<uint64_t>(std::max<uint64_t>(b_need, need), 1u << 30));
+  }
+  if (!plan(c, a0, tt, rg, rows_max, b_need)) return cudaErrorInvalidConfiguration;
   if (c.ns % c.ng != 0 || c.ns > static_cast<uint32_t>(kMaxNS)) return cudaErrorInvalidConfiguration;
   const uint32_t threads = (c.nwc * c.ng + 2) * 32;   // consumers + producer + helper
   // one attribute / occupancy query per (kernel, shared-memory size)
@@ -902,6 +1093,11 @@ cudaError_t launch_dualpath(const DualArgs& a_in, cudaStream_t st) {
       if (seen[i].fn == fn && seen[i].smem == c.smem) occ = seen[i].occ;
     if (occ < 0) {
       cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBudget);
+      // Always the largest shared-memory carveout: an SM configured smaller for
+      // one launch would have no room for a CTA of the next, which then packs
+      // two CTAs onto the SMs that drained first and leaves others idle.
+      if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(fn, cudaFuncAttributePreferredSharedMemoryCarveout, cudaSharedmemCarveoutMaxShared);
       if (e != cudaSuccess) return e;
       e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, fn, threads, c.smem);
       if (e != cudaSuccess) return e;
@@ -919,6 +1115,17 @@ cudaError_t launch_dualpath(const DualArgs& a_in, cudaStream_t st) {
     for (uint32_t i = 0; i < a0.nseg; ++i) a.seg[i].y = a0.seg[i].y + static_cast<size_t>(t0) * a0.seg[i].m;
     if (a0.tok_sel)
       for (uint32_t t = 0; t < 8; ++t) a.tok_term[t] = (t0 + t < a0.T) ? a0.tok_host[t0 + t] : -1;
+    if (a0.nl) {
+      // A fresh epoch per launch; on wrap-around clear the slots first so no
+      // slot can carry a reused epoch.
+      uint32_t ep = ++*a0.ws.epoch_counter;
+      if (ep == 0) {
+        e = cudaMemsetAsync(a0.ws.partial, 0, a0.ws.partial_floats * sizeof(float), st);
+        if (e != cudaSuccess) return e;
+        ep = ++*a0.ws.epoch_counter;
+      }
+      a.epoch = ep;
+    }
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = dim3(G_used);
     cfg.blockDim = dim3(threads);

@@ -1,8 +1,8 @@
 // Allocation-free variant of the dual-path forward.
 //
 // The regular entry point (ovl_linear_forward) takes its kernel scratch -- the
-// low-rank partial sums, the grid arrival counters and the device status word
-// -- from the arena that the caller lent to ovl_create.  Some callers have no
+// low-rank partial sums and the device status word -- from the arena that the
+// caller lent to ovl_create.  Some callers have no
 // arena to lend and cannot allocate device memory when they call: code that
 // runs while a stream capture is in progress in the global capture mode (where
 // cudaMalloc is refused), or an embedder whose device memory is owned entirely
@@ -24,12 +24,12 @@
 namespace ovl {
 namespace {
 
-// 2 MiB of scratch per device: 256 B status word, 256 B arrival counters, the
-// rest low-rank partial sums (T-tile x total rank x shrink CTAs floats).  Every
-// GPU that loads the library keeps this array until the process exits.
+// 2 MiB of scratch per device: a 512 B head holding the status word, the rest
+// epoch-tagged low-rank partial-sum slots (8 bytes per T-tile x total rank x
+// shrink CTA; the launch lowers the number of shrink CTAs to fit).  Every GPU
+// that loads the library keeps this array until the process exits.
 constexpr size_t kNoAllocBytes = 2u << 20;
 constexpr size_t kNoAllocStatus = 0;
-constexpr size_t kNoAllocCounter = 256;
 constexpr size_t kNoAllocPartial = 512;
 constexpr int kMaxDevices = 64;
 
@@ -37,6 +37,7 @@ static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocBytes];
 
 std::mutex g_setup_mu;
 uint8_t* g_scratch_addr[kMaxDevices] = {};
+uint32_t g_epoch[kMaxDevices] = {};   // last partial-slot epoch per device (calls are serialized)
 
 // Device address of the array on the current device, looked up (and the array
 // cleared) on the first call for that device.  In host code the array's name is
@@ -98,16 +99,12 @@ extern "C" ovl_status ovl_dualpath_forward_noalloc(const void* qs, const void* d
     cudaGetLastError();
     return OVL_E_CUDA;
   }
-  // Largest partial-sum demand of any launch of this call: a token tile of at
-  // most 8, the total rank, and at most one shrink chunk per SM.
-  int nsm = 0;
-  cudaDeviceGetAttribute(&nsm, cudaDevAttrMultiProcessorCount, dev);
-  const uint64_t shrink_ctas = std::min<uint64_t>(static_cast<uint64_t>(nsm > 0 ? nsm : 1),
-                                                  static_cast<uint64_t>(rtot) * d_in);
-  const uint64_t need = kNoAllocPartial + 4ull * 8 * rtot * shrink_ctas;
+  // The launch fits its number of shrink CTAs to the slots; it needs at least
+  // one CTA's slots for a full token tile of 8.
+  const uint64_t need = kNoAllocPartial + 8ull * 8 * rtot;
   if (n_terms && need > kNoAllocBytes) return OVL_E_OOM;   // more scratch than the static array holds
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  // The status word and the arrival counters must start at zero.
+  // The status word must start at zero.
   e = cudaMemsetAsync(scratch, 0, kNoAllocPartial, st);
   if (e != cudaSuccess) {
     cudaGetLastError();
@@ -125,9 +122,14 @@ extern "C" ovl_status ovl_dualpath_forward_noalloc(const void* qs, const void* d
   a.nl = n_terms;
   a.rtot = rtot;
   a.ws.status = reinterpret_cast<uint32_t*>(scratch + kNoAllocStatus);
-  a.ws.counter = reinterpret_cast<unsigned long long*>(scratch + kNoAllocCounter);
   a.ws.partial = reinterpret_cast<float*>(scratch + kNoAllocPartial);
   a.ws.partial_floats = (kNoAllocBytes - kNoAllocPartial) / sizeof(float);
+  a.ws.epoch_counter = &g_epoch[dev];
+  // B rows are bulk-copied in 16-byte granules only when that stays inside the
+  // caller's B arrays.
+  a.b_pad = 1;
+  for (uint32_t k = 0; k < n_terms; ++k)
+    if ((reinterpret_cast<uintptr_t>(B[k]) & 15) || (static_cast<uint64_t>(d_out) * rank[k] * 4) % 16) a.b_pad = 0;
   e = launch_dualpath(a, st);
   if (e != cudaSuccess) {
     cudaGetLastError();

@@ -35,7 +35,6 @@ namespace {
 
 constexpr size_t kArenaAlign = 256;
 constexpr size_t kStatusOff = 0;
-constexpr size_t kCounterOff = 256;
 constexpr size_t kPartialOff = 1024;
 constexpr size_t kPartialBytes = 8u << 20;
 constexpr size_t kReservedEnd = kPartialOff + kPartialBytes;
@@ -139,6 +138,7 @@ struct ovl_ctx {
   cudaEvent_t fwd_done = nullptr;
   bool fwd_recorded = false;
   ovl::Workspace ws{};
+  uint32_t slot_epoch = 0;   // last partial-slot epoch handed to a launch
   // base
   bool base_loaded = false;
   uint32_t quant = 0;
@@ -365,9 +365,9 @@ ovl_status ovl_create(ovl_ctx** out, int device, void* arena_dev, size_t arena_b
     return OVL_E_CUDA;
   }
   c->ws.status = reinterpret_cast<uint32_t*>(c->arena + kStatusOff);
-  c->ws.counter = reinterpret_cast<unsigned long long*>(c->arena + kCounterOff);
   c->ws.partial = reinterpret_cast<float*>(c->arena + kPartialOff);
   c->ws.partial_floats = kPartialBytes / sizeof(float);
+  c->ws.epoch_counter = &c->slot_epoch;
   *out = c;
   return OVL_OK;
 }
@@ -670,6 +670,7 @@ ovl_status ovl_linear_forward(ovl_ctx* ctx, uint32_t tensor, const void* x, uint
   const uint32_t nl = stack_terms(ctx, *ctx->active, tensor, terms, &rtot, &used);
   if (path == OVL_PATH_DUAL) {
     DualArgs a{};
+    a.b_pad = 1;   // factors live in the arena: 16-byte aligned, allocations rounded to 256 bytes
     a.qs = ctx->base + td.qs_off;
     a.dpl = ctx->base + td.d_off;
     a.m = td.d_out;
@@ -728,6 +729,7 @@ ovl_status ovl_linear_forward_multi(ovl_ctx* ctx, uint32_t n, const uint32_t* te
   if (!x) return fail(ctx, OVL_E_ARG, "null activation");
   DeviceGuard g(ctx->device);
   DualArgs a{};
+  a.b_pad = 1;   // factors live in the arena: 16-byte aligned, allocations rounded to 256 bytes
   std::vector<Adapter*> used;
   for (uint32_t i = 0; i < n; ++i) {
     const ovl_tensor_desc& td = ctx->tensors[tensors[i]];
@@ -790,6 +792,7 @@ ovl_status ovl_segmented_forward(ovl_ctx* ctx, uint32_t tensor, const void* x, u
   // low-rank terms: every table slot that targets this tensor
   const ovl_tensor_desc& td = ctx->tensors[tensor];
   DualArgs a{};
+  a.b_pad = 1;   // factors live in the arena: 16-byte aligned, allocations rounded to 256 bytes
   std::vector<int> slot_term(n_slots, -1);
   std::vector<Adapter*> used;
   for (int32_t sl = 0; sl < n_slots; ++sl) {
@@ -883,9 +886,9 @@ ovl_status ovl_check_device(ovl_ctx* ctx, void* stream) {
   if (e == cudaSuccess) e = cudaMemcpy(&st, ctx->ws.status, 4, cudaMemcpyDeviceToHost);
   if (e != cudaSuccess) return cuda_fail(ctx, e, "check device");
   if (st != kDevOk) {
-    // Reset the status word and the workspace counters so the next launch starts clean.
+    // Reset the status word so the next launch starts clean (the partial-sum
+    // slots need nothing: every launch tags its own with a fresh epoch).
     cudaMemset(ctx->ws.status, 0, 4);
-    cudaMemset(ctx->ws.counter, 0, 2 * sizeof(unsigned long long));
     return fail(ctx, OVL_E_DEVICE_TIMEOUT, "a bounded device wait ran out (code " + std::to_string(st) + ")");
   }
   return ok(ctx);

@@ -17,7 +17,7 @@ enum : uint32_t {
   kDevOk = 0,
   kDevTimeoutFull = 1,      // consumer gave up waiting for a staged tile
   kDevTimeoutEmpty = 2,     // producer gave up waiting for a free stage
-  kDevTimeoutShrink = 3,    // epilogue gave up waiting for the low-rank partials
+  kDevTimeoutShrink = 3,    // gave up waiting for the low-rank partial sums
 };
 
 // One low-rank term as the kernels see it: A [r][d_in], B [d_out][r] (fp32,
@@ -29,12 +29,16 @@ struct LoraRef {
   float s;
 };
 
-// Device workspace carved from the arena at context creation.
+// Device workspace carved from the arena at context creation.  The low-rank
+// partial sums are 64-bit slots {launch epoch (high word), f32 value (low
+// word)}: a reader accepts a slot once it carries its own launch's epoch, so no
+// slot ever needs clearing between launches.  The epoch counter is host memory
+// (launcher only); epochs start at 1 and the slots are cleared when it wraps.
 struct Workspace {
-  uint32_t* status;               // one status word
-  unsigned long long* counter;    // [0]: arrivals, [1]: departures (self-resetting)
-  float* partial;                 // low-rank partial sums
-  size_t partial_floats;
+  uint32_t* status;               // one status word (device)
+  float* partial;                 // partial-sum slots (device), 8 bytes each
+  size_t partial_floats;          // size of that region in floats
+  uint32_t* epoch_counter;        // host: last epoch handed out
 };
 
 // One tensor of a (multi-tensor) dual-path launch.  All tensors of a launch
@@ -55,24 +59,31 @@ constexpr int kMaxMulti = 4;
 // Fused dual-path forward over a token chunk (T <= 8).  Single-tensor callers
 // fill qs/dpl/m/y; multi-tensor callers fill nseg and seg[] (qs, dpl, y, m,
 // k0, k1, rb0) and leave m = total rows.
+// Field order: the kernel reads its parameters through the constant cache, and
+// a line first touched late in the kernel costs a memory round trip there.
+// Everything the kernel reads late (epoch, workspace, token selection) shares
+// the first cache lines with fields every warp reads at the start.
 struct DualArgs {
   const uint8_t* qs;      // qs plane
   const uint8_t* dpl;     // d plane (binary16)
-  uint32_t m, n, quant;
   const void* x;          // [T][n], fp32 or bf16
-  uint32_t xdt, T;
   float* y;               // [T][m]
+  uint32_t m, n, quant;
+  uint32_t xdt, T;
   uint32_t nl;            // number of low-rank terms
   uint32_t rtot;          // sum of ranks
-  LoraRef lora[OVL_MAX_TABLE];
+  uint32_t epoch;         // this launch's partial-slot epoch (filled by the launcher)
+  uint32_t nseg;          // 0: single tensor (qs/dpl/m/y); else seg[0..nseg)
   // Per-token term selection (segmented batches): when tok_sel is set, token t
   // of the launch receives only term tok_term[t] (-1: base only).
   uint32_t tok_sel;
-  int8_t tok_term[8];           // this launch's slice (filled by the launcher)
-  const int8_t* tok_host;       // host array of T entries (launcher only)
-  uint32_t nseg;                // 0: single tensor (qs/dpl/m/y); else seg[0..nseg)
-  DualSeg seg[kMaxMulti];
+  int8_t tok_term[8];     // this launch's slice (filled by the launcher)
+  uint32_t b_pad;         // 1: each B may be read in 16-byte granules around its rows
+                          //    (arena-resident factors), so B rows can be bulk-copied
   Workspace ws;
+  DualSeg seg[kMaxMulti];
+  LoraRef lora[OVL_MAX_TABLE];
+  const int8_t* tok_host;  // host array of T entries (launcher only)
 };
 
 // Materialize S = deq(W) + sum_k s_k B_k A_k into fp32 scratch [m][n].
