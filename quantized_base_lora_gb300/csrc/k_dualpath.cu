@@ -92,7 +92,9 @@ struct DualCfg {
   uint32_t xvec;                 // 1: x (staged or global) allows 16-byte vector loads
   uint32_t stage_a;              // 1: the shrink chunk of A is staged in shared memory
   uint32_t xwin;                 // >0: the helper stages the x window of its chunk (capacity, elements)
+  uint32_t shrink_vec;           // 1: A chunk and x window share one index, 16-byte vector reads
   uint32_t b_ring;               // 1: B rows arrive as one ring stage after the last base stage
+  uint32_t b_areg;               // 1: the helper copies B rows into the A/x-window area after its shrink
   uint32_t div32;                // 1: rtot * n * gs < 2^32, chunk arithmetic fits 32 bits
   uint32_t smem;
 };
@@ -651,9 +653,9 @@ __global__ void __launch_bounds__(K1Shape<TT, RG>::threads, K1Shape<TT, RG>::min
       // ---------------- producer: stream this CTA's rows in order.  The base is
       // immutable, so this starts before the preceding grid has finished.
       const uint64_t pol = l2_evict_first_policy();
-      // The B rows are copied in only after the last base stage: bring them
-      // into L2 now so that copy does not wait on HBM.
-      if (c.b_ring)
+      // The B rows are copied in late (after the shrink, or after the last
+      // base stage): bring them into L2 now so that copy does not wait on HBM.
+      if (c.b_ring || c.b_areg)
         for (uint32_t k = 0; k < sg.k1 - sg.k0; ++k) {
           const BSpan sp = b_span(ep[k].B, ep[k].r, row0, nrows);
           bulk_prefetch_l2(sp.lo, sp.bytes);
@@ -713,7 +715,26 @@ __global__ void __launch_bounds__(K1Shape<TT, RG>::threads, K1Shape<TT, RG>::min
     if (!a.nl) return;
     uint64_t lo = 0, hi = 0;
     if (cta < c.gs) shrink_bounds(a, c, cta, &lo, &hi);
-    if (c.stage_a && cta < c.gs) {
+    const bool vec = c.shrink_vec && cta < c.gs;
+    uint32_t rho_a = 0, w0 = 0;
+    if (vec) {
+      // Element f of the chunk lives at index f - rho_a n - w0 of both the
+      // staged A and the x window (w0 = the window start, a multiple of the
+      // 16-byte granule); each factor row is copied as its 16-byte aligned
+      // superset [j0 & ~3, (j1 + 3) & ~3).
+      const uint32_t g = a.xdt == OVL_BF16 ? 8u : 4u;
+      rho_a = static_cast<uint32_t>(lo / a.n);
+      w0 = static_cast<uint32_t>(lo - static_cast<uint64_t>(rho_a) * a.n) / g * g;
+      const uint32_t rho_b = static_cast<uint32_t>((hi - 1) / a.n);
+      for (uint32_t rho = rho_a; rho <= rho_b; ++rho) {
+        const uint64_t rs = static_cast<uint64_t>(rho) * a.n;
+        const uint32_t j0 = static_cast<uint32_t>(max(lo, rs) - rs);
+        const uint32_t j1 = static_cast<uint32_t>(min(hi, rs + a.n) - rs);
+        const float* Arow = factor_ptr(a, rs);
+        float* dst = sA + ((rho - rho_a) * a.n - w0);
+        for (uint32_t e = (j0 >> 2) + lane; e < ((j1 + 3) >> 2); e += 32) cp_async16(dst + 4 * e, Arow + 4 * e);
+      }
+    } else if (c.stage_a && cta < c.gs) {
       const uint32_t rho_a = static_cast<uint32_t>(lo / a.n), rho_b = static_cast<uint32_t>((hi - 1) / a.n);
       for (uint32_t rho = rho_a; rho <= rho_b; ++rho) {
         const uint64_t rs = static_cast<uint64_t>(rho) * a.n;
@@ -743,12 +764,58 @@ __global__ void __launch_bounds__(K1Shape<TT, RG>::threads, K1Shape<TT, RG>::min
     __syncwarp();
     if (c.stage_x) named_bar(2, nthr + 32);         // the consumers have staged x
     const void* xsrc = c.stage_x ? static_cast<const void*>(sm + c.off_x) : a.x;
-    if (cta < c.gs) shrink_chunk_warp<TT>(a, c, cta, sA, xsrc, xw, win, lane);
+    if (vec) {
+      unsigned long long* slots = reinterpret_cast<unsigned long long*>(a.ws.partial);
+      const uint32_t rho_b = static_cast<uint32_t>((hi - 1) / a.n);
+      const uint64_t fb = static_cast<uint64_t>(rho_a) * a.n + w0;
+      for (uint32_t rho = rho_a; rho <= rho_b; ++rho) {
+        const uint64_t rs = static_cast<uint64_t>(rho) * a.n;
+        const uint32_t i0 = static_cast<uint32_t>(max(lo, rs) - fb);
+        const uint32_t i1 = static_cast<uint32_t>(min(hi, rs + a.n) - fb);
+        float c4[4] = {0.f, 0.f, 0.f, 0.f};
+        for (uint32_t idx = (i0 & ~3u) + 4 * lane; idx < i1; idx += 128) {
+          const float4 av = *reinterpret_cast<const float4*>(sA + idx);
+          float xv[4];
+          if (a.xdt == OVL_BF16) {
+            const uint2 w = *reinterpret_cast<const uint2*>(static_cast<const uint16_t*>(xw) + idx);
+            xv[0] = __uint_as_float(w.x << 16); xv[1] = __uint_as_float(w.x & 0xFFFF0000u);
+            xv[2] = __uint_as_float(w.y << 16); xv[3] = __uint_as_float(w.y & 0xFFFF0000u);
+          } else {
+            const float4 w = *reinterpret_cast<const float4*>(static_cast<const float*>(xw) + idx);
+            xv[0] = w.x; xv[1] = w.y; xv[2] = w.z; xv[3] = w.w;
+          }
+          const float aq[4] = {av.x, av.y, av.z, av.w};
+#pragma unroll
+          for (int q = 0; q < 4; ++q)
+            if (idx + q >= i0 && idx + q < i1) c4[q] = fmaf(aq[q], xv[q], c4[q]);
+        }
+        const float v = warp_sum((c4[0] + c4[1]) + (c4[2] + c4[3]));
+        if (lane == 0)
+          st_relaxed_u64(slots + static_cast<size_t>(rho) * c.gs + cta,
+                         (static_cast<unsigned long long>(a.epoch) << 32) | __float_as_uint(v));
+      }
+    } else if (cta < c.gs) {
+      shrink_chunk_warp<TT>(a, c, cta, sA, xsrc, xw, win, lane);
+    }
+    if (c.b_areg) {
+      // The A chunk and the x window are consumed: reuse their area for this
+      // CTA's B rows (16-byte copies of each term's span), ready long before
+      // the base stream ends.
+      __syncwarp();
+      uint8_t* dstB = sm + c.off_a;
+      for (uint32_t k = 0; k < sg.k1 - sg.k0; ++k) {
+        const BSpan sp = b_span(ep[k].B, ep[k].r, row0, nrows);
+        uint8_t* d = dstB + ep[k].here - sp.skew;
+        for (uint32_t e = lane; e < sp.bytes / 16; e += 32) cp_async16(d + e * 16, sp.lo + e * 16);
+      }
+      cp_async_commit();
+    }
     // v[t][rho] = sum over the shrink CTAs covering row rho, in CTA order.
     for (uint32_t base = 0; base < a.T * a.rtot; base += 64) {
       if (a.T * a.rtot - base > 32) gather_rows<2, 6>(a, c, vsm, base, lane);
       else gather_rows<1, 16>(a, c, vsm, base, lane);
     }
+    cp_async_wait_all();   // B rows (when copied here) land before the release
     __syncwarp();
     if (lane == 0) mbar_arrive(vbar);
     return;
@@ -859,21 +926,70 @@ __global__ void __launch_bounds__(K1Shape<TT, RG>::threads, K1Shape<TT, RG>::min
   // Every base stage has been consumed (so the B stage's barrier is on the
   // phase of the B copy itself).
   named_bar(1, nthr);
+  const bool b_staged = (c.b_ring || c.b_areg) && sg.k1 > sg.k0;
+  const uint8_t* sBst = c.b_areg ? sm + c.off_a : stages + static_cast<size_t>(nst % c.ns) * c.stage_bytes;
+  const uint32_t nterm = sg.k1 - sg.k0;
+  // Common single-token case: at most one output per thread and at most one
+  // term of rank <= 16 with its B rows staged.  Every shared-memory read that
+  // does not need v is issued before the waits below, and the B and v reads
+  // after them go out in one round: a chain of dependent shared-memory rounds
+  // is what an epilogue costs at the end of a memory-bound launch.
+  const uint32_t r0f = nterm ? ep[0].r : 0u;
+  const bool fast = TT == 1 && nrows <= nthr && !a.tok_sel && nterm <= 1 && r0f <= 16 && (nterm == 0 || b_staged);
+  float rv[kMaxThreads / 32];
+  EpTerm e0{};
+  uint32_t rot0 = 0;
+  if (fast) {
+    const uint32_t lr = threadIdx.x;
+#pragma unroll
+    for (int w = 0; w < kMaxThreads / 32; ++w)
+      rv[w] = (lr < nrows && w < static_cast<int>(c.nwc)) ? red[w * c.rows_max + lr] : 0.f;
+    if (nterm) {
+      e0 = ep[0];
+      rot0 = lr % e0.r;
+    }
+  }
   // 4. the low-rank vector from the helper warp and the B rows from the
   //    producer (bounded waits)
   if (a.nl && !mbar_wait_bounded(vbar, 0)) {
     latch(a.ws.status, kDevTimeoutShrink);
     ok = false;
   }
-  const bool b_staged = c.b_ring && sg.k1 > sg.k0;
-  const uint8_t* sBst = stages + static_cast<size_t>(nst % c.ns) * c.stage_bytes;
-  if (ok && b_staged && !mbar_wait_bounded(&full[nst % c.ns], (nst / c.ns) & 1)) {
+  if (ok && c.b_ring && b_staged && !mbar_wait_bounded(&full[nst % c.ns], (nst / c.ns) & 1)) {
     latch(a.ws.status, kDevTimeoutFull);
     ok = false;
   }
 
   // 5. epilogue, one output per thread: y = base + sum_k s_k (B_k v_k)
   if (!ok) return;
+  if (fast) {
+    const uint32_t lr = threadIdx.x;
+    if (lr >= nrows) return;
+    float yv = 0.f;
+#pragma unroll
+    for (int w = 0; w < kMaxThreads / 32; ++w)
+      if (w < static_cast<int>(c.nwc)) yv += rv[w];
+    if (nterm) {
+      const uint32_t r = e0.r;
+      const float* Brow = reinterpret_cast<const float*>(sBst + e0.here) + lr * r;
+      const float* vv = vsm + sg.rb0;
+      float b16[16], v16[16];
+#pragma unroll
+      for (int u = 0; u < 16; ++u) {
+        uint32_t j = u + rot0;
+        j = j >= r ? j - r : j;
+        b16[u] = static_cast<uint32_t>(u) < r ? Brow[j] : 0.f;
+        v16[u] = static_cast<uint32_t>(u) < r ? vv[j] : 0.f;
+      }
+      float dot = 0.f;
+#pragma unroll
+      for (int u = 0; u < 16; ++u)
+        if (static_cast<uint32_t>(u) < r) dot = fmaf(b16[u], v16[u], dot);
+      yv = fmaf(e0.s, dot, yv);
+    }
+    sg.y[row0 + lr] = yv;
+    return;
+  }
   for (uint32_t i = threadIdx.x; i < a.T * nrows; i += nthr) {
     const uint32_t t = i / nrows, lr = i - t * nrows;
     const uint32_t row = row0 + lr;
@@ -957,12 +1073,18 @@ bool plan(DualCfg& c, const DualArgs& a, int tt, int rg, uint32_t rows_max, uint
   c.off_x = off;
   if (c.stage_x) off = round_up(off + tt * a.n * (a.xdt == OVL_BF16 ? 2 : 4), 128);
   c.off_a = off;
-  if (c.stage_a) off = round_up(off + (static_cast<uint32_t>(static_cast<uint64_t>(a.rtot) * a.n / std::max<uint32_t>(c.gs, 1)) + 2) * 4, 128);
+  if (c.stage_a) {
+    const uint32_t chunk = static_cast<uint32_t>((static_cast<uint64_t>(a.rtot) * a.n + c.gs - 1) / std::max<uint32_t>(c.gs, 1));
+    off = round_up(off + (chunk + (c.shrink_vec ? 24u : 2u)) * 4, 128);
+  }
   c.off_xw = off;
   if (c.xwin) off = round_up(off + c.xwin * (a.xdt == OVL_BF16 ? 2 : 4), 128);
   c.stage_q = rg * c.rowbytes;
   c.stage_bytes = round_up(c.stage_q + round_up(rg * c.nb * 2, 16) + 32, 128);
-  c.b_ring = a.nl && a.b_pad && b_need > 0 && b_need <= c.stage_bytes;
+  // B rows: into the A chunk + x window area after the shrink when they fit
+  // there, else as one ring stage after the last base stage, else from global
+  c.b_areg = a.nl && a.b_pad && b_need > 0 && b_need <= off - c.off_a;
+  c.b_ring = a.nl && a.b_pad && !c.b_areg && b_need > 0 && b_need <= c.stage_bytes;
   c.off_stage = off;
   // Group g consumes the stages s = g, g+ng, ...  With ns a multiple of ng every
   // slot is consumed by one group only, in order, so a consumer is never more
@@ -1069,6 +1191,9 @@ cudaError_t launch_dualpath(const DualArgs& a_in, cudaStream_t st) {
     // pieces: at most chunk + 2g elements, and at most n + g when the chunk wraps
     const uint64_t cap = std::min<uint64_t>(static_cast<uint64_t>(a0.n) + g, chunk + 2 * g);
     c.xwin = cap * esz_x <= 8192 ? static_cast<uint32_t>(cap) : 0;
+    // one index for the A chunk and the x window: every chunk shorter than a
+    // factor row (so it touches at most two), 16-byte aligned factors
+    c.shrink_vec = c.xwin && c.stage_a && a0.a16 && chunk + g < a0.n && (chunk + 24) * 4 <= 32768;
   }
   // Bytes of the B stage of the largest CTA slice (16-byte spans per term).
   uint32_t b_need = 0;

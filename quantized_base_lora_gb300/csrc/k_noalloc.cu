@@ -128,8 +128,11 @@ extern "C" ovl_status ovl_dualpath_forward_noalloc(const void* qs, const void* d
   // B rows are bulk-copied in 16-byte granules only when that stays inside the
   // caller's B arrays.
   a.b_pad = 1;
-  for (uint32_t k = 0; k < n_terms; ++k)
+  a.a16 = 1;
+  for (uint32_t k = 0; k < n_terms; ++k) {
     if ((reinterpret_cast<uintptr_t>(B[k]) & 15) || (static_cast<uint64_t>(d_out) * rank[k] * 4) % 16) a.b_pad = 0;
+    if (reinterpret_cast<uintptr_t>(A[k]) & 15) a.a16 = 0;
+  }
   e = launch_dualpath(a, st);
   if (e != cudaSuccess) {
     cudaGetLastError();

@@ -671,6 +671,7 @@ ovl_status ovl_linear_forward(ovl_ctx* ctx, uint32_t tensor, const void* x, uint
   if (path == OVL_PATH_DUAL) {
     DualArgs a{};
     a.b_pad = 1;   // factors live in the arena: 16-byte aligned, allocations rounded to 256 bytes
+  a.a16 = 1;
     a.qs = ctx->base + td.qs_off;
     a.dpl = ctx->base + td.d_off;
     a.m = td.d_out;
@@ -730,6 +731,7 @@ ovl_status ovl_linear_forward_multi(ovl_ctx* ctx, uint32_t n, const uint32_t* te
   DeviceGuard g(ctx->device);
   DualArgs a{};
   a.b_pad = 1;   // factors live in the arena: 16-byte aligned, allocations rounded to 256 bytes
+  a.a16 = 1;
   std::vector<Adapter*> used;
   for (uint32_t i = 0; i < n; ++i) {
     const ovl_tensor_desc& td = ctx->tensors[tensors[i]];
@@ -793,6 +795,7 @@ ovl_status ovl_segmented_forward(ovl_ctx* ctx, uint32_t tensor, const void* x, u
   const ovl_tensor_desc& td = ctx->tensors[tensor];
   DualArgs a{};
   a.b_pad = 1;   // factors live in the arena: 16-byte aligned, allocations rounded to 256 bytes
+  a.a16 = 1;
   std::vector<int> slot_term(n_slots, -1);
   std::vector<Adapter*> used;
   for (int32_t sl = 0; sl < n_slots; ++sl) {

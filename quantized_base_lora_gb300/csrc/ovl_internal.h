@@ -80,6 +80,7 @@ struct DualArgs {
   int8_t tok_term[8];     // this launch's slice (filled by the launcher)
   uint32_t b_pad;         // 1: each B may be read in 16-byte granules around its rows
                           //    (arena-resident factors), so B rows can be bulk-copied
+  uint32_t a16;           // 1: every A is 16-byte aligned (16-byte copies of its rows)
   Workspace ws;
   DualSeg seg[kMaxMulti];
   LoraRef lora[OVL_MAX_TABLE];

@@ -39,11 +39,35 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Bounded wait on a barrier phase: returns false if it gave up (~0.5 s or more).
+// try_wait with a suspend-time hint: a thread whose phase is not complete is
+// suspended in hardware until it completes or about `ns` nanoseconds pass,
+// instead of re-polling the barrier (polls share the shared-memory pipe).
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t parity, uint32_t ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(ns)
+      : "memory");
+  return ok != 0;
+}
+
+__device__ __forceinline__ uint64_t global_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// Bounded wait on a barrier phase: returns false if it gave up after about
+// two seconds (checked on the global timer) or 2^24 attempts.
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_ns();
   for (uint32_t it = 0; it < (1u << 24); ++it) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if (it > 64) __nanosleep(32);
+    if (mbar_try_wait_sleep(bar, parity, 20000u)) return true;
+    if ((it & 63) == 63 && global_ns() - t0 > 2000000000ull) return false;
   }
   return false;
 }
