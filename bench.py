@@ -9,8 +9,22 @@ bf16 activation of its own d_in.  value = effective weight bytes (quantized base
 per step / device time per step; tok/s = steps / s.
 
 Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                      [--workload decode|q4-stacked|segmented|jit-prefill|decode32|switch]
 Under torchrun (N > 1) every rank runs an independent replica on its own GPU
 (the path has no data exchange); the slowest rank's time is used.
+
+--workload selects the other measured configurations (one GPU, one JSON line
+each; the default, decode, is the headline line above):
+  q4-stacked   8B-shape q4_0 block, stacked rank-16 (s=1) + rank-64 (s=0.5)
+               adapters, dual path at T = 1, 4, 8
+  segmented    64 decode requests over 16 rank-16 adapters (TABLE, Zipf 1.1),
+               q4_0 q (4096x4096) and gate (14336x4096)
+  jit-prefill  one 8B-shape q8_0 layer + rank-16 adapter, T = 512 prefill on the
+               per-layer JIT path (fp32 materialization + tcgen05 TF32 GEMM)
+  decode32     32 layers of the 8B block (q8_0 + rank-16 on all 224 tensors),
+               batch-1 decode, tokens/s
+  switch       activate / rollback latency over four 32-layer adapters
+               (168 MB each, one with a corrupt declared digest)
 """
 from __future__ import annotations
 
@@ -336,13 +350,398 @@ def run_ours(args, world, rank, local):
         rt.close()
 
 
+# ---------------------------------------------------------------- other workloads
+LEAF = 65536
+
+
+def replicated_digest(layer: np.ndarray, copies: int) -> bytes:
+    """Content digest of `copies` back-to-back copies of `layer` (a multiple
+    of the 64 KiB leaf): the leaves of one copy repeat."""
+    import hashlib
+    assert layer.nbytes % LEAF == 0
+    mv = memoryview(np.ascontiguousarray(layer)).cast("B")
+    leaves = b"".join(hashlib.sha256(mv[i:i + LEAF]).digest() for i in range(0, layer.nbytes, LEAF))
+    return hashlib.sha256(leaves * copies).digest()
+
+
+def timed_steps(step, steps, warmup, stream):
+    """Mean device ms per step: warm-up, then one event pair around `steps`."""
+    import torch
+    with torch.cuda.stream(stream):
+        for i in range(max(warmup, 3)):
+            step(i)
+    stream.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for i in range(steps):
+            step(i)
+        e1.record(stream)
+    stream.synchronize()
+    return e0.elapsed_time(e1) / steps
+
+
+def emit(line: dict):
+    print(json.dumps(line), flush=True)
+
+
+def hbm_roofline(bytes_per_step: float, ms: float, kernel: str) -> dict:
+    peak, kind = peaks()
+    gbs = bytes_per_step / (ms / 1e3) / 1e9
+    return {"bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s", "frac": gbs / peak, "traffic": None,
+            "kernel": kernel, "note": f"peak = {kind} HBM copy bandwidth"}
+
+
+WORKLOADS = {}
+
+
+def _contexts(base, adapters, scales, copies, arena_mb, mode=None):
+    """`copies` contexts over identical device copies of the base, each with
+    `adapters` staged and activated with `scales` (rotated per step so no step
+    is L2-resident)."""
+    import quantized_base_lora_gb300 as q
+    from quantized_base_lora_gb300.runtime import Runtime
+    tt = [(t.layer, t.proj, t.d_out, t.d_in, t.qs_off, t.d_off) for t in base.tensors]
+    dg = S.content_digest(base.buf)
+    ad_dg = [S.content_digest(ad.payload) for ad in adapters]
+    rts = []
+    for _ in range(copies):
+        rt = Runtime(arena_bytes=arena_mb << 20)
+        q.check(rt.load_base(base.quant, tt, base.buf, dg), rt.ctx)
+        hs = []
+        for ad, d in zip(adapters, ad_dg):
+            st, h = rt.stage(ad, d)
+            q.check(st, rt.ctx)
+            hs.append(h)
+        if hs:
+            q.check(rt.activate(hs, scales, mode if mode is not None else q.OVL_MODE_STACK)[0], rt.ctx)
+        rts.append(rt)
+    return rts
+
+
+def _block_step(base, rts, xs, ys, T, sh):
+    """One decode step of the block: q+k+v, o, gate+up, down (4 launches)."""
+    import quantized_base_lora_gb300 as q
+    groups = [[0, 1, 2], [3], [4, 5], [6]]
+
+    def step(i):
+        rt = rts[i % len(rts)]
+        for grp in groups:
+            xp = xs[base.tensors[grp[0]].d_in]
+            if len(grp) == 1:
+                st = q.ovl_linear_forward(rt.ctx, grp[0], xp, q.OVL_BF16, T, ys[grp[0]], q.OVL_PATH_DUAL, 0, 0, sh)
+            else:
+                st = q.ovl_linear_forward_multi(rt.ctx, grp, xp, q.OVL_BF16, T, [ys[j] for j in grp], sh)
+            if st != 0:
+                raise q.OvlError(st, q.ovl_last_error(rt.ctx))
+    return step
+
+
+def _check_all(rts, sh):
+    import quantized_base_lora_gb300 as q
+    for rt in rts:
+        q.check(q.ovl_check_device(rt.ctx, sh), rt.ctx)
+
+
+def workload_q4_stacked(args):
+    import torch
+    base = S.block_base(S.Q4_0)
+    ads = [S.block_adapter(base, adapter=0, rank=16), S.block_adapter(base, adapter=1, rank=64)]
+    rts = _contexts(base, ads, [1.0, 0.5], N_COPIES, 96)
+    stream = torch.cuda.Stream()
+    sh = int(stream.cuda_stream)
+    planes = sum(S.qs_bytes(base.quant, t.d_out, t.d_in) + S.d_bytes(t.d_out, t.d_in) for t in base.tensors)
+    lora = sum((16 + 64) * (t.d_in + t.d_out) * 4 for t in base.tensors)
+    per_T = {}
+    for T in (1, 4, 8):
+        xs = {d: torch.from_numpy(S.to_bf16_bits(S.activations(T, d)).view(np.int16)).cuda().view(torch.bfloat16)
+              for d in (4096, 14336)}
+        ybufs = [torch.empty((T, t.d_out), dtype=torch.float32, device="cuda") for t in base.tensors]
+        step = _block_step(base, rts, {d: v.data_ptr() for d, v in xs.items()}, [y.data_ptr() for y in ybufs], T, sh)
+        ms = timed_steps(step, args.steps, args.warmup, stream)
+        _check_all(rts, sh)
+        alg = planes + lora + sum(T * (t.d_in * 2 + t.d_out * 4) for t in base.tensors)
+        per_T[T] = {"ms_per_step": ms, "effective_gbs": (planes + lora) / (ms / 1e3) / 1e9,
+                    "tok_s": T / (ms / 1e3), "roofline": hbm_roofline(alg, ms, "k_dualpath (4 launches per step)")}
+    emit({"workload": "q4-stacked", "metric": "decode effective weight GB/s (8B shape, q4_0 + stacked r16/r64)",
+          "unit": "GB/s", "value": per_T[1]["effective_gbs"], "per_T": per_T, "steps": args.steps,
+          "config": {"base": "8B-shape block q4_0 (122.7 MB)", "adapters": "r16 s=1.0 then r64 s=0.5 on all 7",
+                     "x": "bf16", "l2": f"{N_COPIES} base copies rotated"}})
+
+
+WORKLOADS["q4-stacked"] = workload_q4_stacked
+
+
+def workload_segmented(args):
+    import torch
+    import quantized_base_lora_gb300 as q
+    base = S.block_base(S.Q4_0, projs=("q", "gate"))
+    ads = [S.block_adapter(base, adapter=a, rank=16) for a in range(16)]
+    rts = _contexts(base, ads, [2.0] * 16, N_COPIES, 128, mode=q.OVL_MODE_TABLE)
+    stream = torch.cuda.Stream()
+    sh = int(stream.cuda_stream)
+    T = 64
+    ids = S.zipf_ids(T, 16, 1.1)
+    perm, offsets, slots = S.segments(ids)
+    x = torch.from_numpy(S.to_bf16_bits(S.activations(T, 4096)).view(np.int16)).cuda().view(torch.bfloat16)
+    ys = [torch.empty((T, t.d_out), dtype=torch.float32, device="cuda") for t in base.tensors]
+    offs, sl, pm = [int(v) for v in offsets], [int(v) for v in slots], [int(v) for v in perm]
+
+    def step(i):
+        rt = rts[i % len(rts)]
+        for j in range(len(base.tensors)):
+            st = q.ovl_segmented_forward(rt.ctx, j, x.data_ptr(), q.OVL_BF16, T, offs, sl, pm, ys[j].data_ptr(), sh)
+            if st != 0:
+                raise q.OvlError(st, q.ovl_last_error(rt.ctx))
+    ms = timed_steps(step, args.steps, args.warmup, stream)
+    _check_all(rts, sh)
+    planes = sum(S.qs_bytes(base.quant, t.d_out, t.d_in) + S.d_bytes(t.d_out, t.d_in) for t in base.tensors)
+    lora = 16 * sum(16 * (t.d_in + t.d_out) * 4 for t in base.tensors)
+    alg = planes + lora + sum(T * (t.d_in * 2 + t.d_out * 4) for t in base.tensors)
+    flops = sum(2 * T * t.d_out * t.d_in for t in base.tensors)
+    emit({"workload": "segmented", "metric": "segmented multi-adapter batch time (64 requests, 16 adapters)",
+          "unit": "us", "value": ms * 1e3, "higher_is_better": False, "steps": args.steps,
+          "tok_s": T / (ms / 1e3), "effective_gbs": (planes + lora) / (ms / 1e3) / 1e9,
+          "distinct_adapters": int(len(set(int(v) for v in ids))), "segments": len(sl),
+          "roofline": hbm_roofline(alg, ms, "k_dualpath (8-token tiles, one launch per tile and tensor)"),
+          "base_tflops": flops / (ms / 1e3) / 1e12,
+          "config": {"base": "q4_0 q 4096x4096 + gate 14336x4096 (42.5 MB)", "adapters": "16 x r16, s=2.0, TABLE",
+                     "requests": "64, Zipf(1.1) seed 3000", "x": "bf16", "l2": f"{N_COPIES} base copies rotated"}})
+
+
+WORKLOADS["segmented"] = workload_segmented
+
+
+def tf32_peak():
+    """Dense TF32 tensor peak: the measured bf16 GEMM peak x the nominal
+    tf32/bf16 ratio (1.1 / 2.25 PFLOP/s)."""
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["bf16_tflops"]) * 1.1 / 2.25, "measured bf16 x nominal tf32/bf16"
+    except Exception:
+        return 1900.0 * 1.1 / 2.25, "fallback bf16 x nominal tf32/bf16"
+
+
+def workload_jit_prefill(args):
+    import torch
+    import quantized_base_lora_gb300 as q
+    base = S.block_base(S.Q8_0)
+    ad = S.block_adapter(base, adapter=0, rank=RANK)
+    rt = _contexts(base, [ad], [SCALE], 1, 64)[0]
+    stream = torch.cuda.Stream()
+    sh = int(stream.cuda_stream)
+    T = 512
+    xs = {d: torch.from_numpy(S.to_bf16_bits(S.activations(T, d)).view(np.int16)).cuda().view(torch.bfloat16)
+          for d in (4096, 14336)}
+    ys = [torch.empty((T, t.d_out), dtype=torch.float32, device="cuda") for t in base.tensors]
+    need = max((t.d_out * t.d_in * 4 + 127) // 128 * 128 + T * t.d_in * 4 for t in base.tensors) + 256
+    scratch = torch.empty(need, dtype=torch.uint8, device="cuda")
+    sp = (scratch.data_ptr() + 127) // 128 * 128
+    sb = need - (sp - scratch.data_ptr())
+
+    def step(i):
+        for j, t in enumerate(base.tensors):
+            st = q.ovl_linear_forward(rt.ctx, j, xs[t.d_in].data_ptr(), q.OVL_BF16, T, ys[j].data_ptr(),
+                                      q.OVL_PATH_JIT, sp, sb, sh)
+            if st != 0:
+                raise q.OvlError(st, q.ovl_last_error(rt.ctx))
+    steps = max(3, min(args.steps, 20))
+    ms = timed_steps(step, steps, min(args.warmup, 3), stream)
+    _check_all([rt], sh)
+    w = sum(t.d_out * t.d_in for t in base.tensors)
+    planes = sum(S.qs_bytes(base.quant, t.d_out, t.d_in) + S.d_bytes(t.d_out, t.d_in) for t in base.tensors)
+    lora = sum(RANK * (t.d_in + t.d_out) * 4 for t in base.tensors)
+    io = sum(T * (t.d_in * 2 + t.d_in * 4 * 2 + t.d_out * 4) for t in base.tensors)   # x, widened x w+r, y
+    alg_bytes = planes + lora + 2 * 4 * w + io          # S written once and read once
+    gemm_flop = sum(2 * T * t.d_out * t.d_in for t in base.tensors)
+    merge_flop = sum(2 * RANK * t.d_out * t.d_in for t in base.tensors)
+    tpk, tkind = tf32_peak()
+    hpk, hkind = peaks()
+    t_mem = alg_bytes / (hpk * 1e9) * 1e3
+    t_tc = gemm_flop / (tpk * 1e12) * 1e3
+    emit({"workload": "jit-prefill", "metric": "per-layer JIT prefill time (8B-shape q8_0 layer + r16, T=512)",
+          "unit": "ms", "value": ms, "higher_is_better": False, "steps": steps,
+          "tok_s": T / (ms / 1e3), "gemm_tflops": gemm_flop / (ms / 1e3) / 1e12,
+          "roofline": {"bound": "tensor" if t_tc > t_mem else "hbm",
+                       "ideal_ms_hbm": t_mem, "ideal_ms_tensor": t_tc, "frac": max(t_mem, t_tc) / ms,
+                       "algorithmic_bytes": alg_bytes, "gemm_flop": gemm_flop, "merge_flop": merge_flop,
+                       "hbm_peak_gbs": hpk, "tf32_peak_tflops": tpk, "note": f"{hkind}; {tkind}"},
+          "config": {"layer": "q,k,v,o,gate,up,down of the 8B block, q8_0", "adapter": "r16 s=2.0", "T": T,
+                     "x": "bf16", "path": "k_materialize -> k_widen -> k_jit_gemm per projection"}})
+
+
+WORKLOADS["jit-prefill"] = workload_jit_prefill
+
+LAYERS = 32
+
+
+class _Replicated:
+    """A payload of `copies` back-to-back copies of one layer's bytes (each
+    padded to a multiple of the 64 KiB leaf) with per-copy offsets."""
+
+    def __init__(self, one: np.ndarray, copies: int):
+        self.stride = (one.nbytes + LEAF - 1) // LEAF * LEAF
+        self.layer = np.zeros(self.stride, dtype=np.uint8)
+        self.layer[:one.nbytes] = one
+        self.copies = copies
+        self.digest = replicated_digest(self.layer, copies)
+
+
+def _layers_base(rt, copies):
+    """32 device copies of the 8B-shape q8_0 layer in one buffer, registered
+    as one base of 224 tensors (layer-major)."""
+    import torch
+    import quantized_base_lora_gb300 as q
+    one = S.block_base(S.Q8_0)
+    rep = _Replicated(one.buf, copies)
+    dev = torch.empty(copies * rep.stride, dtype=torch.uint8, device="cuda")
+    first = torch.from_numpy(rep.layer).cuda()
+    for l in range(copies):
+        dev[l * rep.stride:(l + 1) * rep.stride].copy_(first)
+    del first
+    tensors = [(l, t.proj, t.d_out, t.d_in, l * rep.stride + t.qs_off, l * rep.stride + t.d_off)
+               for l in range(copies) for t in one.tensors]
+    q.check(q.ovl_load_base(rt.ctx, S.Q8_0, tensors, dev.data_ptr(), dev.numel(), rep.digest,
+                            int(torch.cuda.current_stream().cuda_stream)), rt.ctx)
+    rt.base, rt.tensors = dev, tensors
+    return one, rep
+
+
+class _LayersAdapter:
+    """Rank-r adapter of seed `adapter` on all 7 tensors of every layer, the
+    factors of one layer repeated in every layer (payload replicated)."""
+
+    def __init__(self, one, adapter, rank, copies):
+        ad = S.block_adapter(one, adapter=adapter, rank=rank)
+        rep = _Replicated(ad.payload, copies)
+        n = len(one.tensors)
+        self.targets = [l * n + i for l in range(copies) for i in ad.targets]
+        self.ranks = [r for _ in range(copies) for r in ad.ranks]
+        self.a_off = [l * rep.stride + o for l in range(copies) for o in ad.a_off]
+        self.b_off = [l * rep.stride + o for l in range(copies) for o in ad.b_off]
+        self.payload = np.tile(rep.layer, copies)
+        self.digest = rep.digest
+
+
+def workload_decode32(args):
+    import torch
+    import quantized_base_lora_gb300 as q
+    from quantized_base_lora_gb300.runtime import Runtime
+    rt = Runtime(arena_bytes=256 << 20)
+    one, rep = _layers_base(rt, LAYERS)
+    ad = _LayersAdapter(one, 0, RANK, LAYERS)
+    st, h = rt.stage(ad, ad.digest)
+    q.check(st, rt.ctx)
+    q.check(rt.activate([h], [SCALE])[0], rt.ctx)
+    stream = torch.cuda.Stream()
+    sh = int(stream.cuda_stream)
+    xs = {d: torch.from_numpy(S.to_bf16_bits(S.activations(1, d)).view(np.int16)).cuda().view(torch.bfloat16)
+          for d in (4096, 14336)}
+    xa = {d: v.data_ptr() for d, v in xs.items()}
+    n = len(one.tensors)
+    ys = [torch.empty((1, t.d_out), dtype=torch.float32, device="cuda") for t in one.tensors]
+    yp = [y.data_ptr() for y in ys]
+    groups = [[0, 1, 2], [3], [4, 5], [6]]
+
+    def step(i):
+        for l in range(LAYERS):
+            for grp in groups:
+                xp = xa[one.tensors[grp[0]].d_in]
+                if len(grp) == 1:
+                    st = q.ovl_linear_forward(rt.ctx, l * n + grp[0], xp, q.OVL_BF16, 1, yp[grp[0]],
+                                              q.OVL_PATH_DUAL, 0, 0, sh)
+                else:
+                    st = q.ovl_linear_forward_multi(rt.ctx, [l * n + j for j in grp], xp, q.OVL_BF16, 1,
+                                                    [yp[j] for j in grp], sh)
+                if st != 0:
+                    raise q.OvlError(st, q.ovl_last_error(rt.ctx))
+    steps = max(3, min(args.steps, 50))
+    ms = timed_steps(step, steps, min(args.warmup, 3), stream)
+    _check_all([rt], sh)
+    eff = LAYERS * (effective_bytes(one, None))
+    alg = LAYERS * (algorithmic_bytes(one, None))
+    emit({"workload": "decode32", "metric": "32-layer decode tok/s (8B shape, q8_0 + r16 on all 224 tensors)",
+          "unit": "tok/s", "value": 1e3 / ms, "ms_per_token": ms, "steps": steps,
+          "effective_gbs": eff / (ms / 1e3) / 1e9,
+          "roofline": hbm_roofline(alg, ms, f"k_dualpath ({LAYERS * len(groups)} launches per token)"),
+          "config": {"base": f"{LAYERS} device copies of the 8B-shape q8_0 layer ({LAYERS * rep.stride / 1e9:.2f} GB)",
+                     "adapter": "r16 s=2.0 on all 224 tensors (one layer's factors repeated)",
+                     "x": "bf16, the same activation per d_in for every layer", "l2": "7.6 GB working set"}})
+
+
+WORKLOADS["decode32"] = workload_decode32
+
+
+def workload_switch(args):
+    """Stage a0..a2 (valid) and a3 (declared digest with its first byte
+    flipped: must fail), then 100 ops: op 2i activates a_(i mod 4) (a3:
+    re-stage, which must fail again), op 2i+1 rolls back.  Host wall time per
+    call (every call returns only when its work is done)."""
+    import torch
+    import quantized_base_lora_gb300 as q
+    from quantized_base_lora_gb300.runtime import Runtime
+    rt = Runtime(arena_bytes=768 << 20)
+    one, rep = _layers_base(rt, LAYERS)
+    ads = [_LayersAdapter(one, a, RANK, LAYERS) for a in range(4)]
+    bad = bytes([ads[3].digest[0] ^ 0xFF]) + ads[3].digest[1:]
+    lat = {"stage": [], "stage_corrupt": [], "activate": [], "rollback": []}
+    status = {}
+    handles = []
+    torch.cuda.synchronize()
+    for a in range(4):
+        t0 = time.perf_counter()
+        st, h = rt.stage(ads[a], ads[a].digest if a < 3 else bad)
+        lat["stage" if a < 3 else "stage_corrupt"].append(time.perf_counter() - t0)
+        status[st] = status.get(st, 0) + 1
+        handles.append(h)
+    for i in range(100):
+        if i % 2 == 0:
+            a = (i // 2) % 4
+            t0 = time.perf_counter()
+            if a < 3:
+                st = rt.activate([handles[a]], [SCALE])[0]
+                lat["activate"].append(time.perf_counter() - t0)
+            else:
+                st, _ = rt.stage(ads[3], bad)
+                lat["stage_corrupt"].append(time.perf_counter() - t0)
+        else:
+            t0 = time.perf_counter()
+            st = rt.rollback()[0]
+            lat["rollback"].append(time.perf_counter() - t0)
+        status[st] = status.get(st, 0) + 1
+
+    def pct(v, p):
+        return float(np.percentile(np.array(v) * 1e6, p)) if v else None
+    summary = {k: {"n": len(v), "p50_us": pct(v, 50), "p99_us": pct(v, 99), "max_us": pct(v, 100)}
+               for k, v in lat.items()}
+    st_counts = {q.STATUS_NAMES.get(k, str(k)): c for k, c in status.items()}
+    emit({"workload": "switch", "metric": "adapter activate latency p50 (32-layer, 168 MB adapters)",
+          "unit": "us", "value": summary["activate"]["p50_us"], "higher_is_better": False,
+          "latency": summary, "op_status_counts": st_counts,
+          "stage_bytes": int(ads[0].payload.nbytes),
+          "config": {"base": f"{LAYERS} layers of the 8B-shape q8_0 block (device copies)",
+                     "adapters": "4 x r16 on all 224 tensors, a3 declared digest corrupted",
+                     "ops": "100: activate a_(i mod 4) / rollback alternately"}})
+
+
+WORKLOADS["switch"] = workload_switch
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=["decode"] + sorted(WORKLOADS), default="decode")
     args = ap.parse_args()
+    if args.workload != "decode":
+        if args.impl == "reference" or args.gpus != 1:
+            print(json.dumps({"workload": args.workload, "unavailable": "measured on one GPU, our path only"}))
+            return
+        WORKLOADS[args.workload](args)
+        return
     world, rank, local = dist_setup(args.gpus)
     if args.impl == "reference":
         run_reference(args, world, rank)

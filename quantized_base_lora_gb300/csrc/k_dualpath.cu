@@ -459,19 +459,60 @@ struct EpTerm {
   uint32_t pad;
 };
 
+// Eight consecutive activations x[idx .. idx+8) (idx a multiple of 8, rows
+// 16-byte aligned): one 16-byte load for bf16, two for fp32.
+__device__ __forceinline__ void load_x8(const void* x, uint32_t xdt, size_t idx, float (&v)[8]) {
+  if (xdt == OVL_BF16) {
+    const uint4 w = *reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(x) + idx);
+    v[0] = __uint_as_float(w.x << 16); v[1] = __uint_as_float(w.x & 0xFFFF0000u);
+    v[2] = __uint_as_float(w.y << 16); v[3] = __uint_as_float(w.y & 0xFFFF0000u);
+    v[4] = __uint_as_float(w.z << 16); v[5] = __uint_as_float(w.z & 0xFFFF0000u);
+    v[6] = __uint_as_float(w.w << 16); v[7] = __uint_as_float(w.w & 0xFFFF0000u);
+  } else {
+    const float4 p = *reinterpret_cast<const float4*>(static_cast<const float*>(x) + idx);
+    const float4 q = *reinterpret_cast<const float4*>(static_cast<const float*>(x) + idx + 4);
+    v[0] = p.x; v[1] = p.y; v[2] = p.z; v[3] = p.w;
+    v[4] = q.x; v[5] = q.y; v[6] = q.z; v[7] = q.w;
+  }
+}
+
+// Term (index into this CTA's term table) that factor row rho belongs to.
+__device__ __forceinline__ uint32_t term_of_row(const EpTerm* ep, uint32_t nterm, uint32_t rho) {
+  uint32_t k = 0, base = 0;
+  while (k + 1 < nterm && rho >= base + ep[k].r) base += ep[k++].r;
+  return k;
+}
+
+// Tokens of the launch that need factor row rho: all of them, or (segmented
+// batches) those whose selected term owns the row.
+__device__ __forceinline__ uint32_t row_token_mask(const DualArgs& a, const EpTerm* ep, uint32_t nterm, uint32_t rho) {
+  uint32_t m = a.T >= 32 ? ~0u : ((1u << a.T) - 1u);
+  if (a.tok_sel) {
+    const int k = static_cast<int>(term_of_row(ep, nterm, rho));
+    m = 0;
+    for (uint32_t t = 0; t < a.T && t < 8; ++t)
+      if (a.tok_term[t] == k) m |= 1u << t;
+  }
+  return m;
+}
+
 // Partial shrink sums of this CTA's chunk of the flattened [rtot][n] factor
 // space, computed by one warp: slot (t * rtot + rho) * gs + cta receives
-// sum_{j in chunk, row rho} A[rho][j] x[t][j] (lane-strided, fixed-order warp
-// reduction), tagged with the launch epoch in one 64-bit store.  With `xw`
-// set, x comes from the staged window (single token) instead of `xsrc`.
+// sum_{j in chunk, row rho} A[rho][j] x[t][j] for every token t that needs
+// row rho, tagged with the launch epoch in one 64-bit store.  Each lane takes
+// groups of eight consecutive elements (one 16-byte activation load per
+// token); sums run in a fixed order (per lane over its groups, then a fixed
+// warp reduction).
 template <int TT>
 __device__ void shrink_chunk_warp(const DualArgs& a, const DualCfg& c, uint32_t cta, const float* sA,
-                                  const void* xsrc, const void* xw, const XWindow& win, uint32_t lane) {
+                                  const void* xsrc, const EpTerm* ep, uint32_t nterm, uint32_t lane) {
   uint64_t lo, hi;
   shrink_bounds(a, c, cta, &lo, &hi);
   unsigned long long* slots = reinterpret_cast<unsigned long long*>(a.ws.partial);
   const uint32_t rho_a = static_cast<uint32_t>(lo / a.n), rho_b = static_cast<uint32_t>((hi - 1) / a.n);
   for (uint32_t rho = rho_a; rho <= rho_b; ++rho) {
+    const uint32_t tmask = row_token_mask(a, ep, nterm, rho);
+    if (!tmask) continue;
     const uint64_t rs = static_cast<uint64_t>(rho) * a.n;
     const uint32_t j0 = static_cast<uint32_t>(max(lo, rs) - rs);
     const uint32_t j1 = static_cast<uint32_t>(min(hi, rs + a.n) - rs);
@@ -479,34 +520,35 @@ __device__ void shrink_chunk_warp(const DualArgs& a, const DualCfg& c, uint32_t 
     float acc[TT];
 #pragma unroll
     for (int t = 0; t < TT; ++t) acc[t] = 0.f;
-    if (TT == 1) {
-      // eight independent chains, combined in a fixed order
-      float c8[8];
+    if (c.xvec) {
+      constexpr int kUnroll = TT == 1 ? 2 : 1;   // loads in flight without spilling
+#pragma unroll kUnroll
+      for (uint32_t jj = (j0 & ~7u) + 8 * lane; jj < j1; jj += 256) {
+        float av[8];
 #pragma unroll
-      for (int u = 0; u < 8; ++u) c8[u] = 0.f;
-      for (uint32_t j = j0 + lane; j < j1; j += 256) {
+        for (int e = 0; e < 8; ++e) av[e] = (jj + e >= j0 && jj + e < j1) ? Arow[jj + e] : 0.f;
 #pragma unroll
-        for (int u = 0; u < 8; ++u) {
-          const uint32_t jj = j + 32 * u;
-          if (jj < j1) {
-            const float xv = xw ? load_x(xw, a.xdt, x_window_index(win, jj)) : load_x(xsrc, a.xdt, jj);
-            c8[u] = fmaf(Arow[jj], xv, c8[u]);
-          }
+        for (int t = 0; t < TT; ++t) {
+          if (!((tmask >> t) & 1u)) continue;
+          float xv[8];
+          load_x8(xsrc, a.xdt, static_cast<size_t>(t) * a.n + jj, xv);
+#pragma unroll
+          for (int e = 0; e < 8; ++e) acc[t] = fmaf(av[e], xv[e], acc[t]);
         }
       }
-      acc[0] = ((c8[0] + c8[1]) + (c8[2] + c8[3])) + ((c8[4] + c8[5]) + (c8[6] + c8[7]));
     } else {
       for (uint32_t j = j0 + lane; j < j1; j += 32) {
         const float av = Arow[j];
 #pragma unroll
         for (int t = 0; t < TT; ++t)
-          if (t < static_cast<int>(a.T)) acc[t] = fmaf(av, load_x(xsrc, a.xdt, static_cast<size_t>(t) * a.n + j), acc[t]);
+          if ((tmask >> t) & 1u) acc[t] = fmaf(av, load_x(xsrc, a.xdt, static_cast<size_t>(t) * a.n + j), acc[t]);
       }
     }
 #pragma unroll
     for (int t = 0; t < TT; ++t) {
+      if (!((tmask >> t) & 1u)) continue;
       const float v = warp_sum(acc[t]);
-      if (lane == 0 && t < static_cast<int>(a.T))
+      if (lane == 0)
         st_relaxed_u64(slots + (static_cast<size_t>(t) * a.rtot + rho) * c.gs + cta,
                        (static_cast<unsigned long long>(a.epoch) << 32) | __float_as_uint(v));
     }
@@ -519,7 +561,7 @@ __device__ void shrink_chunk_warp(const DualArgs& a, const DualCfg& c, uint32_t 
 // launch's epoch.  Each row is summed over its slots in CTA order.
 template <int NP, int PER>
 __device__ __forceinline__ void gather_rows(const DualArgs& a, const DualCfg& c, float* vsm, uint32_t base,
-                                            uint32_t lane) {
+                                            const EpTerm* ep, uint32_t nterm, uint32_t lane) {
   const unsigned long long* slots = reinterpret_cast<const unsigned long long*>(a.ws.partial);
   const uint32_t npairs = a.T * a.rtot;
   uint32_t cf[NP], cl[NP];
@@ -531,6 +573,8 @@ __device__ __forceinline__ void gather_rows(const DualArgs& a, const DualCfg& c,
     const uint32_t i = base + lane + 32 * h;
     live[h] = i < npairs;
     const uint32_t t = live[h] ? i / a.rtot : 0, rho = live[h] ? i - t * a.rtot : 0;
+    // segmented batches: a token needs only the rows of its own term
+    if (live[h] && a.tok_sel && a.tok_term[t] != static_cast<int>(term_of_row(ep, nterm, rho))) live[h] = false;
     partial_range(a, c, rho, &cf[h], &cl[h]);
     pp[h] = slots + (static_cast<size_t>(t) * a.rtot + rho) * c.gs;
     sum[h] = 0.f;
@@ -795,7 +839,7 @@ __global__ void __launch_bounds__(K1Shape<TT, RG>::threads, K1Shape<TT, RG>::min
                          (static_cast<unsigned long long>(a.epoch) << 32) | __float_as_uint(v));
       }
     } else if (cta < c.gs) {
-      shrink_chunk_warp<TT>(a, c, cta, sA, xsrc, xw, win, lane);
+      shrink_chunk_warp<TT>(a, c, cta, sA, xsrc, ep, sg.k1 - sg.k0, lane);
     }
     if (c.b_areg) {
       // The A chunk and the x window are consumed: reuse their area for this
@@ -812,8 +856,8 @@ __global__ void __launch_bounds__(K1Shape<TT, RG>::threads, K1Shape<TT, RG>::min
     }
     // v[t][rho] = sum over the shrink CTAs covering row rho, in CTA order.
     for (uint32_t base = 0; base < a.T * a.rtot; base += 64) {
-      if (a.T * a.rtot - base > 32) gather_rows<2, 6>(a, c, vsm, base, lane);
-      else gather_rows<1, 16>(a, c, vsm, base, lane);
+      if (a.T * a.rtot - base > 32) gather_rows<2, 6>(a, c, vsm, base, ep, sg.k1 - sg.k0, lane);
+      else gather_rows<1, 16>(a, c, vsm, base, ep, sg.k1 - sg.k0, lane);
     }
     cp_async_wait_all();   // B rows (when copied here) land before the release
     __syncwarp();
@@ -1190,10 +1234,11 @@ cudaError_t launch_dualpath(const DualArgs& a_in, cudaStream_t st) {
     const uint64_t chunk = (static_cast<uint64_t>(a0.rtot) * a0.n + c.gs - 1) / c.gs;
     // pieces: at most chunk + 2g elements, and at most n + g when the chunk wraps
     const uint64_t cap = std::min<uint64_t>(static_cast<uint64_t>(a0.n) + g, chunk + 2 * g);
-    c.xwin = cap * esz_x <= 8192 ? static_cast<uint32_t>(cap) : 0;
     // one index for the A chunk and the x window: every chunk shorter than a
-    // factor row (so it touches at most two), 16-byte aligned factors
-    c.shrink_vec = c.xwin && c.stage_a && a0.a16 && chunk + g < a0.n && (chunk + 24) * 4 <= 32768;
+    // factor row (so it touches at most two), 16-byte aligned factors; other
+    // launches read x from global memory (16-byte loads) in the shrink
+    c.shrink_vec = cap * esz_x <= 8192 && c.stage_a && a0.a16 && chunk + g < a0.n && (chunk + 24) * 4 <= 32768;
+    c.xwin = c.shrink_vec ? static_cast<uint32_t>(cap) : 0;
   }
   // Bytes of the B stage of the largest CTA slice (16-byte spans per term).
   uint32_t b_need = 0;

@@ -365,8 +365,12 @@ ovl_status ovl_create(ovl_ctx** out, int device, void* arena_dev, size_t arena_b
     return OVL_E_CUDA;
   }
   c->ws.status = reinterpret_cast<uint32_t*>(c->arena + kStatusOff);
+  // lower half: the dual path's partial-sum slots; upper half: scratch of the
+  // tensor-core path (widened activations, low-rank vectors)
   c->ws.partial = reinterpret_cast<float*>(c->arena + kPartialOff);
-  c->ws.partial_floats = kPartialBytes / sizeof(float);
+  c->ws.partial_floats = kPartialBytes / 2 / sizeof(float);
+  c->ws.tc_scratch = reinterpret_cast<float*>(c->arena + kPartialOff + kPartialBytes / 2);
+  c->ws.tc_scratch_bytes = kPartialBytes / 2;
   c->ws.epoch_counter = &c->slot_epoch;
   *out = c;
   return OVL_OK;
@@ -606,6 +610,38 @@ uint32_t stack_terms(ovl_ctx* c, const Composition& comp, uint32_t tensor, LoraR
   return nl;
 }
 
+// Launches of four or more tokens run on the tensor cores (K4) when the shape
+// allows: there the integer dot products would be bound by issue slots.
+constexpr uint32_t kTcMinT = 4;
+
+bool use_tc(const ovl_ctx* c, uint32_t T, const ovl_tensor_desc& td, uint32_t rtot) {
+  return T >= kTcMinT && c->ws.tc_scratch_bytes > 0 && fused_gemm_supported(td.d_out, td.d_in) &&
+         fused_gemm_scratch_bytes(T, td.d_in, rtot) <= c->ws.tc_scratch_bytes;
+}
+
+cudaError_t launch_tc(const ovl_ctx* c, const ovl_tensor_desc& td, const void* x, uint32_t xdt, uint32_t T, float* y,
+                      const LoraRef* terms, uint32_t nl, uint32_t rtot, const int8_t* tok, cudaStream_t st) {
+  FusedLaunch L{};
+  L.qs = c->base + td.qs_off;
+  L.dpl = c->base + td.d_off;
+  L.quant = c->quant;
+  L.m = td.d_out;
+  L.n = td.d_in;
+  L.x = x;
+  L.xdt = xdt;
+  L.T = T;
+  L.y = y;
+  L.nl = nl;
+  L.rtot = rtot;
+  for (uint32_t k = 0; k < nl; ++k) L.lora[k] = terms[k];
+  L.tok_sel = tok != nullptr;
+  L.tok_host = tok;
+  L.scratch = c->ws.tc_scratch;
+  L.scratch_bytes = c->ws.tc_scratch_bytes;
+  L.status = c->ws.status;
+  return launch_fused_gemm(L, st);
+}
+
 // One event per forward call: forward work on a context is stream-ordered, so
 // once the latest record has completed every earlier forward has too.
 ovl_status record_use(ovl_ctx* c, const std::vector<Adapter*>& used, cudaStream_t st) {
@@ -668,10 +704,13 @@ ovl_status ovl_linear_forward(ovl_ctx* ctx, uint32_t tensor, const void* x, uint
   uint32_t rtot;
   std::vector<Adapter*> used;
   const uint32_t nl = stack_terms(ctx, *ctx->active, tensor, terms, &rtot, &used);
-  if (path == OVL_PATH_DUAL) {
+  if (path == OVL_PATH_DUAL && use_tc(ctx, T, td, rtot)) {
+    cudaError_t e = launch_tc(ctx, td, x, x_dtype, T, y, terms, nl, rtot, nullptr, st);
+    if (e != cudaSuccess) return cuda_fail(ctx, e, "tensor-core launch");
+  } else if (path == OVL_PATH_DUAL) {
     DualArgs a{};
     a.b_pad = 1;   // factors live in the arena: 16-byte aligned, allocations rounded to 256 bytes
-  a.a16 = 1;
+    a.a16 = 1;
     a.qs = ctx->base + td.qs_off;
     a.dpl = ctx->base + td.d_off;
     a.m = td.d_out;
@@ -729,6 +768,30 @@ ovl_status ovl_linear_forward_multi(ovl_ctx* ctx, uint32_t n, const uint32_t* te
   if (T == 0) return ok(ctx);
   if (!x) return fail(ctx, OVL_E_ARG, "null activation");
   DeviceGuard g(ctx->device);
+  {
+    // multi-token: one tensor-core launch per tensor when every tensor allows it
+    bool tc_all = true;
+    for (uint32_t i = 0; i < n && tc_all; ++i) {
+      LoraRef terms[OVL_MAX_STACK];
+      uint32_t rt;
+      std::vector<Adapter*> tmp;
+      stack_terms(ctx, *ctx->active, tensors[i], terms, &rt, &tmp);
+      tc_all = use_tc(ctx, T, ctx->tensors[tensors[i]], rt);
+    }
+    if (tc_all) {
+      cudaStream_t st = static_cast<cudaStream_t>(stream);
+      std::vector<Adapter*> used;
+      for (uint32_t i = 0; i < n; ++i) {
+        LoraRef terms[OVL_MAX_STACK];
+        uint32_t rt;
+        const uint32_t nl = stack_terms(ctx, *ctx->active, tensors[i], terms, &rt, &used);
+        cudaError_t e = launch_tc(ctx, ctx->tensors[tensors[i]], x, x_dtype, T, ys[i], terms, nl, rt, nullptr, st);
+        if (e != cudaSuccess) return cuda_fail(ctx, e, "tensor-core launch");
+      }
+      if (ovl_status s = record_use(ctx, used, st)) return s;
+      return ok(ctx);
+    }
+  }
   DualArgs a{};
   a.b_pad = 1;   // factors live in the arena: 16-byte aligned, allocations rounded to 256 bytes
   a.a16 = 1;
@@ -831,7 +894,9 @@ ovl_status ovl_segmented_forward(ovl_ctx* ctx, uint32_t tensor, const void* x, u
   a.tok_sel = 1;
   a.tok_host = tok.data();
   a.ws = ctx->ws;
-  cudaError_t e = launch_dualpath(a, st);
+  cudaError_t e = use_tc(ctx, T, td, a.rtot)
+                      ? launch_tc(ctx, td, x, x_dtype, T, y, a.lora, a.nl, a.rtot, tok.data(), st)
+                      : launch_dualpath(a, st);
   if (e != cudaSuccess) return cuda_fail(ctx, e, "segmented launch");
   if (ovl_status s = record_use(ctx, used, st)) return s;
   return ok(ctx);

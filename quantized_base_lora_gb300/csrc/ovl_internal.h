@@ -39,6 +39,8 @@ struct Workspace {
   float* partial;                 // partial-sum slots (device), 8 bytes each
   size_t partial_floats;          // size of that region in floats
   uint32_t* epoch_counter;        // host: last epoch handed out
+  float* tc_scratch;              // tensor-core path scratch (device, 256-byte aligned)
+  size_t tc_scratch_bytes;        // 0: the tensor-core path is not available
 };
 
 // One tensor of a (multi-tensor) dual-path launch.  All tensors of a launch
@@ -55,6 +57,7 @@ struct DualSeg {
 };
 
 constexpr int kMaxMulti = 4;
+constexpr uint32_t kTokTile = 64;       // tokens per tensor-core launch
 
 // Fused dual-path forward over a token chunk (T <= 8).  Single-tensor callers
 // fill qs/dpl/m/y; multi-tensor callers fill nseg and seg[] (qs, dpl, y, m,
@@ -86,6 +89,28 @@ struct DualArgs {
   LoraRef lora[OVL_MAX_TABLE];
   const int8_t* tok_host;  // host array of T entries (launcher only)
 };
+
+// Dual path on the tensor cores (K4) for multi-token launches of one tensor:
+// token chunks of kTokTile, each widen -> shrink -> fused dequantizing GEMM.
+struct FusedLaunch {
+  const uint8_t* qs;
+  const uint8_t* dpl;
+  uint32_t quant, m, n;
+  const void* x;            // [T][n], fp32 or bf16
+  uint32_t xdt, T;
+  float* y;                 // [T][m]
+  uint32_t nl, rtot;
+  LoraRef lora[OVL_MAX_TABLE];
+  uint32_t tok_sel;         // segmented: token t adds only term tok_host[t] (-1: none)
+  const int8_t* tok_host;   // host, T entries
+  float* scratch;           // widened activations + low-rank vectors
+  size_t scratch_bytes;
+  uint32_t* status;
+};
+// d_in a multiple of 256 (the f16 scale rows feed 16-byte tensor-map boxes).
+bool fused_gemm_supported(uint32_t m, uint32_t n);
+size_t fused_gemm_scratch_bytes(uint32_t T, uint32_t n, uint32_t rtot);
+cudaError_t launch_fused_gemm(const FusedLaunch& L, cudaStream_t st);
 
 // Materialize S = deq(W) + sum_k s_k B_k A_k into fp32 scratch [m][n].
 struct MatArgs {
