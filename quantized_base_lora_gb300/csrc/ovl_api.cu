@@ -610,9 +610,9 @@ uint32_t stack_terms(ovl_ctx* c, const Composition& comp, uint32_t tensor, LoraR
   return nl;
 }
 
-// Launches of four or more tokens run on the tensor cores (K4) when the shape
+// Launches of sixteen or more tokens run on the tensor cores (K4) when the shape
 // allows: there the integer dot products would be bound by issue slots.
-constexpr uint32_t kTcMinT = 4;
+constexpr uint32_t kTcMinT = 16;
 
 bool use_tc(const ovl_ctx* c, uint32_t T, const ovl_tensor_desc& td, uint32_t rtot) {
   return T >= kTcMinT && c->ws.tc_scratch_bytes > 0 && fused_gemm_supported(td.d_out, td.d_in) &&

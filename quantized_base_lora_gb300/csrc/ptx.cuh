@@ -60,6 +60,18 @@ __device__ __forceinline__ uint64_t global_ns() {
   return t;
 }
 
+// Bounded wait that keeps polling (no suspension): for dedicated role threads
+// whose next step is latency-critical.  Gives up after about two seconds.
+__device__ __forceinline__ bool mbar_wait_spin(uint64_t* bar, uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = global_ns();
+  for (uint32_t it = 0; it < (1u << 30); ++it) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((it & 255) == 255 && global_ns() - t0 > 2000000000ull) return false;
+  }
+  return false;
+}
+
 // Bounded wait on a barrier phase: returns false if it gave up after about
 // two seconds (checked on the global timer) or 2^24 attempts.
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity) {

@@ -243,3 +243,37 @@ def test_multi_tensor_launch_rejects_mixed_d_in(block_q8):
     assert st == q.OVL_E_SHAPE
     st = q.ovl_linear_forward_multi(rt.ctx, [0, 1, 2, 3, 4], xd.data_ptr(), q.OVL_F32, 1, [ys[0].data_ptr()] * 5)
     assert st == q.OVL_E_ARG
+
+
+# ----------------------------------------------------------------- tensor-core path (16+ tokens)
+TC_CASES = [  # (quant, d_out, d_in, T, ranks, xdtype): token chunks of 64, ragged rows and tokens
+    (S.Q8_0, 1000, 4096, 64, (16, 64), "bf16"),
+    (S.Q8_0, 300, 2048, 512, (8,), "bf16"),
+    (S.Q4_0, 777, 1024, 100, (5, 3), "f32"),
+    (S.Q8_0, 129, 256, 16, (), "f32"),
+]
+
+
+@pytest.mark.parametrize("case", TC_CASES, ids=[f"q{c[0]}_{c[1]}x{c[2]}_T{c[3]}_r{'-'.join(map(str, c[4]))}_{c[5]}"
+                                                for c in TC_CASES])
+def test_tensor_core_path(case):
+    require_gpu()
+    quant, m, n, T, ranks, xdt = case
+    rng = np.random.default_rng(m + 31 * n + T)
+    W = S.gaussian(rng, (m, n), 0.02)
+    base = S.build_base(quant, [(0, 0, W)])
+    ads = []
+    for k, r in enumerate(ranks):
+        A = S.gaussian(rng, (r, n), 0.01)
+        B = S.gaussian(rng, (m, r), 0.01)
+        ads.append((S.build_adapter(base, [0], [r], [(A, B)]), [2.0, 0.5][k % 2]))
+    rt = make_runtime(base, arena_bytes=64 << 20)
+    hs = [stage(rt, ad) for ad, _ in ads]
+    assert rt.activate(hs, [s for _, s in ads])[0] == 0
+    x = S.gaussian(rng, (T, n), 1.0)
+    xd, x64 = x_device(x, xdt)
+    y = fwd(rt, 0, xd)
+    assert_within_bound(y, deq_of(base, 0), lora_terms(ads, 0), x64, str(case))
+    y2 = fwd(rt, 0, xd)                                  # deterministic
+    assert np.array_equal(y.view(np.uint32), y2.view(np.uint32))
+    rt.close()
