@@ -14,22 +14,28 @@
 // kernel dequantizes on the way into the tensor cores instead of materializing
 // the layer:
 //  * one CTA per 128-row tile of W and per tile of up to 64 tokens (UMMA M = 128,
-//    N = token tile rounded up to 16);
-//  * producer (warp 0, one thread): every 8 K-blocks (K-block = 32 weights,
-//    exactly one quantization block per row) one TMA 2-D copy of the tile's raw
-//    codes for those 8 blocks (one 128 / 256-byte run per row) and one of their
-//    f16 scales; per K-block the fp32 activations (128-byte swizzle);
-//  * converters (warps 2..9, two per TMEM lane quarter, 16 weights of a row
-//    each): d * q in fp32 (exact: 11 x 8 significant bits), stored straight
-//    into tensor memory (row r in lane r, K along columns) with tcgen05.st --
+//    N = token tile rounded up to 16); a pipeline stage is 4 K-blocks (128
+//    weights; a K-block is one quantization block);
+//  * code-group producer (one thread, own warp): every 8 K-blocks one TMA copy
+//    of the tile's raw codes (128-byte swizzle, so the 32 rows a converter warp
+//    reads hit different banks) and one of their f16 scales, several groups
+//    ahead; the weights are immutable, so it starts before the kernels that
+//    produce the activations have finished;
+//  * activation producer (warp 0, one thread): one 3-D TMA box per stage, the
+//    4 K-blocks' fp32 activation tiles (128-byte swizzle);
+//  * converters (16 warps, four per TMEM lane quarter, one K-block each):
+//    d (q - bias) in fp32, exactly (one byte permute and one FMA per weight),
+//    stored straight into tensor memory (row r in lane r, K along columns) --
 //    the dequantized operand never touches shared memory;
-//  * MMA issuer (warp 1, one thread): tcgen05.mma.kind::tf32 (K = 8) with A in
-//    TMEM and the activations in shared memory, accumulator in TMEM;
-//    tcgen05.commit frees each stage;
-//  * epilogue (warps 2..5, one TMEM lane quarter each): accumulator + the
-//    low-rank term from v (computed by k_shrink), stored to Y.
-// TF32 keeps 10 explicit mantissa bits of d*q (|error| <= 2^-10 |w|); the
-// activations (bf16, or fp32 rounded by the tensor core) likewise; fp32
+//  * MMA issuers (four threads, one warp each): a thread can issue a
+//    tcgen05.mma only every ~110 cycles, while an M = 128, N = 64, K = 8 tf32
+//    MMA keeps the tensor core busy for ~37, so issuer w takes K-block w of
+//    every stage into its own accumulator; tcgen05.commit frees each stage;
+//  * epilogue (four converter warps, one TMEM lane quarter each): the
+//    accumulators summed in a fixed order, stored to Y.  The low-rank term runs
+//    as extra K-blocks (A = the B factors' rows, B = s v from k_shrink).
+// TF32 keeps 10 explicit mantissa bits of d (q - bias) (|error| <= 2^-10 |w|);
+// the activations (bf16, or fp32 rounded by the tensor core) likewise; fp32
 // accumulation.  Every wait is bounded and latches a status code.
 #include <cuda.h>
 #include <cuda_fp16.h>
@@ -46,39 +52,96 @@ namespace {
 
 constexpr uint32_t BM = 128;              // rows of W per CTA (UMMA M)
 constexpr uint32_t BK = 32;               // weights per K-block: one quantization block
-constexpr uint32_t kDGroup = 8;           // K-blocks per scale tile
+constexpr uint32_t kSub = 4;              // K-blocks per pipeline stage (128 weights)
+constexpr uint32_t kStageCols = kSub * BK;   // TMEM columns of one stage's weight operand
+constexpr uint32_t kDGroup = 8;           // K-blocks per code group (two stages)
 constexpr uint32_t kDBytes = BM * kDGroup * 2;   // one scale tile: 128 rows x 8 f16
-constexpr uint32_t kMaxStages = 14;
+// One thread can issue a tcgen05.mma only every ~110 cycles, while an M = 128,
+// N = 64, K = 8 tf32 MMA takes the tensor core ~37: several issuing threads,
+// each with its own accumulator over its own share of K, keep it busy.
+constexpr uint32_t kIssuers = 4;          // MMA-issuing threads (lane 0 of warps 1 .. kIssuers)
+constexpr uint32_t kKbPerIssuer = kSub / kIssuers;
+constexpr uint32_t kTmemCols = 512;       // accumulators (bn columns each), then the stages' weight operands
+constexpr uint32_t kMaxStages = 3;
+constexpr uint32_t kMaxGroups = 4;
 constexpr uint32_t kSmemCap = 220 * 1024;
-constexpr uint32_t kTmemCols = 512;       // accumulator at columns [0, 64), A stages at 64 + 32 s
-constexpr uint32_t kAcol = 64;
-constexpr uint32_t kConvWarps = 8;        // two threads per tile row
-constexpr uint32_t kThreads = (2 + kConvWarps) * 32;   // producer, MMA issuer, converters
+constexpr uint32_t kConvWarps = 16;       // four per TMEM lane quarter: one K-block of a stage each
+constexpr uint32_t kConv0 = 1 + kIssuers;   // first converter warp
+constexpr uint32_t kGroupWarp = kConv0 + kConvWarps;   // code-group producer
+constexpr uint32_t kThreads = (kGroupWarp + 1) * 32;   // producer, MMA issuers, converters, group producer
 constexpr uint32_t kTimeoutFused = 5;
+static_assert(kSub % kIssuers == 0, "stage split");
+static_assert(kIssuers * kTokTile + 2 * kStageCols <= kTmemCols, "TMEM budget: two stages at the widest token tile");
 
 struct FusedArgs {
   uint32_t m, n, T, quant;
   uint32_t bn;            // UMMA N (multiple of 16, <= kTokTile)
-  uint32_t ns;            // pipeline depth
+  uint32_t ns;            // pipeline stages (activation tiles + TMEM weight operands)
+  uint32_t acol;          // first TMEM column of the weight operands: kIssuers bn
+  uint32_t ng;            // code-group buffers
   uint32_t kblocks;       // n / 32
+  uint32_t bstages;       // base stages: kblocks / kSub
+  uint32_t lkb;           // K-blocks of the low-rank term (ranks in chunks of 32)
   uint32_t qrow;          // raw code bytes per row and K-block (32 or 16)
-  uint32_t b_off;         // offset of the B tile in a stage
-  uint32_t gbytes;        // one code group: scales (kDBytes) then codes (BM x 8 qrow)
-  uint32_t stage_bytes;
+  uint32_t gbytes;        // one code group: codes (128-byte swizzled boxes) then scales
+  uint32_t xbytes;        // one activation tile: bn rows x 128 bytes
+  uint32_t stage_bytes;   // kSub activation tiles (one 3-D box)
   uint32_t tmem_cols;
   uint32_t idesc;
-  uint32_t lkb;           // extra K-blocks of the low-rank term (ranks in chunks of 32)
   uint32_t nl, rtot;
   float* y;
   uint32_t* status;
   LoraRef lora[OVL_MAX_TABLE];
 };
 
-// Four consecutive weights of one 32-bit word as floats, exactly: the byte goes
-// into the low mantissa bits of 2^23 (one byte permute) and 2^23 + bias comes
-// off again (exact); `bias` = 128 for offset-binary int8, 8 for q4 codes.
-__device__ __forceinline__ float byte_value(uint32_t word, uint32_t b, float bias) {
-  return __int_as_float(static_cast<int>(__byte_perm(word, 0x4B000000u, 0x7540u + b))) - (8388608.f + bias);
+// Byte b of a 32-bit word placed at mantissa bits 8..15 of 2^15: the float
+// 2^15 + byte, in one byte permute.
+__device__ __forceinline__ float magic15(uint32_t word, uint32_t b) {
+  return __int_as_float(static_cast<int>(__byte_perm(word, 0x47000000u, 0x7404u | (b << 4))));
+}
+
+// Byte offset of 16-byte chunk c of row r in a tile written by TMA with the
+// 128-byte swizzle (rows of 128 bytes; chunk c of row r lands at c ^ (r mod 8)).
+__device__ __forceinline__ uint32_t sw128_off(uint32_t r, uint32_t c) { return r * 128u + ((c ^ (r & 7u)) << 4); }
+
+// One K-block (32 weights) of row r, dequantized to d (q - bias) in fp32,
+// exactly: with f = 2^15 + q, fma(f, d, -d (2^15 + bias)) is d (q - bias)
+// rounded once, and both d (2^15 + bias) (at most 11 + 13 significant bits)
+// and d (q - bias) (at most 11 + 8) are representable.  `codes` is the group's
+// code area, `kbg` the K-block within the group.
+__device__ __forceinline__ void dequant_kblock(const uint8_t* codes, uint32_t quant, uint32_t r, uint32_t kbg, float d,
+                                               uint32_t (&bits)[32]) {
+  if (quant == OVL_Q8_0) {
+    // two boxes of 4 K-blocks; a K-block is two chunks; int8 made offset-binary
+    // (bias 128) by flipping the sign bits
+    const float c = -d * (32768.f + 128.f);
+    const uint8_t* box = codes + (kbg >> 2) * (BM * 128u);
+    const uint32_t ch = 2u * (kbg & 3u);
+    const uint4 q0 = *reinterpret_cast<const uint4*>(box + sw128_off(r, ch));
+    const uint4 q1 = *reinterpret_cast<const uint4*>(box + sw128_off(r, ch + 1));
+    const uint32_t words[8] = {q0.x, q0.y, q0.z, q0.w, q1.x, q1.y, q1.z, q1.w};
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const uint32_t u = words[i] ^ 0x80808080u;
+#pragma unroll
+      for (int b = 0; b < 4; ++b) bits[4 * i + b] = __float_as_uint(fmaf(magic15(u, b), d, c));
+    }
+  } else {
+    // one box of 8 K-blocks; a K-block is one chunk, byte p holding elements
+    // 2p (low nibble) and 2p + 1 (high nibble); bias 8
+    const float c = -d * (32768.f + 8.f);
+    const uint4 q = *reinterpret_cast<const uint4*>(codes + sw128_off(r, kbg));
+    const uint32_t words[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const uint32_t lo = words[i] & 0x0F0F0F0Fu, hi = (words[i] >> 4) & 0x0F0F0F0Fu;
+#pragma unroll
+      for (int b = 0; b < 4; ++b) {
+        bits[8 * i + 2 * b] = __float_as_uint(fmaf(magic15(lo, b), d, c));
+        bits[8 * i + 2 * b + 1] = __float_as_uint(fmaf(magic15(hi, b), d, c));
+      }
+    }
+  }
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -87,14 +150,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                  const FusedArgs g) {
   extern __shared__ __align__(1024) uint8_t sm_raw[];
   uint8_t* sm = sm_raw + ((1024u - (smem_u32(sm_raw) & 1023u)) & 1023u);
-  uint8_t* tiles = sm;                                   // ns x (A | B | raw codes)
-  uint8_t* gring = sm + g.ns * g.stage_bytes;            // 2 code groups (scales + codes)
-  uint64_t* full = reinterpret_cast<uint64_t*>(gring + 2 * g.gbytes);
+  uint8_t* tiles = sm;                                   // ns x kSub activation tiles
+  uint8_t* gring = sm + g.ns * g.stage_bytes;            // ng code groups (codes, then scales)
+  uint64_t* full = reinterpret_cast<uint64_t*>(gring + g.ng * g.gbytes);
   uint64_t* empty = full + kMaxStages;
-  uint64_t* conv = empty + kMaxStages;
-  uint64_t* dfull = conv + kMaxStages;
-  uint64_t* dempty = dfull + 2;
-  uint64_t* accum = dempty + 2;
+  uint64_t* conv = empty + kMaxStages;     // [issuer][stage]
+  uint64_t* dfull = conv + kIssuers * kMaxStages;
+  uint64_t* dempty = dfull + kMaxGroups;
+  uint64_t* accum = dempty + kMaxGroups;
   uint32_t* s_taddr = reinterpret_cast<uint32_t*>(accum + 1);
 
   const uint32_t warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -109,14 +172,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 32) {
     for (uint32_t i = 0; i < g.ns; ++i) {
       mbar_init(&full[i], 1);
-      mbar_init(&empty[i], 1);
-      mbar_init(&conv[i], kConvWarps);   // one arrival per converter warp
+      mbar_init(&empty[i], kIssuers);    // one commit per issuer
+      for (uint32_t w = 0; w < kIssuers; ++w)
+        mbar_init(&conv[w * kMaxStages + i], kConvWarps / kIssuers);   // the converters of its K-blocks
     }
-    for (uint32_t i = 0; i < 2; ++i) {
+    for (uint32_t i = 0; i < g.ng; ++i) {
       mbar_init(&dfull[i], 1);
       mbar_init(&dempty[i], kConvWarps);
     }
-    mbar_init(accum, 1);
+    mbar_init(accum, kIssuers);
     mbar_fence_init();
   }
   tc_fence_before();
@@ -125,164 +189,176 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t taddr = *s_taddr;
   griddep_launch_dependents();
 
-  const uint32_t ktot = g.kblocks + g.lkb;   // base K-blocks, then the low-rank ones
+  // Stages: kSub K-blocks each; the base ones, then the low-rank ones (the last
+  // may hold fewer K-blocks).
+  const uint32_t stot = g.bstages + (g.lkb + kSub - 1) / kSub;
+  auto nsub = [&](uint32_t s) { return s < g.bstages ? kSub : min(kSub, g.lkb - (s - g.bstages) * kSub); };
   // Each CTA walks the base K-blocks from its own group onwards (wrapping), so
   // the CTAs of a launch read different activation tiles at any moment
   // instead of all asking the same few L2 lines for the same tile.  d_in is a
-  // multiple of 256 here: group boundaries stay aligned.  The order is fixed
+  // multiple of 256 here: stages and groups stay aligned.  The order is fixed
   // per CTA: results are deterministic.
   const uint32_t rot = (blockIdx.x % (g.kblocks / kDGroup)) * kDGroup;
-  auto kdata = [&](uint32_t kb) { return kb < g.kblocks ? (kb + rot) % g.kblocks : kb; };
+  auto kdata = [&](uint32_t kb) { return (kb + rot) % g.kblocks; };
   if (warp == 0 && lane == 0) {
-    // ---- producer
+    // ---- activation producer
+    prefetch_tensormap(&tmX);
+    prefetch_tensormap(&tmV);
     griddep_wait();   // the widened activations and s v come from preceding kernels
-    for (uint32_t kb = 0; kb < ktot; ++kb) {
-      const uint32_t st = kb % g.ns;
-      const bool base = kb < g.kblocks;
-      if (base && kb % kDGroup == 0) {
-        const uint32_t dg = kb / kDGroup, ds = dg & 1;
-        if (dg >= 2 && !mbar_wait_spin(&dempty[ds], ((dg / 2) - 1) & 1)) {
-          latch_status(g.status, kTimeoutFused);
-          break;
-        }
-        uint8_t* grp = gring + ds * g.gbytes;
-        mbar_arrive_expect_tx(&dfull[ds], g.gbytes);
-        const uint32_t dgd = kdata(kb) / kDGroup;   // the group's data
-        tma_load_2d(grp, &tmD, static_cast<int32_t>(dgd * kDGroup), static_cast<int32_t>(m0), &dfull[ds]);
-        tma_load_2d(grp + kDBytes, &tmQ, static_cast<int32_t>(dgd * kDGroup * g.qrow), static_cast<int32_t>(m0),
-                    &dfull[ds]);
-      }
-      if (kb >= g.ns && !mbar_wait_spin(&empty[st], ((kb / g.ns) - 1) & 1)) {
+    for (uint32_t s = 0; s < stot; ++s) {
+      const uint32_t st = s % g.ns;
+      const bool base = s < g.bstages;
+      if (s >= g.ns && !mbar_wait_spin(&empty[st], ((s / g.ns) - 1) & 1)) {
         latch_status(g.status, kTimeoutFused);
         break;
       }
+      // the stage's kSub activation tiles in one box {32, bn, kSub} (token rows
+      // and K-blocks past the ends read as zero)
       uint8_t* stg = tiles + st * g.stage_bytes;
-      if (base) {
-        mbar_arrive_expect_tx(&full[st], g.bn * 128);
-        tma_load_2d(stg + g.b_off, &tmX, 0, static_cast<int32_t>(kdata(kb) * g.T + n0), &full[st]);
-      } else {
-        mbar_arrive_expect_tx(&full[st], g.bn * 128);
-        tma_load_2d(stg + g.b_off, &tmV, static_cast<int32_t>((kb - g.kblocks) * BK), static_cast<int32_t>(n0),
-                    &full[st]);
-      }
+      mbar_arrive_expect_tx(&full[st], g.stage_bytes);
+      if (base)
+        tma_load_3d(stg, &tmX, 0, static_cast<int32_t>(n0), static_cast<int32_t>(kdata(s * kSub)), &full[st]);
+      else
+        tma_load_3d(stg, &tmV, 0, static_cast<int32_t>(n0), static_cast<int32_t>((s - g.bstages) * kSub), &full[st]);
     }
-  } else if (warp == 1 && lane == 0) {
-    // ---- MMA issuer
-    for (uint32_t kb = 0; kb < ktot; ++kb) {
-      const uint32_t st = kb % g.ns;
-      if (!mbar_wait_spin(&conv[st], (kb / g.ns) & 1) || !mbar_wait_spin(&full[st], (kb / g.ns) & 1)) {
+  } else if (warp == kGroupWarp && lane == 0) {
+    // ---- code-group producer: raw codes and scales of two stages per group,
+    // up to ng groups ahead of the converters.  The base weights are
+    // immutable, so this starts before the preceding kernels have finished.
+    prefetch_tensormap(&tmQ);
+    prefetch_tensormap(&tmD);
+    for (uint32_t dg = 0; dg < g.bstages / 2; ++dg) {
+      const uint32_t ds = dg % g.ng;
+      if (dg >= g.ng && !mbar_wait_bounded(&dempty[ds], ((dg / g.ng) - 1) & 1)) {
+        latch_status(g.status, kTimeoutFused);
+        break;
+      }
+      uint8_t* grp = gring + ds * g.gbytes;
+      mbar_arrive_expect_tx(&dfull[ds], g.gbytes);
+      const uint32_t kb0 = kdata(dg * kDGroup);   // the group's data: a multiple of 8 K-blocks
+      for (uint32_t b = 0; b < g.qrow / 16; ++b)   // 128-byte boxes: q4 one, q8 two
+        tma_load_2d(grp + b * (BM * 128u), &tmQ, static_cast<int32_t>(kb0 * g.qrow + b * 128u),
+                    static_cast<int32_t>(m0), &dfull[ds]);
+      tma_load_2d(grp + BM * kDGroup * g.qrow, &tmD, static_cast<int32_t>(kb0), static_cast<int32_t>(m0), &dfull[ds]);
+    }
+  } else if (warp >= 1 && warp <= kIssuers && lane == 0) {
+    // ---- MMA issuers: issuer w takes K-blocks [w kKbPerIssuer, (w + 1) kKbPerIssuer)
+    // of every stage into its own accumulator (columns [w bn, (w + 1) bn))
+    const uint32_t w = warp - 1, j0 = w * kKbPerIssuer;
+    const uint32_t dacc = taddr + w * g.bn;
+    for (uint32_t s = 0; s < stot; ++s) {
+      const uint32_t st = s % g.ns, ph = (s / g.ns) & 1;
+      if (!mbar_wait_spin(&conv[w * kMaxStages + st], ph) || !mbar_wait_spin(&full[st], ph)) {
         latch_status(g.status, kTimeoutFused);
         break;
       }
       tc_fence_after();
-      const uint64_t bdesc = sdesc_sw128(smem_u32(tiles + st * g.stage_bytes + g.b_off));
-      const uint32_t acol = taddr + kAcol + BK * st;
+      const uint32_t acol = taddr + g.acol + kStageCols * st;
+      // K = 8 tf32 per instruction: 8 TMEM columns of A, 32 bytes of each B row
+      const uint64_t b0 = sdesc_sw128(smem_u32(tiles + st * g.stage_bytes));
+      const uint64_t bstep = static_cast<uint64_t>(g.xbytes >> 4);   // next tile, in descriptor address units
+      if (s < g.bstages) {
 #pragma unroll
-      for (uint32_t k = 0; k < BK / 8; ++k)   // K = 8 tf32 per instruction: 8 TMEM columns, 32 bytes of B
-        umma_tf32_ts(taddr, acol + 8 * k, bdesc + 2 * k, g.idesc, (kb | k) != 0);
+        for (uint32_t i = 0; i < kKbPerIssuer * (BK / 8); ++i) {
+          const uint32_t j = j0 + (i >> 2), kk = i & 3u;
+          umma_tf32_ts(dacc, acol + BK * j + 8 * kk, b0 + j * bstep + 2u * kk, g.idesc, (s | i) != 0);
+        }
+      } else {
+        const uint32_t nk = nsub(s);
+        for (uint32_t j = j0; j < j0 + kKbPerIssuer && j < nk; ++j)
+          for (uint32_t kk = 0; kk < BK / 8; ++kk)
+            umma_tf32_ts(dacc, acol + BK * j + 8 * kk, b0 + j * bstep + 2u * kk, g.idesc, 1u);
+      }
       umma_commit(&empty[st]);
     }
     umma_commit(accum);
-  } else if (warp >= 2) {
-    // ---- converters: weights [16 h, 16 h + 16) of row r = TMEM lane r; a warp
-    // may only reach its own lane quarter (warp mod 4)
-    const uint32_t quarter = warp & 3u, h = (warp - 2) >> 2, r = quarter * 32 + lane;
-    bool pending = false;
-    uint32_t pend_st = 0;
-    for (uint32_t kb = 0; kb < ktot; ++kb) {
-      const uint32_t st = kb % g.ns;
-      const bool base = kb < g.kblocks;
-      const uint32_t dg = kb / kDGroup, ds = dg & 1;
-      if (base && kb % kDGroup == 0 && !mbar_wait_spin(&dfull[ds], (dg / 2) & 1)) {
+  } else if (warp >= kConv0 && warp < kConv0 + kConvWarps) {
+    // ---- converters: row r = TMEM lane r (a warp reaches only its own lane
+    // quarter, warp mod 4); warp h of a quarter takes K-block h of each stage
+    const uint32_t quarter = warp & 3u, h = (warp - kConv0) >> 2, r = quarter * 32 + lane;
+    uint64_t* myconv = conv + (h / kKbPerIssuer) * kMaxStages;
+    const uint32_t lanes = taddr + ((quarter * 32u) << 16);
+    for (uint32_t s = 0; s < stot; ++s) {
+      const uint32_t st = s % g.ns;
+      const bool base = s < g.bstages;
+      const uint32_t dg = s >> 1, ds = dg % g.ng;
+      if (base && (s & 1u) == 0 && !mbar_wait_spin(&dfull[ds], (dg / g.ng) & 1)) {
         latch_status(g.status, kTimeoutFused);
         break;
       }
-      // TMEM buffer st is free once the MMAs of K-block kb - ns completed (the
-      // converters never read the activation tile)
-      if (kb >= g.ns && !mbar_wait_spin(&empty[st], ((kb / g.ns) - 1) & 1)) {
+      // the weight operand of stage st is free once the MMAs of stage s - ns
+      // completed (the converters never read the activation tiles)
+      if (s >= g.ns && !mbar_wait_spin(&empty[st], ((s / g.ns) - 1) & 1)) {
         latch_status(g.status, kTimeoutFused);
         break;
       }
-      float w[16];
+      const uint32_t col = lanes + g.acol + kStageCols * st;
       if (base) {
         const uint8_t* grp = gring + ds * g.gbytes;
-        const float d = __half2float(reinterpret_cast<const __half*>(grp)[r * kDGroup + kb % kDGroup]);
-        const uint8_t* qrowp = grp + kDBytes + r * (kDGroup * g.qrow) + (kb % kDGroup) * g.qrow;
-        if (g.quant == OVL_Q8_0) {
-          const uint4 q = *reinterpret_cast<const uint4*>(qrowp + h * 16);
-          const uint32_t words[4] = {q.x ^ 0x80808080u, q.y ^ 0x80808080u, q.z ^ 0x80808080u, q.w ^ 0x80808080u};
-#pragma unroll
-          for (int i = 0; i < 4; ++i)
-#pragma unroll
-            for (int b = 0; b < 4; ++b) w[4 * i + b] = d * byte_value(words[i], b, 128.f);
-        } else {
-          const uint2 q = *reinterpret_cast<const uint2*>(qrowp + h * 8);
-          const uint32_t words[2] = {q.x, q.y};
-#pragma unroll
-          for (int i = 0; i < 2; ++i) {
-            const uint32_t lo = words[i] & 0x0F0F0F0Fu, hi = (words[i] >> 4) & 0x0F0F0F0Fu;
-#pragma unroll
-            for (int b = 0; b < 4; ++b) {   // element 2p in the low nibble, 2p+1 in the high one
-              w[8 * i + 2 * b] = d * byte_value(lo, b, 8.f);
-              w[8 * i + 2 * b + 1] = d * byte_value(hi, b, 8.f);
-            }
-          }
-        }
-      } else {
-        // low-rank K-block j: ranks 32 j + [16 h, 16 h + 16) of B (all terms,
-        // concatenated in order), row m0 + r; zero past the ranks or the rows
+        const uint32_t kbg = (s & 1u) * kSub + h;   // this warp's K-block within the group
+        const float d =
+            __half2float(*reinterpret_cast<const __half*>(grp + BM * kDGroup * g.qrow + r * (kDGroup * 2) + kbg * 2));
+        uint32_t bits[32];
+        dequant_kblock(grp, g.quant, r, kbg, d, bits);
+        __syncwarp();   // every lane is done with this stage's codes and scales
+        if (lane == 0 && ((s & 1u) == 1 || s + 1 == g.bstages)) mbar_arrive(&dempty[ds]);
+        tmem_st32_async(col + BK * h, bits);
+      } else if (h < nsub(s)) {
+        // low-rank K-block h of the stage: ranks 32 c + [0, 32) of the B
+        // factors (all terms, concatenated in order), row m0 + r; zero past the
+        // ranks or the rows
         const uint32_t row = m0 + r;
-        uint32_t rho = (kb - g.kblocks) * BK + 16 * h, k = 0, rb = 0;
+        uint32_t rho = ((s - g.bstages) * kSub + h) * BK, k = 0, rb = 0;
         while (k + 1 < g.nl && rho >= rb + g.lora[k].r) rb += g.lora[k++].r;
+        uint32_t bits[32];
 #pragma unroll
-        for (int e = 0; e < 16; ++e, ++rho) {
+        for (int e = 0; e < 32; ++e, ++rho) {
           while (k + 1 < g.nl && rho >= rb + g.lora[k].r) rb += g.lora[k++].r;
-          w[e] = (row < g.m && rho < g.rtot) ? g.lora[k].B[static_cast<size_t>(row) * g.lora[k].r + (rho - rb)] : 0.f;
+          bits[e] = __float_as_uint((row < g.m && rho < g.rtot)
+                                        ? g.lora[k].B[static_cast<size_t>(row) * g.lora[k].r + (rho - rb)]
+                                        : 0.f);
         }
+        tmem_st32_async(col + BK * h, bits);
       }
-      __syncwarp();               // every lane is done with this group's codes and scales
-      if (lane == 0 && base && (kb % kDGroup == kDGroup - 1 || kb + 1 == g.kblocks)) mbar_arrive(&dempty[ds]);
-      // Software pipeline: K-block kb - 1 was stored to TMEM one iteration
-      // ago; wait for that store only now (its latency overlapped this
-      // conversion) and release it to the MMA issuer, then store kb.
-      if (pending) {
-        tmem_wait_st();
-        tc_fence_before();        // the MMA issuer reads these columns after the barrier
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&conv[pend_st]);
-      }
-      uint32_t bits[16];
-#pragma unroll
-      for (int e = 0; e < 16; ++e) bits[e] = __float_as_uint(w[e]);
-      tmem_st16_async(taddr + ((quarter * 32u) << 16) + kAcol + BK * st + 16 * h, bits);
-      pending = true;
-      pend_st = st;
-    }
-    if (pending) {
+      // hand the stage to this K-block's issuer as soon as the store landed
+      // (with two stages, deferring it would serialize conversion and MMAs)
       tmem_wait_st();
-      tc_fence_before();
+      tc_fence_before();   // the issuer reads these columns after the barrier
       __syncwarp();
-      if (lane == 0) mbar_arrive(&conv[pend_st]);
+      if (lane == 0) mbar_arrive(&myconv[st]);
     }
   }
   __syncwarp();
 
-  // ---- epilogue (warps 2..5): TMEM lane quarter (warp mod 4) = 32 rows, column = token
+  // ---- epilogue (the first four converter warps, one per TMEM lane quarter:
+  // 32 rows; column = token): the issuers' accumulators summed in a fixed order
   griddep_wait();   // Y may still be read by a preceding kernel
-  if (warp >= 2 && warp < 6) {
+  if (warp >= kConv0 && warp < kConv0 + 4) {
     const bool ok = mbar_wait_bounded(accum, 0);
     if (!ok) latch_status(g.status, kTimeoutFused);
     tc_fence_after();
     const uint32_t quarter = warp & 3u;
     const uint32_t row = m0 + quarter * 32 + lane;
     for (uint32_t c0 = 0; c0 < g.bn; c0 += 32) {
-      uint32_t acc[32];
-      tmem_ld32(taddr + ((quarter * 32u) << 16) + c0, acc);
+      float sum[32];
+      {
+        uint32_t acc[32];
+        tmem_ld32(taddr + ((quarter * 32u) << 16) + c0, acc);
+#pragma unroll
+        for (uint32_t j = 0; j < 32; ++j) sum[j] = __uint_as_float(acc[j]);
+      }
+#pragma unroll
+      for (uint32_t w = 1; w < kIssuers; ++w) {
+        uint32_t acc[32];
+        tmem_ld32(taddr + ((quarter * 32u) << 16) + w * g.bn + c0, acc);
+#pragma unroll
+        for (uint32_t j = 0; j < 32; ++j) sum[j] += __uint_as_float(acc[j]);
+      }
       if (!ok || row >= g.m) continue;
 #pragma unroll
       for (uint32_t j = 0; j < 32; ++j) {
         const uint32_t t = n0 + c0 + j;
-        if (c0 + j < g.bn && t < g.T) g.y[static_cast<size_t>(t) * g.m + row] = __uint_as_float(acc[j]);
+        if (c0 + j < g.bn && t < g.T) g.y[static_cast<size_t>(t) * g.m + row] = sum[j];
       }
     }
   }
@@ -382,7 +458,9 @@ cudaError_t launch_fused_gemm(const FusedLaunch& L, cudaStream_t st) {
   const uint32_t qrow = L.quant == OVL_Q8_0 ? 32u : 16u;
   const uint32_t rowbytes = L.n / BK * qrow;
   CUtensorMap tmQ, tmD;
-  if (!encode_map_2d(&tmQ, CU_TENSOR_MAP_DATA_TYPE_UINT8, L.qs, rowbytes, L.m, rowbytes, kDGroup * qrow, BM, false) ||
+  // codes: 128-byte boxes (8 q4 K-blocks or 4 q8 ones) in the 128-byte swizzle,
+  // so the 32 rows a converter warp reads fall in different banks
+  if (!encode_map_2d(&tmQ, CU_TENSOR_MAP_DATA_TYPE_UINT8, L.qs, rowbytes, L.m, rowbytes, 128, BM, true) ||
       !encode_map_2d(&tmD, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, L.dpl, L.n / BK, L.m, L.n / BK * 2, kDGroup, BM, false))
     return cudaErrorInvalidValue;
   const size_t esz = L.xdt == OVL_BF16 ? 2 : 4;
@@ -414,13 +492,17 @@ cudaError_t launch_fused_gemm(const FusedLaunch& L, cudaStream_t st) {
     g.quant = L.quant;
     g.bn = (tc + 15) / 16 * 16;
     g.kblocks = L.n / BK;
+    g.bstages = g.kblocks / kSub;
     g.qrow = qrow;
-    g.b_off = 0;
-    g.gbytes = kDBytes + BM * kDGroup * qrow;
-    g.stage_bytes = (g.bn * 128 + 1023) / 1024 * 1024;
+    g.gbytes = BM * kDGroup * qrow + kDBytes;   // multiple of 1024: every group stays swizzle-aligned
+    g.xbytes = g.bn * 128;                      // multiple of 2048
+    g.stage_bytes = kSub * g.xbytes;
     g.lkb = L.nl ? rpad / BK : 0;
-    g.ns = std::min<uint32_t>(kMaxStages, (kSmemCap - 1024 - 2 * g.gbytes - 512) / g.stage_bytes);
-    if (g.ns < 2) return cudaErrorInvalidConfiguration;
+    g.acol = kIssuers * g.bn;
+    g.ns = std::min<uint32_t>(kMaxStages, (kTmemCols - g.acol) / kStageCols);
+    const uint32_t left = kSmemCap - 1024 - 512 - g.ns * g.stage_bytes;
+    g.ng = std::min<uint32_t>(kMaxGroups, left / g.gbytes);
+    if (g.ng < 2) return cudaErrorInvalidConfiguration;
     g.tmem_cols = kTmemCols;
     g.idesc = (1u << 4)                  // accumulator: f32
               | (2u << 7) | (2u << 10)   // A, B: tf32
@@ -434,14 +516,19 @@ cudaError_t launch_fused_gemm(const FusedLaunch& L, cudaStream_t st) {
     int8_t tok_term[kTokTile];
     for (uint32_t t = 0; t < kTokTile; ++t) tok_term[t] = (L.tok_sel && t < tc) ? L.tok_host[t0 + t] : -1;
     CUtensorMap tmX, tmV;
-    // K-block-major activations: row j * tc + t holds x[t][32 j .. 32 j + 32)
-    if (!encode_map_2d(&tmX, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, xf, BK, static_cast<uint64_t>(g.kblocks) * tc, BK * 4,
-                       BK, g.bn, true))
-      return cudaErrorInvalidValue;
+    // K-block-major activations as {element e, token t, K-block j}:
+    // x[t][32 j + e] at ((j tc + t) 32 + e); one box = kSub tiles of bn tokens
+    const uint32_t box[3] = {BK, g.bn, kSub};
+    {
+      const uint64_t dims[3] = {BK, tc, g.kblocks};
+      const uint64_t str[2] = {BK * 4, static_cast<uint64_t>(tc) * BK * 4};
+      if (!encode_map_3d(&tmX, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, xf, dims, str, box, true)) return cudaErrorInvalidValue;
+    }
     if (L.nl) {
-      if (!encode_map_2d(&tmV, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, v, rpad, tc, static_cast<uint64_t>(rpad) * 4, BK, g.bn,
-                         true))
-        return cudaErrorInvalidValue;
+      // s v as {rank within a chunk of 32, token, chunk}: v[t][32 c + e]
+      const uint64_t dims[3] = {BK, tc, rpad / BK};
+      const uint64_t str[2] = {static_cast<uint64_t>(rpad) * 4, BK * 4};
+      if (!encode_map_3d(&tmV, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, v, dims, str, box, true)) return cudaErrorInvalidValue;
     } else {
       tmV = tmX;   // no low-rank K-blocks: never read
     }
@@ -473,7 +560,9 @@ cudaError_t launch_fused_gemm(const FusedLaunch& L, cudaStream_t st) {
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = dim3((L.m + BM - 1) / BM, 1);
     cfg.blockDim = dim3(kThreads);
-    cfg.dynamicSmemBytes = g.ns * g.stage_bytes + 2 * g.gbytes + 512 + 1024;
+    // at least 120 KiB, so that two CTAs never share an SM (each holds all of
+    // its SM's tensor memory)
+    cfg.dynamicSmemBytes = std::max<uint32_t>(g.ns * g.stage_bytes + g.ng * g.gbytes + 512 + 1024, 120 * 1024);
     cfg.stream = st;
     cfg.attrs = at;
     cfg.numAttrs = 1;

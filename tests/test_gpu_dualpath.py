@@ -251,6 +251,7 @@ TC_CASES = [  # (quant, d_out, d_in, T, ranks, xdtype): token chunks of 64, ragg
     (S.Q8_0, 300, 2048, 512, (8,), "bf16"),
     (S.Q4_0, 777, 1024, 100, (5, 3), "f32"),
     (S.Q8_0, 129, 256, 16, (), "f32"),
+    (S.Q4_0, 256, 512, 33, (64, 100), "bf16"),   # low-rank K-blocks over two pipeline stages
 ]
 
 
