@@ -198,17 +198,17 @@ __global__ void __launch_bounds__(kThreads, 1)
   // instead of all asking the same few L2 lines for the same tile.  d_in is a
   // multiple of 256 here: stages and groups stay aligned.  The order is fixed
   // per CTA: results are deterministic.
+  // Slots and phase parities advance as counters (no divisions in the loops).
   const uint32_t rot = (blockIdx.x % (g.kblocks / kDGroup)) * kDGroup;
-  auto kdata = [&](uint32_t kb) { return (kb + rot) % g.kblocks; };
   if (warp == 0 && lane == 0) {
     // ---- activation producer
     prefetch_tensormap(&tmX);
     prefetch_tensormap(&tmV);
     griddep_wait();   // the widened activations and s v come from preceding kernels
+    uint32_t st = 0, ph = 0, kd = rot;   // slot, its use parity, the stage's first K-block of data
     for (uint32_t s = 0; s < stot; ++s) {
-      const uint32_t st = s % g.ns;
       const bool base = s < g.bstages;
-      if (s >= g.ns && !mbar_wait_spin(&empty[st], ((s / g.ns) - 1) & 1)) {
+      if (s >= g.ns && !mbar_wait_spin(&empty[st], ph ^ 1u)) {
         latch_status(g.status, kTimeoutFused);
         break;
       }
@@ -217,9 +217,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint8_t* stg = tiles + st * g.stage_bytes;
       mbar_arrive_expect_tx(&full[st], g.stage_bytes);
       if (base)
-        tma_load_3d(stg, &tmX, 0, static_cast<int32_t>(n0), static_cast<int32_t>(kdata(s * kSub)), &full[st]);
+        tma_load_3d(stg, &tmX, 0, static_cast<int32_t>(n0), static_cast<int32_t>(kd), &full[st]);
       else
         tma_load_3d(stg, &tmV, 0, static_cast<int32_t>(n0), static_cast<int32_t>((s - g.bstages) * kSub), &full[st]);
+      kd += kSub;
+      if (kd >= g.kblocks) kd -= g.kblocks;
+      if (++st == g.ns) {
+        st = 0;
+        ph ^= 1u;
+      }
     }
   } else if (warp == kGroupWarp && lane == 0) {
     // ---- code-group producer: raw codes and scales of two stages per group,
@@ -227,27 +233,33 @@ __global__ void __launch_bounds__(kThreads, 1)
     // immutable, so this starts before the preceding kernels have finished.
     prefetch_tensormap(&tmQ);
     prefetch_tensormap(&tmD);
+    uint32_t ds = 0, gph = 0, kd = rot;
     for (uint32_t dg = 0; dg < g.bstages / 2; ++dg) {
-      const uint32_t ds = dg % g.ng;
-      if (dg >= g.ng && !mbar_wait_bounded(&dempty[ds], ((dg / g.ng) - 1) & 1)) {
+      if (dg >= g.ng && !mbar_wait_bounded(&dempty[ds], gph ^ 1u)) {
         latch_status(g.status, kTimeoutFused);
         break;
       }
       uint8_t* grp = gring + ds * g.gbytes;
       mbar_arrive_expect_tx(&dfull[ds], g.gbytes);
-      const uint32_t kb0 = kdata(dg * kDGroup);   // the group's data: a multiple of 8 K-blocks
+      // the group's data starts at K-block kd, a multiple of 8
       for (uint32_t b = 0; b < g.qrow / 16; ++b)   // 128-byte boxes: q4 one, q8 two
-        tma_load_2d(grp + b * (BM * 128u), &tmQ, static_cast<int32_t>(kb0 * g.qrow + b * 128u),
+        tma_load_2d(grp + b * (BM * 128u), &tmQ, static_cast<int32_t>(kd * g.qrow + b * 128u),
                     static_cast<int32_t>(m0), &dfull[ds]);
-      tma_load_2d(grp + BM * kDGroup * g.qrow, &tmD, static_cast<int32_t>(kb0), static_cast<int32_t>(m0), &dfull[ds]);
+      tma_load_2d(grp + BM * kDGroup * g.qrow, &tmD, static_cast<int32_t>(kd), static_cast<int32_t>(m0), &dfull[ds]);
+      kd += kDGroup;
+      if (kd >= g.kblocks) kd -= g.kblocks;
+      if (++ds == g.ng) {
+        ds = 0;
+        gph ^= 1u;
+      }
     }
   } else if (warp >= 1 && warp <= kIssuers && lane == 0) {
     // ---- MMA issuers: issuer w takes K-blocks [w kKbPerIssuer, (w + 1) kKbPerIssuer)
     // of every stage into its own accumulator (columns [w bn, (w + 1) bn))
     const uint32_t w = warp - 1, j0 = w * kKbPerIssuer;
     const uint32_t dacc = taddr + w * g.bn;
+    uint32_t st = 0, ph = 0;
     for (uint32_t s = 0; s < stot; ++s) {
-      const uint32_t st = s % g.ns, ph = (s / g.ns) & 1;
       if (!mbar_wait_spin(&conv[w * kMaxStages + st], ph) || !mbar_wait_spin(&full[st], ph)) {
         latch_status(g.status, kTimeoutFused);
         break;
@@ -270,6 +282,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             umma_tf32_ts(dacc, acol + BK * j + 8 * kk, b0 + j * bstep + 2u * kk, g.idesc, 1u);
       }
       umma_commit(&empty[st]);
+      if (++st == g.ns) {
+        st = 0;
+        ph ^= 1u;
+      }
     }
     umma_commit(accum);
   } else if (warp >= kConv0 && warp < kConv0 + kConvWarps) {
@@ -278,17 +294,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t quarter = warp & 3u, h = (warp - kConv0) >> 2, r = quarter * 32 + lane;
     uint64_t* myconv = conv + (h / kKbPerIssuer) * kMaxStages;
     const uint32_t lanes = taddr + ((quarter * 32u) << 16);
+    uint32_t st = 0, ph = 0, ds = 0, gph = 0;   // stage slot and parity; group slot and parity
     for (uint32_t s = 0; s < stot; ++s) {
-      const uint32_t st = s % g.ns;
       const bool base = s < g.bstages;
-      const uint32_t dg = s >> 1, ds = dg % g.ng;
-      if (base && (s & 1u) == 0 && !mbar_wait_spin(&dfull[ds], (dg / g.ng) & 1)) {
+      if (base && (s & 1u) == 0 && !mbar_wait_spin(&dfull[ds], gph)) {
         latch_status(g.status, kTimeoutFused);
         break;
       }
       // the weight operand of stage st is free once the MMAs of stage s - ns
       // completed (the converters never read the activation tiles)
-      if (s >= g.ns && !mbar_wait_spin(&empty[st], ((s / g.ns) - 1) & 1)) {
+      if (s >= g.ns && !mbar_wait_spin(&empty[st], ph ^ 1u)) {
         latch_status(g.status, kTimeoutFused);
         break;
       }
@@ -326,6 +341,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_before();   // the issuer reads these columns after the barrier
       __syncwarp();
       if (lane == 0) mbar_arrive(&myconv[st]);
+      if (base && (s & 1u) == 1 && ++ds == g.ng) {   // the group's second stage is done
+        ds = 0;
+        gph ^= 1u;
+      }
+      if (++st == g.ns) {
+        st = 0;
+        ph ^= 1u;
+      }
     }
   }
   __syncwarp();
