@@ -33,7 +33,7 @@
 //    every stage into its own accumulator; tcgen05.commit frees each stage;
 //  * epilogue (four converter warps, one TMEM lane quarter each): the
 //    accumulators summed in a fixed order, stored to Y.  The low-rank term runs
-//    as extra K-blocks (A = the B factors' rows, B = s v from k_shrink).
+//    as extra K-blocks (A = the B factors' rows, B = s v from k_widen_shrink).
 // TF32 keeps 10 explicit mantissa bits of d (q - bias) (|error| <= 2^-10 |w|);
 // the activations (bf16, or fp32 rounded by the tensor core) likewise; fp32
 // accumulation.  Every wait is bounded and latches a status code.
@@ -393,63 +393,154 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
+// Four activations x[idx .. idx + 4) as fp32 (idx a multiple of 4).
+__device__ __forceinline__ float4 load_x4(const void* x, uint32_t xdt, size_t idx) {
+  if (xdt == OVL_BF16) {
+    const uint2 raw = *reinterpret_cast<const uint2*>(static_cast<const uint16_t*>(x) + idx);
+    return make_float4(__uint_as_float(raw.x << 16), __uint_as_float(raw.x & 0xFFFF0000u), __uint_as_float(raw.y << 16),
+                       __uint_as_float(raw.y & 0xFFFF0000u));
+  }
+  return *reinterpret_cast<const float4*>(static_cast<const float*>(x) + idx);
+}
+
 // Activations of one token chunk -> fp32 in K-block-major order:
 // out[(j * T + t) * 32 + e] = x[t][32 j + e].  One K-block of every token is
 // then one contiguous run (its tile is spread over many L2 slices, instead of T
-// lines a row apart that every CTA asks for at once).
+// lines a row apart that every CTA asks for at once).  Four elements a thread.
 __global__ void __launch_bounds__(256) k_widen_kblk(const void* __restrict__ x, uint32_t xdt, uint32_t T, uint32_t n,
                                                    float* __restrict__ out) {
   griddep_launch_dependents();
   griddep_wait();
-  const size_t count = static_cast<size_t>(T) * n;
-  for (size_t i = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < count;
-       i += static_cast<size_t>(gridDim.x) * blockDim.x) {
-    const uint32_t e = static_cast<uint32_t>(i & 31), rest = static_cast<uint32_t>(i >> 5);
+  const uint32_t count4 = T * n / 4;
+  for (uint32_t i = blockIdx.x * blockDim.x + threadIdx.x; i < count4; i += gridDim.x * blockDim.x) {
+    const uint32_t e4 = i & 7u, rest = i >> 3;
     const uint32_t t = rest % T, j = rest / T;
-    const size_t src = static_cast<size_t>(t) * n + j * 32u + e;
-    out[i] = xdt == OVL_BF16 ? __uint_as_float(static_cast<uint32_t>(static_cast<const uint16_t*>(x)[src]) << 16)
-                             : static_cast<const float*>(x)[src];
+    *reinterpret_cast<float4*>(out + static_cast<size_t>(i) * 4) = load_x4(x, xdt, static_cast<size_t>(t) * n + j * 32u + e4 * 4);
   }
 }
 
-// v[t][rho] = s_k A_k[rho - rb_k] . x[t] for every token and factor row (one
-// warp per pair, 16-byte loads, fixed-order sums), rows padded to a multiple of
-// 32 with zeros; pairs a segmented token does not use are zero as well.  The
-// fused kernel multiplies these by the B rows on the tensor cores.
+// The low-rank side product and the widening in one pass:
+//   v[t][rho] = s_k A_k[rho - rb_k] . x[t]   (rows padded to a multiple of 32
+// with zeros; pairs a segmented token does not use are zero as well), and the
+// K-block-major fp32 copy of x that the fused kernel's tiles come from.
+// One block per 2 factor rows x 8 tokens; warp w takes the 128-element chunks
+// c = w mod W of the row, each lane 4 elements of a chunk with all 16 sums in
+// registers; the sums are folded across lanes (butterfly) and then across
+// warps in a fixed order: deterministic.  Each (chunk, token) of the widened
+// copy is written by exactly one block.
 struct ShrinkArgs {
-  const float* x;         // widened activations [T][n]
+  const void* x;          // the chunk's activations [T][n] (xdt)
+  float* xw;              // widened activations, K-block-major
   float* v;               // [T][rpad]
-  uint32_t n, T, nl, rtot, rpad, tok_sel;
+  uint32_t xdt, n, T, nl, rtot, rpad, tok_sel;
   LoraRef lora[OVL_MAX_TABLE];
   int8_t tok_term[kTokTile];
 };
 
-__global__ void __launch_bounds__(256) k_shrink(const ShrinkArgs s) {
+constexpr uint32_t kShrinkRows = 2;     // factor rows per block
+constexpr uint32_t kShrinkToks = 8;     // tokens per block
+constexpr uint32_t kShrinkSums = kShrinkRows * kShrinkToks;
+// W warps split K: 32 make one load round for d_in = 4096 when the grid is
+// small; 8 when there are many blocks (many factor rows), most of them empty.
+template <uint32_t kShrinkWarps>
+__global__ void __launch_bounds__(kShrinkWarps * 32) k_widen_shrink(const ShrinkArgs a) {
   griddep_launch_dependents();
-  griddep_wait();   // the widened activations
-  const uint32_t lane = threadIdx.x & 31;
-  const uint32_t pairs = s.T * s.rpad;
-  for (uint32_t p = (blockIdx.x * blockDim.x + threadIdx.x) >> 5; p < pairs; p += (gridDim.x * blockDim.x) >> 5) {
-    const uint32_t t = p / s.rpad, rho = p - t * s.rpad;
+  griddep_wait();   // x may come from a preceding kernel; xw and v may still be read by one
+  __shared__ float part[kShrinkWarps][kShrinkSums];
+  __shared__ float ssc[kShrinkRows];
+  const uint32_t warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rho0 = blockIdx.x * kShrinkRows, t0 = blockIdx.y * kShrinkToks;
+  // this block's factor rows and the (token, row) pairs it computes
+  const float* arow[kShrinkRows];
+  float sc[kShrinkRows];
+  uint32_t mask = 0;   // bit tt * kShrinkRows + i
+  {
     uint32_t k = 0, rb = 0;
-    while (k + 1 < s.nl && rho >= rb + s.lora[k].r) rb += s.lora[k++].r;
-    float acc = 0.f;
-    if (rho < s.rtot && (!s.tok_sel || s.tok_term[t] == static_cast<int>(k))) {
-      const float4* a = reinterpret_cast<const float4*>(s.lora[k].A + static_cast<size_t>(rho - rb) * s.n);
-      for (uint32_t j = lane; j < s.n / 4; j += 32) {
-        // element 4 j of token t in the K-block-major layout
-        const float4 xv = *reinterpret_cast<const float4*>(s.x + (static_cast<size_t>(j >> 3) * s.T + t) * 32 + (j & 7) * 4);
-        const float4 av = a[j];
-        acc = fmaf(av.x, xv.x, acc);
-        acc = fmaf(av.y, xv.y, acc);
-        acc = fmaf(av.z, xv.z, acc);
-        acc = fmaf(av.w, xv.w, acc);
-      }
 #pragma unroll
-      for (int o = 16; o >= 1; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-      acc *= s.lora[k].s;
+    for (uint32_t i = 0; i < kShrinkRows; ++i) {
+      const uint32_t rho = rho0 + i;
+      while (k + 1 < a.nl && rho >= rb + a.lora[k].r) rb += a.lora[k++].r;
+      const bool live = rho < a.rtot;
+      arow[i] = live ? a.lora[k].A + static_cast<size_t>(rho - rb) * a.n : nullptr;
+      sc[i] = live ? a.lora[k].s : 0.f;
+#pragma unroll
+      for (uint32_t tt = 0; tt < kShrinkToks; ++tt) {
+        const uint32_t t = t0 + tt;
+        if (live && t < a.T && (!a.tok_sel || a.tok_term[t] == static_cast<int>(k))) mask |= 1u << (tt * kShrinkRows + i);
+      }
     }
-    if (lane == 0) s.v[p] = acc;
+  }
+  float acc[kShrinkSums];
+#pragma unroll
+  for (uint32_t i = 0; i < kShrinkSums; ++i) acc[i] = 0.f;
+  const uint32_t nchunks = a.n / 128;
+  for (uint32_t c = warp; c < nchunks; c += kShrinkWarps) {
+    const bool widen = (c / kShrinkWarps) % gridDim.x == blockIdx.x;   // this block's share of the widened copy
+    if (!mask && !widen) continue;
+    const uint32_t j = c * 128 + lane * 4;
+    float4 xv[kShrinkToks];
+#pragma unroll
+    for (uint32_t tt = 0; tt < kShrinkToks; ++tt) {
+      const uint32_t t = t0 + tt;
+      xv[tt] = t < a.T ? load_x4(a.x, a.xdt, static_cast<size_t>(t) * a.n + j) : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    if (widen) {
+#pragma unroll
+      for (uint32_t tt = 0; tt < kShrinkToks; ++tt) {
+        const uint32_t t = t0 + tt;
+        if (t < a.T) *reinterpret_cast<float4*>(a.xw + (static_cast<size_t>(j >> 5) * a.T + t) * 32 + (j & 31)) = xv[tt];
+      }
+    }
+    if (mask) {
+#pragma unroll
+      for (uint32_t i = 0; i < kShrinkRows; ++i) {
+        if (!arow[i]) continue;
+        const float4 av = *reinterpret_cast<const float4*>(arow[i] + j);
+#pragma unroll
+        for (uint32_t tt = 0; tt < kShrinkToks; ++tt) {
+          float s = acc[tt * kShrinkRows + i];
+          s = fmaf(av.x, xv[tt].x, s);
+          s = fmaf(av.y, xv[tt].y, s);
+          s = fmaf(av.z, xv[tt].z, s);
+          s = fmaf(av.w, xv[tt].w, s);
+          acc[tt * kShrinkRows + i] = s;
+        }
+      }
+    }
+  }
+  if (!mask) {   // nothing to sum: zeros (the block still wrote its share of xw)
+    if (threadIdx.x < kShrinkSums) {
+      const uint32_t t = t0 + threadIdx.x / kShrinkRows, rho = rho0 + threadIdx.x % kShrinkRows;
+      if (t < a.T) a.v[static_cast<size_t>(t) * a.rpad + rho] = 0.f;
+    }
+    return;
+  }
+  // fold the 16 sums across the warp: each round halves what a lane keeps;
+  // lane l ends with sum l / 2 (its neighbour holds the same)
+#pragma unroll
+  for (uint32_t r = 0; r < 4; ++r) {
+    const uint32_t off = 16u >> r, cnt = kShrinkSums >> (r + 1);
+    const bool up = (lane & off) != 0;
+#pragma unroll
+    for (uint32_t i = 0; i < cnt; ++i) {
+      const float send = up ? acc[i] : acc[i + cnt];
+      const float keep = up ? acc[i + cnt] : acc[i];
+      acc[i] = keep + __shfl_xor_sync(0xffffffffu, send, off);
+    }
+  }
+  acc[0] += __shfl_xor_sync(0xffffffffu, acc[0], 1);
+  if ((lane & 1) == 0) part[warp][lane >> 1] = acc[0];
+  if (threadIdx.x == 0) {
+#pragma unroll
+    for (uint32_t i = 0; i < kShrinkRows; ++i) ssc[i] = sc[i];
+  }
+  __syncthreads();
+  if (threadIdx.x < kShrinkSums) {
+    float s = part[0][threadIdx.x];
+#pragma unroll
+    for (uint32_t w = 1; w < kShrinkWarps; ++w) s += part[w][threadIdx.x];
+    const uint32_t tt = threadIdx.x / kShrinkRows, i = threadIdx.x % kShrinkRows, t = t0 + tt;
+    if (t < a.T) a.v[static_cast<size_t>(t) * a.rpad + rho0 + i] = ((mask >> threadIdx.x) & 1) ? s * ssc[i] : 0.f;
   }
 }
 
@@ -494,20 +585,43 @@ cudaError_t launch_fused_gemm(const FusedLaunch& L, cudaStream_t st) {
     const uint32_t tc = std::min<uint32_t>(kTokTile, L.T - t0);
     const void* xc = static_cast<const uint8_t*>(L.x) + static_cast<size_t>(t0) * L.n * esz;
     cudaError_t e;
-    {
+    cudaLaunchAttribute at[1];
+    at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    at[0].val.programmaticStreamSerializationAllowed = 1;
+    if (L.nl) {
+      // widened activations and s v in one pass
+      ShrinkArgs s{};
+      s.x = xc;
+      s.xw = xf;
+      s.v = v;
+      s.xdt = L.xdt;
+      s.n = L.n;
+      s.T = tc;
+      s.nl = L.nl;
+      s.rtot = L.rtot;
+      s.rpad = rpad;
+      s.tok_sel = L.tok_sel;
+      for (uint32_t k = 0; k < L.nl; ++k) s.lora[k] = L.lora[k];
+      for (uint32_t t = 0; t < kTokTile; ++t) s.tok_term[t] = (L.tok_sel && t < tc) ? L.tok_host[t0 + t] : -1;
+      cudaLaunchConfig_t cs{};
+      cs.gridDim = dim3(rpad / kShrinkRows, (tc + kShrinkToks - 1) / kShrinkToks);
+      const bool wide = cs.gridDim.x * cs.gridDim.y <= 2 * 152;
+      cs.blockDim = dim3(wide ? 1024 : 256);
+      cs.stream = st;
+      cs.attrs = at;
+      cs.numAttrs = 1;
+      e = wide ? cudaLaunchKernelEx(&cs, k_widen_shrink<32>, s) : cudaLaunchKernelEx(&cs, k_widen_shrink<8>, s);
+    } else {
       cudaLaunchConfig_t cw{};
-      const size_t count = static_cast<size_t>(tc) * L.n;
-      cw.gridDim = dim3(static_cast<unsigned>(std::max<size_t>(1, std::min<size_t>((count + 255) / 256, 1184))));
+      const uint32_t count4 = tc * L.n / 4;
+      cw.gridDim = dim3(std::max<uint32_t>(1, std::min<uint32_t>((count4 + 255) / 256, 1184)));
       cw.blockDim = dim3(256);
       cw.stream = st;
-      cudaLaunchAttribute aw[1];
-      aw[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-      aw[0].val.programmaticStreamSerializationAllowed = 1;
-      cw.attrs = aw;
+      cw.attrs = at;
       cw.numAttrs = 1;
       e = cudaLaunchKernelEx(&cw, k_widen_kblk, xc, L.xdt, tc, L.n, xf);
-      if (e != cudaSuccess) return e;
     }
+    if (e != cudaSuccess) return e;
     FusedArgs g{};
     g.m = L.m;
     g.n = L.n;
@@ -536,8 +650,6 @@ cudaError_t launch_fused_gemm(const FusedLaunch& L, cudaStream_t st) {
     g.y = L.y + static_cast<size_t>(t0) * L.m;
     g.status = L.status;
     for (uint32_t k = 0; k < L.nl; ++k) g.lora[k] = L.lora[k];
-    int8_t tok_term[kTokTile];
-    for (uint32_t t = 0; t < kTokTile; ++t) tok_term[t] = (L.tok_sel && t < tc) ? L.tok_host[t0 + t] : -1;
     CUtensorMap tmX, tmV;
     // K-block-major activations as {element e, token t, K-block j}:
     // x[t][32 j + e] at ((j tc + t) 32 + e); one box = kSub tiles of bn tokens
@@ -554,31 +666,6 @@ cudaError_t launch_fused_gemm(const FusedLaunch& L, cudaStream_t st) {
       if (!encode_map_3d(&tmV, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, v, dims, str, box, true)) return cudaErrorInvalidValue;
     } else {
       tmV = tmX;   // no low-rank K-blocks: never read
-    }
-    cudaLaunchAttribute at[1];
-    at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    at[0].val.programmaticStreamSerializationAllowed = 1;
-    if (L.nl) {
-      ShrinkArgs s{};
-      s.x = xf;
-      s.v = v;
-      s.n = L.n;
-      s.T = tc;
-      s.nl = L.nl;
-      s.rtot = L.rtot;
-      s.rpad = rpad;
-      s.tok_sel = L.tok_sel;
-      for (uint32_t k = 0; k < L.nl; ++k) s.lora[k] = L.lora[k];
-      for (uint32_t t = 0; t < kTokTile; ++t) s.tok_term[t] = tok_term[t];
-      cudaLaunchConfig_t cs{};
-      const uint32_t warps = tc * rpad;
-      cs.gridDim = dim3(std::max<uint32_t>(1, std::min<uint32_t>((warps + 7) / 8, 1184)));
-      cs.blockDim = dim3(256);
-      cs.stream = st;
-      cs.attrs = at;
-      cs.numAttrs = 1;
-      e = cudaLaunchKernelEx(&cs, k_shrink, s);
-      if (e != cudaSuccess) return e;
     }
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = dim3((L.m + BM - 1) / BM, 1);

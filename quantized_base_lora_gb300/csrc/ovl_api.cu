@@ -614,8 +614,10 @@ uint32_t stack_terms(ovl_ctx* c, const Composition& comp, uint32_t tensor, LoraR
 // allows: there the integer dot products would be bound by issue slots.
 constexpr uint32_t kTcMinT = 16;
 
-bool use_tc(const ovl_ctx* c, uint32_t T, const ovl_tensor_desc& td, uint32_t rtot) {
-  return T >= kTcMinT && c->ws.tc_scratch_bytes > 0 && fused_gemm_supported(td.d_out, td.d_in) &&
+// The tensor-core kernel reads the activations 16 bytes at a time.
+bool use_tc(const ovl_ctx* c, uint32_t T, const ovl_tensor_desc& td, uint32_t rtot, const void* x) {
+  return T >= kTcMinT && (reinterpret_cast<uintptr_t>(x) & 15) == 0 && c->ws.tc_scratch_bytes > 0 &&
+         fused_gemm_supported(td.d_out, td.d_in) &&
          fused_gemm_scratch_bytes(T, td.d_in, rtot) <= c->ws.tc_scratch_bytes;
 }
 
@@ -704,7 +706,7 @@ ovl_status ovl_linear_forward(ovl_ctx* ctx, uint32_t tensor, const void* x, uint
   uint32_t rtot;
   std::vector<Adapter*> used;
   const uint32_t nl = stack_terms(ctx, *ctx->active, tensor, terms, &rtot, &used);
-  if (path == OVL_PATH_DUAL && use_tc(ctx, T, td, rtot)) {
+  if (path == OVL_PATH_DUAL && use_tc(ctx, T, td, rtot, x)) {
     cudaError_t e = launch_tc(ctx, td, x, x_dtype, T, y, terms, nl, rtot, nullptr, st);
     if (e != cudaSuccess) return cuda_fail(ctx, e, "tensor-core launch");
   } else if (path == OVL_PATH_DUAL) {
@@ -776,7 +778,7 @@ ovl_status ovl_linear_forward_multi(ovl_ctx* ctx, uint32_t n, const uint32_t* te
       uint32_t rt;
       std::vector<Adapter*> tmp;
       stack_terms(ctx, *ctx->active, tensors[i], terms, &rt, &tmp);
-      tc_all = use_tc(ctx, T, ctx->tensors[tensors[i]], rt);
+      tc_all = use_tc(ctx, T, ctx->tensors[tensors[i]], rt, x);
     }
     if (tc_all) {
       cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -894,7 +896,7 @@ ovl_status ovl_segmented_forward(ovl_ctx* ctx, uint32_t tensor, const void* x, u
   a.tok_sel = 1;
   a.tok_host = tok.data();
   a.ws = ctx->ws;
-  cudaError_t e = use_tc(ctx, T, td, a.rtot)
+  cudaError_t e = use_tc(ctx, T, td, a.rtot, x)
                       ? launch_tc(ctx, td, x, x_dtype, T, y, a.lora, a.nl, a.rtot, tok.data(), st)
                       : launch_dualpath(a, st);
   if (e != cudaSuccess) return cuda_fail(ctx, e, "segmented launch");
