@@ -503,13 +503,54 @@ def workload_segmented(args):
           "unit": "us", "value": ms * 1e3, "higher_is_better": False, "steps": args.steps,
           "tok_s": T / (ms / 1e3), "effective_gbs": (planes + lora) / (ms / 1e3) / 1e9,
           "distinct_adapters": int(len(set(int(v) for v in ids))), "segments": len(sl),
-          "roofline": hbm_roofline(alg, ms, "k_dualpath (8-token tiles, one launch per tile and tensor)"),
-          "base_tflops": flops / (ms / 1e3) / 1e12,
+          "roofline": {"bound": "tensor", "achieved": flops / (ms / 1e3) / 1e12, "peak": tf32_peak()[0],
+                       "unit": "TFLOP/s", "frac": flops / (ms / 1e3) / 1e12 / tf32_peak()[0], "traffic": None,
+                       "kernel": "k_widen_shrink + k_fused_gemm per tensor (64 tokens, all TABLE slots)",
+                       "note": f"peak = {tf32_peak()[1]}"},
+          "hbm": hbm_roofline(alg, ms, "k_widen_shrink + k_fused_gemm"),
           "config": {"base": "q4_0 q 4096x4096 + gate 14336x4096 (42.5 MB)", "adapters": "16 x r16, s=2.0, TABLE",
                      "requests": "64, Zipf(1.1) seed 3000", "x": "bf16", "l2": f"{N_COPIES} base copies rotated"}})
 
 
 WORKLOADS["segmented"] = workload_segmented
+
+
+def workload_prefill_dual(args):
+    """The dual path at T = 64 and 256 tokens (tensor-core route, K4): the
+    8B-shape q8_0 block with a rank-16 adapter on all seven projections, the
+    same four launches per step as decode."""
+    import torch
+    base = S.block_base(S.Q8_0)
+    ads = [S.block_adapter(base, adapter=0, rank=16)]
+    rts = _contexts(base, ads, [2.0], N_COPIES, 96)
+    stream = torch.cuda.Stream()
+    sh = int(stream.cuda_stream)
+    planes = sum(S.qs_bytes(base.quant, t.d_out, t.d_in) + S.d_bytes(t.d_out, t.d_in) for t in base.tensors)
+    lora = sum(16 * (t.d_in + t.d_out) * 4 for t in base.tensors)
+    tpeak, tkind = tf32_peak()
+    per_T = {}
+    for T in (64, 256):
+        xs = {d: torch.from_numpy(S.to_bf16_bits(S.activations(T, d)).view(np.int16)).cuda().view(torch.bfloat16)
+              for d in (4096, 14336)}
+        ybufs = [torch.empty((T, t.d_out), dtype=torch.float32, device="cuda") for t in base.tensors]
+        step = _block_step(base, rts, {d: v.data_ptr() for d, v in xs.items()}, [y.data_ptr() for y in ybufs], T, sh)
+        ms = timed_steps(step, args.steps, args.warmup, stream)
+        _check_all(rts, sh)
+        flops = sum(2 * T * t.d_out * t.d_in for t in base.tensors) + sum(2 * T * 16 * (t.d_in + t.d_out)
+                                                                          for t in base.tensors)
+        tfs = flops / (ms / 1e3) / 1e12
+        per_T[T] = {"ms_per_step": ms, "tok_s": T / (ms / 1e3), "effective_gbs": (planes + lora) / (ms / 1e3) / 1e9,
+                    "roofline": {"bound": "tensor", "achieved": tfs, "peak": tpeak, "unit": "TFLOP/s",
+                                 "frac": tfs / tpeak, "traffic": None,
+                                 "kernel": "k_widen_shrink + k_fused_gemm per tensor and 64-token chunk",
+                                 "note": f"peak = {tkind}"}}
+    emit({"workload": "prefill-dual", "metric": "dual-path multi-token step (8B shape, q8_0 + r16, tensor cores)",
+          "unit": "tok/s", "value": per_T[64]["tok_s"], "per_T": per_T, "steps": args.steps,
+          "config": {"base": "8B-shape block q8_0 (231.7 MB)", "adapter": "r16 s=2.0 on all 7", "x": "bf16",
+                     "T": [64, 256], "l2": f"{N_COPIES} base copies rotated"}})
+
+
+WORKLOADS["prefill-dual"] = workload_prefill_dual
 
 
 def tf32_peak():

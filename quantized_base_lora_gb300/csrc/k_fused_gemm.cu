@@ -80,7 +80,10 @@ struct FusedArgs {
   uint32_t acol;          // first TMEM column of the weight operands: kIssuers bn
   uint32_t ng;            // code-group buffers
   uint32_t kblocks;       // n / 32
-  uint32_t bstages;       // base stages: kblocks / kSub
+  uint32_t splits;        // CTAs (one cluster) sharing a row tile, each with kbs K-blocks
+  uint32_t kbs;           // base K-blocks per CTA: kblocks / splits, a multiple of kDGroup
+  uint32_t bstages;       // base stages per CTA: kbs / kSub
+  uint32_t recv_bytes;    // split-K receive buffer: BM x bn fp32 (0 without splits)
   uint32_t lkb;           // K-blocks of the low-rank term (ranks in chunks of 32)
   uint32_t qrow;          // raw code bytes per row and K-block (32 or 16)
   uint32_t gbytes;        // one code group: codes (128-byte swizzled boxes) then scales
@@ -152,16 +155,22 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* sm = sm_raw + ((1024u - (smem_u32(sm_raw) & 1023u)) & 1023u);
   uint8_t* tiles = sm;                                   // ns x kSub activation tiles
   uint8_t* gring = sm + g.ns * g.stage_bytes;            // ng code groups (codes, then scales)
-  uint64_t* full = reinterpret_cast<uint64_t*>(gring + g.ng * g.gbytes);
+  float* recv = reinterpret_cast<float*>(gring + g.ng * g.gbytes);   // split-K partials of the rows this CTA owns
+  uint64_t* full = reinterpret_cast<uint64_t*>(gring + g.ng * g.gbytes + g.recv_bytes);
   uint64_t* empty = full + kMaxStages;
   uint64_t* conv = empty + kMaxStages;     // [issuer][stage]
   uint64_t* dfull = conv + kIssuers * kMaxStages;
   uint64_t* dempty = dfull + kMaxGroups;
   uint64_t* accum = dempty + kMaxGroups;
-  uint32_t* s_taddr = reinterpret_cast<uint32_t*>(accum + 1);
+  uint64_t* red = accum + 1;               // split-K: the owners' partials have arrived
+  uint32_t* s_taddr = reinterpret_cast<uint32_t*>(red + 1);
 
   const uint32_t warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const uint32_t m0 = blockIdx.x * BM, n0 = blockIdx.y * g.bn;
+  // split-K: the CTAs of a cluster share the row tile, CTA `split` (its rank in
+  // the cluster) taking base K-blocks [split kbs, (split + 1) kbs)
+  const uint32_t split = g.splits > 1 ? cluster_ctarank() : 0u;
+  const uint32_t tile = blockIdx.x / g.splits;
+  const uint32_t m0 = tile * BM, n0 = blockIdx.y * g.bn, k0 = split * g.kbs;
 
   if (warp == 0) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(s_taddr)),
@@ -181,17 +190,22 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&dempty[i], kConvWarps);
     }
     mbar_init(accum, kIssuers);
+    mbar_init(red, 4);   // one arrival per epilogue warp (in the cluster) whose rows this CTA owns
     mbar_fence_init();
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
+  // every CTA's barriers are initialized before any CTA of the cluster can
+  // arrive on them remotely
+  if (g.splits > 1) cluster_sync_all();
   const uint32_t taddr = *s_taddr;
   griddep_launch_dependents();
 
-  // Stages: kSub K-blocks each; the base ones, then the low-rank ones (the last
-  // may hold fewer K-blocks).
-  const uint32_t stot = g.bstages + (g.lkb + kSub - 1) / kSub;
+  // Stages: kSub K-blocks each; the base ones, then (in the cluster's last CTA)
+  // the low-rank ones (the last may hold fewer K-blocks).
+  const bool lowrank = split + 1 == g.splits;
+  const uint32_t stot = g.bstages + (lowrank ? (g.lkb + kSub - 1) / kSub : 0u);
   auto nsub = [&](uint32_t s) { return s < g.bstages ? kSub : min(kSub, g.lkb - (s - g.bstages) * kSub); };
   // Each CTA walks the base K-blocks from its own group onwards (wrapping), so
   // the CTAs of a launch read different activation tiles at any moment
@@ -199,7 +213,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // multiple of 256 here: stages and groups stay aligned.  The order is fixed
   // per CTA: results are deterministic.
   // Slots and phase parities advance as counters (no divisions in the loops).
-  const uint32_t rot = (blockIdx.x % (g.kblocks / kDGroup)) * kDGroup;
+  const uint32_t rot = (tile % (g.kbs / kDGroup)) * kDGroup;
   if (warp == 0 && lane == 0) {
     // ---- activation producer
     prefetch_tensormap(&tmX);
@@ -217,11 +231,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint8_t* stg = tiles + st * g.stage_bytes;
       mbar_arrive_expect_tx(&full[st], g.stage_bytes);
       if (base)
-        tma_load_3d(stg, &tmX, 0, static_cast<int32_t>(n0), static_cast<int32_t>(kd), &full[st]);
+        tma_load_3d(stg, &tmX, 0, static_cast<int32_t>(n0), static_cast<int32_t>(k0 + kd), &full[st]);
       else
         tma_load_3d(stg, &tmV, 0, static_cast<int32_t>(n0), static_cast<int32_t>((s - g.bstages) * kSub), &full[st]);
       kd += kSub;
-      if (kd >= g.kblocks) kd -= g.kblocks;
+      if (kd >= g.kbs) kd -= g.kbs;
       if (++st == g.ns) {
         st = 0;
         ph ^= 1u;
@@ -241,13 +255,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       uint8_t* grp = gring + ds * g.gbytes;
       mbar_arrive_expect_tx(&dfull[ds], g.gbytes);
-      // the group's data starts at K-block kd, a multiple of 8
+      // the group's data starts at K-block k0 + kd, a multiple of 8
       for (uint32_t b = 0; b < g.qrow / 16; ++b)   // 128-byte boxes: q4 one, q8 two
-        tma_load_2d(grp + b * (BM * 128u), &tmQ, static_cast<int32_t>(kd * g.qrow + b * 128u),
+        tma_load_2d(grp + b * (BM * 128u), &tmQ, static_cast<int32_t>((k0 + kd) * g.qrow + b * 128u),
                     static_cast<int32_t>(m0), &dfull[ds]);
-      tma_load_2d(grp + BM * kDGroup * g.qrow, &tmD, static_cast<int32_t>(kd), static_cast<int32_t>(m0), &dfull[ds]);
+      tma_load_2d(grp + BM * kDGroup * g.qrow, &tmD, static_cast<int32_t>(k0 + kd), static_cast<int32_t>(m0),
+                  &dfull[ds]);
       kd += kDGroup;
-      if (kd >= g.kblocks) kd -= g.kblocks;
+      if (kd >= g.kbs) kd -= g.kbs;
       if (++ds == g.ng) {
         ds = 0;
         gph ^= 1u;
@@ -354,14 +369,23 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncwarp();
 
   // ---- epilogue (the first four converter warps, one per TMEM lane quarter:
-  // 32 rows; column = token): the issuers' accumulators summed in a fixed order
+  // 32 rows; column = token): the issuers' accumulators summed in a fixed order.
+  // Without split-K they go to Y.  With it, row rl of the tile belongs to the
+  // cluster's CTA rl / (BM / splits): every CTA sends its partial rows there
+  // (distributed shared memory, slot = its own rank) and arrives on that CTA's
+  // `red` barrier; the owner adds the splits' partials in rank order.
   griddep_wait();   // Y may still be read by a preceding kernel
   if (warp >= kConv0 && warp < kConv0 + 4) {
     const bool ok = mbar_wait_bounded(accum, 0);
     if (!ok) latch_status(g.status, kTimeoutFused);
     tc_fence_after();
     const uint32_t quarter = warp & 3u;
-    const uint32_t row = m0 + quarter * 32 + lane;
+    const uint32_t rl = quarter * 32 + lane, row = m0 + rl;
+    const uint32_t per = BM / g.splits;   // rows each CTA of the cluster owns
+    const uint32_t own = rl / per;
+    const uint32_t rs = g.bn + 4;   // recv row stride (floats): 16-byte rows, reads spread over the banks
+    const uint32_t slot = (split * per + (rl - own * per)) * rs;   // in the owner's recv
+    const uint32_t raddr = g.splits > 1 ? cluster_map(recv + slot, own) : 0u;
     for (uint32_t c0 = 0; c0 < g.bn; c0 += 32) {
       float sum[32];
       {
@@ -377,11 +401,46 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (uint32_t j = 0; j < 32; ++j) sum[j] += __uint_as_float(acc[j]);
       }
+      if (g.splits > 1) {
+#pragma unroll
+        for (uint32_t j = 0; j < 32; j += 4)
+          if (c0 + j < g.bn) st_cluster_v4(raddr + (c0 + j) * 4, sum[j], sum[j + 1], sum[j + 2], sum[j + 3]);
+        continue;
+      }
       if (!ok || row >= g.m) continue;
 #pragma unroll
       for (uint32_t j = 0; j < 32; ++j) {
         const uint32_t t = n0 + c0 + j;
         if (c0 + j < g.bn && t < g.T) g.y[static_cast<size_t>(t) * g.m + row] = sum[j];
+      }
+    }
+    if (g.splits > 1) {
+      fence_acq_rel_cluster();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_remote(cluster_map(red, own));
+      if (own == split) {
+        // this warp's rows are this CTA's: wait for all splits, add in rank order
+        const bool got = mbar_wait_cluster(red, 0);
+        if (!got) latch_status(g.status, kTimeoutFused);
+        if (got && ok && row < g.m) {
+          const float* mine = recv + (rl - own * per) * rs;
+          for (uint32_t c = 0; c < g.bn; c += 4) {
+            float4 v = *reinterpret_cast<const float4*>(mine + c);
+            for (uint32_t sp = 1; sp < g.splits; ++sp) {
+              const float4 u = *reinterpret_cast<const float4*>(mine + sp * per * rs + c);
+              v.x += u.x;
+              v.y += u.y;
+              v.z += u.z;
+              v.w += u.w;
+            }
+            const float vv[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (uint32_t q = 0; q < 4; ++q) {
+              const uint32_t t = n0 + c + q;
+              if (t < g.T) g.y[static_cast<size_t>(t) * g.m + row] = vv[q];
+            }
+          }
+        }
       }
     }
   }
@@ -546,6 +605,16 @@ __global__ void __launch_bounds__(kShrinkWarps * 32) k_widen_shrink(const Shrink
 
 }  // namespace
 
+// SMs of the current device (cached per device).
+uint32_t sm_count() {
+  static int cached[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 152;
+  if (!cached[dev] && cudaDeviceGetAttribute(&cached[dev], cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+    return 152;
+  return static_cast<uint32_t>(cached[dev]);
+}
+
 bool fused_gemm_supported(uint32_t m, uint32_t n) { return m > 0 && n >= 256 && n % 256 == 0; }
 
 size_t fused_gemm_scratch_bytes(uint32_t T, uint32_t n, uint32_t rtot) {
@@ -629,7 +698,16 @@ cudaError_t launch_fused_gemm(const FusedLaunch& L, cudaStream_t st) {
     g.quant = L.quant;
     g.bn = (tc + 15) / 16 * 16;
     g.kblocks = L.n / BK;
-    g.bstages = g.kblocks / kSub;
+    // split-K over a cluster when the row tiles alone would leave SMs idle:
+    // each CTA then walks kblocks / splits K-blocks (a whole number of code groups)
+    const uint32_t tiles = (L.m + BM - 1) / BM;
+    g.splits = 1;
+    if (tiles * 4 <= sm_count() && L.n % (BK * kDGroup * 4) == 0)
+      g.splits = 4;
+    else if (tiles * 2 <= sm_count() && L.n % (BK * kDGroup * 2) == 0)
+      g.splits = 2;
+    g.kbs = g.kblocks / g.splits;
+    g.bstages = g.kbs / kSub;
     g.qrow = qrow;
     g.gbytes = BM * kDGroup * qrow + kDBytes;   // multiple of 1024: every group stays swizzle-aligned
     g.xbytes = g.bn * 128;                      // multiple of 2048
@@ -637,7 +715,8 @@ cudaError_t launch_fused_gemm(const FusedLaunch& L, cudaStream_t st) {
     g.lkb = L.nl ? rpad / BK : 0;
     g.acol = kIssuers * g.bn;
     g.ns = std::min<uint32_t>(kMaxStages, (kTmemCols - g.acol) / kStageCols);
-    const uint32_t left = kSmemCap - 1024 - 512 - g.ns * g.stage_bytes;
+    g.recv_bytes = g.splits > 1 ? BM * (g.bn + 4) * 4 : 0u;
+    const uint32_t left = kSmemCap - 1024 - 512 - g.ns * g.stage_bytes - g.recv_bytes;
     g.ng = std::min<uint32_t>(kMaxGroups, left / g.gbytes);
     if (g.ng < 2) return cudaErrorInvalidConfiguration;
     g.tmem_cols = kTmemCols;
@@ -668,14 +747,21 @@ cudaError_t launch_fused_gemm(const FusedLaunch& L, cudaStream_t st) {
       tmV = tmX;   // no low-rank K-blocks: never read
     }
     cudaLaunchConfig_t cfg{};
-    cfg.gridDim = dim3((L.m + BM - 1) / BM, 1);
+    cfg.gridDim = dim3(tiles * g.splits, 1);
     cfg.blockDim = dim3(kThreads);
     // at least 120 KiB, so that two CTAs never share an SM (each holds all of
     // its SM's tensor memory)
-    cfg.dynamicSmemBytes = std::max<uint32_t>(g.ns * g.stage_bytes + g.ng * g.gbytes + 512 + 1024, 120 * 1024);
+    cfg.dynamicSmemBytes =
+        std::max<uint32_t>(g.ns * g.stage_bytes + g.ng * g.gbytes + g.recv_bytes + 512 + 1024, 120 * 1024);
     cfg.stream = st;
-    cfg.attrs = at;
-    cfg.numAttrs = 1;
+    cudaLaunchAttribute ak[2];
+    ak[0] = at[0];
+    ak[1].id = cudaLaunchAttributeClusterDimension;
+    ak[1].val.clusterDim.x = g.splits;
+    ak[1].val.clusterDim.y = 1;
+    ak[1].val.clusterDim.z = 1;
+    cfg.attrs = ak;
+    cfg.numAttrs = g.splits > 1 ? 2 : 1;
     e = cudaLaunchKernelEx(&cfg, k_fused_gemm, tmQ, tmD, tmX, tmV, g);
     if (e != cudaSuccess) return e;
   }

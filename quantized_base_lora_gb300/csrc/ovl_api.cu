@@ -772,7 +772,7 @@ ovl_status ovl_linear_forward_multi(ovl_ctx* ctx, uint32_t n, const uint32_t* te
   DeviceGuard g(ctx->device);
   {
     // multi-token: one tensor-core launch per tensor when every tensor allows it
-    bool tc_all = true;
+    bool tc_all = T >= kTcMinT;   // decode never takes the tensor-core route: skip the term lookups
     for (uint32_t i = 0; i < n && tc_all; ++i) {
       LoraRef terms[OVL_MAX_STACK];
       uint32_t rt;
