@@ -23,6 +23,9 @@ CASES = [
     # quant, d_out, d_in, T, ranks, scales, x dtype
     (S.Q8_0, 1024, 4096, 1, (16,), (2.0,), "bf16"),
     (S.Q4_0, 1000, 288, 3, (5, 7), (1.0, 0.5), "f32"),
+    # 8 tokens at an aligned d_in: linear_forward takes the tensor-core route
+    # here, this entry point the decode kernel's 8-token tiles
+    (S.Q8_0, 512, 2048, 8, (16, 4), (1.0, 0.5), "bf16"),
 ]
 
 
