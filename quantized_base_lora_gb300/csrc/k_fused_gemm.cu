@@ -41,6 +41,7 @@
 #include <cuda_fp16.h>
 
 #include <algorithm>
+#include <cstring>
 #include <mutex>
 
 #include "ovl_internal.h"
@@ -73,8 +74,27 @@ constexpr uint32_t kTimeoutFused = 5;
 static_assert(kSub % kIssuers == 0, "stage split");
 static_assert(kIssuers * kTokTile + 2 * kStageCols <= kTmemCols, "TMEM budget: two stages at the widest token tile");
 
+constexpr uint32_t kMaxFusedTensors = 4;   // tensors sharing x in one launch (q+k+v, gate+up)
+
+// One tensor of a launch: its row tiles are [tile0, tile0 + ceil(m / BM)) of
+// the launch's tiles; its terms lora[term0 .. term0 + nl); its s v columns are
+// chunks [vchunk0, vchunk0 + lkb) of 32 of the launch's v.
+struct FusedTensorArgs {
+  uint32_t m, tile0, lkb, rtot, nl, term0, vchunk0;
+  float* y;                 // [T][m]
+};
+
+// Tensor maps of a launch (kernel parameter, so the TMA unit reads them from
+// the parameter space): codes and scales per tensor, activations, s v.
+struct FusedMaps {
+  CUtensorMap q[kMaxFusedTensors];
+  CUtensorMap d[kMaxFusedTensors];
+  CUtensorMap x, v;
+};
+
 struct FusedArgs {
-  uint32_t m, n, T, quant;
+  uint32_t nt;              // tensors in this launch
+  uint32_t n, T, quant;
   uint32_t bn;            // UMMA N (multiple of 16, <= kTokTile)
   uint32_t ns;            // pipeline stages (activation tiles + TMEM weight operands)
   uint32_t acol;          // first TMEM column of the weight operands: kIssuers bn
@@ -84,16 +104,14 @@ struct FusedArgs {
   uint32_t kbs;           // base K-blocks per CTA: kblocks / splits, a multiple of kDGroup
   uint32_t bstages;       // base stages per CTA: kbs / kSub
   uint32_t recv_bytes;    // split-K receive buffer: BM x bn fp32 (0 without splits)
-  uint32_t lkb;           // K-blocks of the low-rank term (ranks in chunks of 32)
   uint32_t qrow;          // raw code bytes per row and K-block (32 or 16)
   uint32_t gbytes;        // one code group: codes (128-byte swizzled boxes) then scales
   uint32_t xbytes;        // one activation tile: bn rows x 128 bytes
   uint32_t stage_bytes;   // kSub activation tiles (one 3-D box)
   uint32_t tmem_cols;
   uint32_t idesc;
-  uint32_t nl, rtot;
-  float* y;
   uint32_t* status;
+  FusedTensorArgs ts[kMaxFusedTensors];
   LoraRef lora[OVL_MAX_TABLE];
 };
 
@@ -148,9 +166,7 @@ __device__ __forceinline__ void dequant_kblock(const uint8_t* codes, uint32_t qu
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
-    k_fused_gemm(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmD,
-                 const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmV,
-                 const FusedArgs g) {
+    k_fused_gemm(const __grid_constant__ FusedMaps maps, const __grid_constant__ FusedArgs g) {
   extern __shared__ __align__(1024) uint8_t sm_raw[];
   uint8_t* sm = sm_raw + ((1024u - (smem_u32(sm_raw) & 1023u)) & 1023u);
   uint8_t* tiles = sm;                                   // ns x kSub activation tiles
@@ -170,7 +186,18 @@ __global__ void __launch_bounds__(kThreads, 1)
   // the cluster) taking base K-blocks [split kbs, (split + 1) kbs)
   const uint32_t split = g.splits > 1 ? cluster_ctarank() : 0u;
   const uint32_t tile = blockIdx.x / g.splits;
-  const uint32_t m0 = tile * BM, n0 = blockIdx.y * g.bn, k0 = split * g.kbs;
+  // this CTA's tensor (the launch's tiles are the tensors' tiles in order)
+  uint32_t ti = 0;
+  while (ti + 1 < g.nt && tile >= g.ts[ti + 1].tile0) ++ti;
+  const uint32_t tm = g.ts[ti].m, tlkb = g.ts[ti].lkb, trtot = g.ts[ti].rtot, tnl = g.ts[ti].nl;
+  const uint32_t tterm0 = g.ts[ti].term0, tvc0 = g.ts[ti].vchunk0;
+  float* const ty = g.ts[ti].y;
+  const LoraRef* const tlora = g.lora + tterm0;
+  const CUtensorMap* const tmQ = &maps.q[ti];
+  const CUtensorMap* const tmD = &maps.d[ti];
+  const CUtensorMap* const tmX = &maps.x;
+  const CUtensorMap* const tmV = &maps.v;
+  const uint32_t m0 = (tile - g.ts[ti].tile0) * BM, n0 = blockIdx.y * g.bn, k0 = split * g.kbs;
 
   if (warp == 0) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(s_taddr)),
@@ -205,8 +232,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   // Stages: kSub K-blocks each; the base ones, then (in the cluster's last CTA)
   // the low-rank ones (the last may hold fewer K-blocks).
   const bool lowrank = split + 1 == g.splits;
-  const uint32_t stot = g.bstages + (lowrank ? (g.lkb + kSub - 1) / kSub : 0u);
-  auto nsub = [&](uint32_t s) { return s < g.bstages ? kSub : min(kSub, g.lkb - (s - g.bstages) * kSub); };
+  const uint32_t stot = g.bstages + (lowrank ? (tlkb + kSub - 1) / kSub : 0u);
+  auto nsub = [&](uint32_t s) { return s < g.bstages ? kSub : min(kSub, tlkb - (s - g.bstages) * kSub); };
   // Each CTA walks the base K-blocks from its own group onwards (wrapping), so
   // the CTAs of a launch read different activation tiles at any moment
   // instead of all asking the same few L2 lines for the same tile.  d_in is a
@@ -216,8 +243,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t rot = (tile % (g.kbs / kDGroup)) * kDGroup;
   if (warp == 0 && lane == 0) {
     // ---- activation producer
-    prefetch_tensormap(&tmX);
-    prefetch_tensormap(&tmV);
+    prefetch_tensormap(tmX);
+    prefetch_tensormap(tmV);
     griddep_wait();   // the widened activations and s v come from preceding kernels
     uint32_t st = 0, ph = 0, kd = rot;   // slot, its use parity, the stage's first K-block of data
     for (uint32_t s = 0; s < stot; ++s) {
@@ -231,9 +258,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint8_t* stg = tiles + st * g.stage_bytes;
       mbar_arrive_expect_tx(&full[st], g.stage_bytes);
       if (base)
-        tma_load_3d(stg, &tmX, 0, static_cast<int32_t>(n0), static_cast<int32_t>(k0 + kd), &full[st]);
+        tma_load_3d(stg, tmX, 0, static_cast<int32_t>(n0), static_cast<int32_t>(k0 + kd), &full[st]);
       else
-        tma_load_3d(stg, &tmV, 0, static_cast<int32_t>(n0), static_cast<int32_t>((s - g.bstages) * kSub), &full[st]);
+        tma_load_3d(stg, tmV, 0, static_cast<int32_t>(n0), static_cast<int32_t>(tvc0 + (s - g.bstages) * kSub),
+                    &full[st]);
       kd += kSub;
       if (kd >= g.kbs) kd -= g.kbs;
       if (++st == g.ns) {
@@ -245,8 +273,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ---- code-group producer: raw codes and scales of two stages per group,
     // up to ng groups ahead of the converters.  The base weights are
     // immutable, so this starts before the preceding kernels have finished.
-    prefetch_tensormap(&tmQ);
-    prefetch_tensormap(&tmD);
+    prefetch_tensormap(tmQ);
+    prefetch_tensormap(tmD);
     uint32_t ds = 0, gph = 0, kd = rot;
     for (uint32_t dg = 0; dg < g.bstages / 2; ++dg) {
       if (dg >= g.ng && !mbar_wait_bounded(&dempty[ds], gph ^ 1u)) {
@@ -257,9 +285,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_arrive_expect_tx(&dfull[ds], g.gbytes);
       // the group's data starts at K-block k0 + kd, a multiple of 8
       for (uint32_t b = 0; b < g.qrow / 16; ++b)   // 128-byte boxes: q4 one, q8 two
-        tma_load_2d(grp + b * (BM * 128u), &tmQ, static_cast<int32_t>((k0 + kd) * g.qrow + b * 128u),
+        tma_load_2d(grp + b * (BM * 128u), tmQ, static_cast<int32_t>((k0 + kd) * g.qrow + b * 128u),
                     static_cast<int32_t>(m0), &dfull[ds]);
-      tma_load_2d(grp + BM * kDGroup * g.qrow, &tmD, static_cast<int32_t>(k0 + kd), static_cast<int32_t>(m0),
+      tma_load_2d(grp + BM * kDGroup * g.qrow, tmD, static_cast<int32_t>(k0 + kd), static_cast<int32_t>(m0),
                   &dfull[ds]);
       kd += kDGroup;
       if (kd >= g.kbs) kd -= g.kbs;
@@ -339,13 +367,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         // ranks or the rows
         const uint32_t row = m0 + r;
         uint32_t rho = ((s - g.bstages) * kSub + h) * BK, k = 0, rb = 0;
-        while (k + 1 < g.nl && rho >= rb + g.lora[k].r) rb += g.lora[k++].r;
+        while (k + 1 < tnl && rho >= rb + tlora[k].r) rb += tlora[k++].r;
         uint32_t bits[32];
 #pragma unroll
         for (int e = 0; e < 32; ++e, ++rho) {
-          while (k + 1 < g.nl && rho >= rb + g.lora[k].r) rb += g.lora[k++].r;
-          bits[e] = __float_as_uint((row < g.m && rho < g.rtot)
-                                        ? g.lora[k].B[static_cast<size_t>(row) * g.lora[k].r + (rho - rb)]
+          while (k + 1 < tnl && rho >= rb + tlora[k].r) rb += tlora[k++].r;
+          bits[e] = __float_as_uint((row < tm && rho < trtot)
+                                        ? tlora[k].B[static_cast<size_t>(row) * tlora[k].r + (rho - rb)]
                                         : 0.f);
         }
         tmem_st32_async(col + BK * h, bits);
@@ -407,11 +435,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (c0 + j < g.bn) st_cluster_v4(raddr + (c0 + j) * 4, sum[j], sum[j + 1], sum[j + 2], sum[j + 3]);
         continue;
       }
-      if (!ok || row >= g.m) continue;
+      if (!ok || row >= tm) continue;
 #pragma unroll
       for (uint32_t j = 0; j < 32; ++j) {
         const uint32_t t = n0 + c0 + j;
-        if (c0 + j < g.bn && t < g.T) g.y[static_cast<size_t>(t) * g.m + row] = sum[j];
+        if (c0 + j < g.bn && t < g.T) ty[static_cast<size_t>(t) * tm + row] = sum[j];
       }
     }
     if (g.splits > 1) {
@@ -422,7 +450,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // this warp's rows are this CTA's: wait for all splits, add in rank order
         const bool got = mbar_wait_cluster(red, 0);
         if (!got) latch_status(g.status, kTimeoutFused);
-        if (got && ok && row < g.m) {
+        if (got && ok && row < tm) {
           const float* mine = recv + (rl - own * per) * rs;
           for (uint32_t c = 0; c < g.bn; c += 4) {
             float4 v = *reinterpret_cast<const float4*>(mine + c);
@@ -437,7 +465,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (uint32_t q = 0; q < 4; ++q) {
               const uint32_t t = n0 + c + q;
-              if (t < g.T) g.y[static_cast<size_t>(t) * g.m + row] = vv[q];
+              if (t < g.T) ty[static_cast<size_t>(t) * tm + row] = vv[q];
             }
           }
         }
@@ -492,7 +520,9 @@ struct ShrinkArgs {
   float* xw;              // widened activations, K-block-major
   float* v;               // [T][rpad]
   uint32_t xdt, n, T, nl, rtot, rpad, tok_sel;
-  LoraRef lora[OVL_MAX_TABLE];
+  // the launch's terms in order, each tensor's followed by a padding term
+  // (A null) up to a multiple of 32 rows; padding rows of v are zero
+  LoraRef lora[OVL_MAX_TABLE + kMaxFusedTensors];
   int8_t tok_term[kTokTile];
 };
 
@@ -519,7 +549,7 @@ __global__ void __launch_bounds__(kShrinkWarps * 32) k_widen_shrink(const Shrink
     for (uint32_t i = 0; i < kShrinkRows; ++i) {
       const uint32_t rho = rho0 + i;
       while (k + 1 < a.nl && rho >= rb + a.lora[k].r) rb += a.lora[k++].r;
-      const bool live = rho < a.rtot;
+      const bool live = rho < a.rtot && a.lora[k].A != nullptr;
       arow[i] = live ? a.lora[k].A + static_cast<size_t>(rho - rb) * a.n : nullptr;
       sc[i] = live ? a.lora[k].s : 0.f;
 #pragma unroll
@@ -617,21 +647,33 @@ uint32_t sm_count() {
 
 bool fused_gemm_supported(uint32_t m, uint32_t n) { return m > 0 && n >= 256 && n % 256 == 0; }
 
-size_t fused_gemm_scratch_bytes(uint32_t T, uint32_t n, uint32_t rtot) {
+size_t fused_gemm_scratch_bytes(uint32_t T, uint32_t n, uint32_t vcols) {
   const uint32_t tc = std::min<uint32_t>(T, kTokTile);
-  const uint32_t rpad = (rtot + BK - 1) / BK * BK;
-  return (static_cast<size_t>(tc) * n * 4 + 255) / 256 * 256 + static_cast<size_t>(tc) * rpad * 4;
+  return (static_cast<size_t>(tc) * n * 4 + 255) / 256 * 256 + static_cast<size_t>(tc) * vcols * 4;
 }
 
 cudaError_t launch_fused_gemm(const FusedLaunch& L, cudaStream_t st) {
-  if (L.T == 0 || L.m == 0) return cudaSuccess;
-  if (!fused_gemm_supported(L.m, L.n) || L.nl > OVL_MAX_TABLE) return cudaErrorInvalidValue;
-  if ((reinterpret_cast<uintptr_t>(L.qs) & 15) || (reinterpret_cast<uintptr_t>(L.dpl) & 15) ||
-      (reinterpret_cast<uintptr_t>(L.scratch) & 255) || L.scratch_bytes < fused_gemm_scratch_bytes(L.T, L.n, L.rtot))
+  if (L.T == 0) return cudaSuccess;
+  if (L.nt == 0 || L.nt > kMaxFusedTensors || (L.tok_sel && L.nt != 1)) return cudaErrorInvalidValue;
+  // per tensor: its tiles, its terms in the launch's table, its s v columns
+  FusedTensorArgs ta[kMaxFusedTensors] = {};
+  uint32_t tiles = 0, terms = 0, vcols = 0;
+  for (uint32_t i = 0; i < L.nt; ++i) {
+    const FusedTensor& t = L.t[i];
+    if (!fused_gemm_supported(t.m, L.n) || t.nl > OVL_MAX_TABLE || (reinterpret_cast<uintptr_t>(t.qs) & 15) ||
+        (reinterpret_cast<uintptr_t>(t.dpl) & 15))
+      return cudaErrorInvalidValue;
+    for (uint32_t k = 0; k < t.nl; ++k)
+      if (reinterpret_cast<uintptr_t>(t.lora[k].A) & 15) return cudaErrorInvalidValue;
+    const uint32_t rp = t.nl ? fused_vcols(t.rtot) : 0u;
+    ta[i] = FusedTensorArgs{t.m, tiles, rp / BK, t.rtot, t.nl, terms, vcols / BK, nullptr};
+    tiles += (t.m + BM - 1) / BM;
+    terms += t.nl;
+    vcols += rp;
+  }
+  if (terms > OVL_MAX_TABLE || (reinterpret_cast<uintptr_t>(L.scratch) & 255) ||
+      L.scratch_bytes < fused_gemm_scratch_bytes(L.T, L.n, vcols))
     return cudaErrorInvalidValue;
-  for (uint32_t k = 0; k < L.nl; ++k)
-    if (reinterpret_cast<uintptr_t>(L.lora[k].A) & 15) return cudaErrorInvalidValue;
-  const uint32_t rpad = (L.rtot + BK - 1) / BK * BK;
   static std::once_flag attr_once;
   static cudaError_t attr_err = cudaSuccess;
   std::call_once(attr_once, [] {
@@ -640,12 +682,33 @@ cudaError_t launch_fused_gemm(const FusedLaunch& L, cudaStream_t st) {
   if (attr_err != cudaSuccess) return attr_err;
   const uint32_t qrow = L.quant == OVL_Q8_0 ? 32u : 16u;
   const uint32_t rowbytes = L.n / BK * qrow;
-  CUtensorMap tmQ, tmD;
-  // codes: 128-byte boxes (8 q4 K-blocks or 4 q8 ones) in the 128-byte swizzle,
-  // so the 32 rows a converter warp reads fall in different banks
-  if (!encode_map_2d(&tmQ, CU_TENSOR_MAP_DATA_TYPE_UINT8, L.qs, rowbytes, L.m, rowbytes, 128, BM, true) ||
-      !encode_map_2d(&tmD, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, L.dpl, L.n / BK, L.m, L.n / BK * 2, kDGroup, BM, false))
-    return cudaErrorInvalidValue;
+  FusedMaps maps;
+  std::memset(&maps, 0, sizeof(maps));
+  for (uint32_t i = 0; i < L.nt; ++i) {
+    // codes: 128-byte boxes (8 q4 K-blocks or 4 q8 ones) in the 128-byte
+    // swizzle, so the 32 rows a converter warp reads fall in different banks
+    if (!encode_map_2d(&maps.q[i], CU_TENSOR_MAP_DATA_TYPE_UINT8, L.t[i].qs, rowbytes, L.t[i].m, rowbytes, 128, BM,
+                       true) ||
+        !encode_map_2d(&maps.d[i], CU_TENSOR_MAP_DATA_TYPE_FLOAT16, L.t[i].dpl, L.n / BK, L.t[i].m, L.n / BK * 2,
+                       kDGroup, BM, false))
+      return cudaErrorInvalidValue;
+  }
+  // the shrink's table: every tensor's terms, then a padding term (no A) up to
+  // its multiple of 32 rows
+  ShrinkArgs s{};
+  for (uint32_t i = 0; i < L.nt; ++i) {
+    const FusedTensor& t = L.t[i];
+    if (!t.nl) continue;
+    for (uint32_t k = 0; k < t.nl; ++k) s.lora[s.nl++] = t.lora[k];
+    if (fused_vcols(t.rtot) > t.rtot) s.lora[s.nl++] = LoraRef{nullptr, nullptr, fused_vcols(t.rtot) - t.rtot, 0.f};
+  }
+  // split-K over a cluster when the row tiles alone would leave SMs idle:
+  // each CTA then walks kblocks / splits K-blocks (a whole number of code groups)
+  uint32_t splits = 1;
+  if (tiles * 4 <= sm_count() && L.n % (BK * kDGroup * 4) == 0)
+    splits = 4;
+  else if (tiles * 2 <= sm_count() && L.n % (BK * kDGroup * 2) == 0)
+    splits = 2;
   const size_t esz = L.xdt == OVL_BF16 ? 2 : 4;
   float* xf = L.scratch;
   float* v = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(L.scratch) +
@@ -657,24 +720,21 @@ cudaError_t launch_fused_gemm(const FusedLaunch& L, cudaStream_t st) {
     cudaLaunchAttribute at[1];
     at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     at[0].val.programmaticStreamSerializationAllowed = 1;
-    if (L.nl) {
-      // widened activations and s v in one pass
-      ShrinkArgs s{};
+    if (vcols) {
+      // widened activations and s v of every tensor in one pass
       s.x = xc;
       s.xw = xf;
       s.v = v;
       s.xdt = L.xdt;
       s.n = L.n;
       s.T = tc;
-      s.nl = L.nl;
-      s.rtot = L.rtot;
-      s.rpad = rpad;
+      s.rtot = vcols;
+      s.rpad = vcols;
       s.tok_sel = L.tok_sel;
-      for (uint32_t k = 0; k < L.nl; ++k) s.lora[k] = L.lora[k];
       for (uint32_t t = 0; t < kTokTile; ++t) s.tok_term[t] = (L.tok_sel && t < tc) ? L.tok_host[t0 + t] : -1;
       cudaLaunchConfig_t cs{};
-      cs.gridDim = dim3(rpad / kShrinkRows, (tc + kShrinkToks - 1) / kShrinkToks);
-      const bool wide = cs.gridDim.x * cs.gridDim.y <= 2 * 152;
+      cs.gridDim = dim3(vcols / kShrinkRows, (tc + kShrinkToks - 1) / kShrinkToks);
+      const bool wide = cs.gridDim.x * cs.gridDim.y <= 2 * sm_count();
       cs.blockDim = dim3(wide ? 1024 : 256);
       cs.stream = st;
       cs.attrs = at;
@@ -692,27 +752,19 @@ cudaError_t launch_fused_gemm(const FusedLaunch& L, cudaStream_t st) {
     }
     if (e != cudaSuccess) return e;
     FusedArgs g{};
-    g.m = L.m;
+    g.nt = L.nt;
     g.n = L.n;
     g.T = tc;
     g.quant = L.quant;
     g.bn = (tc + 15) / 16 * 16;
     g.kblocks = L.n / BK;
-    // split-K over a cluster when the row tiles alone would leave SMs idle:
-    // each CTA then walks kblocks / splits K-blocks (a whole number of code groups)
-    const uint32_t tiles = (L.m + BM - 1) / BM;
-    g.splits = 1;
-    if (tiles * 4 <= sm_count() && L.n % (BK * kDGroup * 4) == 0)
-      g.splits = 4;
-    else if (tiles * 2 <= sm_count() && L.n % (BK * kDGroup * 2) == 0)
-      g.splits = 2;
+    g.splits = splits;
     g.kbs = g.kblocks / g.splits;
     g.bstages = g.kbs / kSub;
     g.qrow = qrow;
     g.gbytes = BM * kDGroup * qrow + kDBytes;   // multiple of 1024: every group stays swizzle-aligned
     g.xbytes = g.bn * 128;                      // multiple of 2048
     g.stage_bytes = kSub * g.xbytes;
-    g.lkb = L.nl ? rpad / BK : 0;
     g.acol = kIssuers * g.bn;
     g.ns = std::min<uint32_t>(kMaxStages, (kTmemCols - g.acol) / kStageCols);
     g.recv_bytes = g.splits > 1 ? BM * (g.bn + 4) * 4 : 0u;
@@ -724,27 +776,29 @@ cudaError_t launch_fused_gemm(const FusedLaunch& L, cudaStream_t st) {
               | (2u << 7) | (2u << 10)   // A, B: tf32
               | ((g.bn >> 3) << 17)      // N
               | ((BM >> 4) << 24);       // M
-    g.nl = L.nl;
-    g.rtot = L.rtot;
-    g.y = L.y + static_cast<size_t>(t0) * L.m;
     g.status = L.status;
-    for (uint32_t k = 0; k < L.nl; ++k) g.lora[k] = L.lora[k];
-    CUtensorMap tmX, tmV;
+    for (uint32_t i = 0; i < L.nt; ++i) {
+      g.ts[i] = ta[i];
+      g.ts[i].y = L.t[i].y + static_cast<size_t>(t0) * L.t[i].m;
+      for (uint32_t k = 0; k < L.t[i].nl; ++k) g.lora[ta[i].term0 + k] = L.t[i].lora[k];
+    }
     // K-block-major activations as {element e, token t, K-block j}:
     // x[t][32 j + e] at ((j tc + t) 32 + e); one box = kSub tiles of bn tokens
     const uint32_t box[3] = {BK, g.bn, kSub};
     {
       const uint64_t dims[3] = {BK, tc, g.kblocks};
       const uint64_t str[2] = {BK * 4, static_cast<uint64_t>(tc) * BK * 4};
-      if (!encode_map_3d(&tmX, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, xf, dims, str, box, true)) return cudaErrorInvalidValue;
+      if (!encode_map_3d(&maps.x, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, xf, dims, str, box, true))
+        return cudaErrorInvalidValue;
     }
-    if (L.nl) {
+    if (vcols) {
       // s v as {rank within a chunk of 32, token, chunk}: v[t][32 c + e]
-      const uint64_t dims[3] = {BK, tc, rpad / BK};
-      const uint64_t str[2] = {static_cast<uint64_t>(rpad) * 4, BK * 4};
-      if (!encode_map_3d(&tmV, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, v, dims, str, box, true)) return cudaErrorInvalidValue;
+      const uint64_t dims[3] = {BK, tc, vcols / BK};
+      const uint64_t str[2] = {static_cast<uint64_t>(vcols) * 4, BK * 4};
+      if (!encode_map_3d(&maps.v, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, v, dims, str, box, true))
+        return cudaErrorInvalidValue;
     } else {
-      tmV = tmX;   // no low-rank K-blocks: never read
+      maps.v = maps.x;   // no low-rank K-blocks: never read
     }
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = dim3(tiles * g.splits, 1);
@@ -762,7 +816,7 @@ cudaError_t launch_fused_gemm(const FusedLaunch& L, cudaStream_t st) {
     ak[1].val.clusterDim.z = 1;
     cfg.attrs = ak;
     cfg.numAttrs = g.splits > 1 ? 2 : 1;
-    e = cudaLaunchKernelEx(&cfg, k_fused_gemm, tmQ, tmD, tmX, tmV, g);
+    e = cudaLaunchKernelEx(&cfg, k_fused_gemm, maps, g);
     if (e != cudaSuccess) return e;
   }
   return cudaSuccess;

@@ -619,29 +619,39 @@ constexpr uint32_t kTcMinT = 4;
 bool use_tc(const ovl_ctx* c, uint32_t T, const ovl_tensor_desc& td, uint32_t rtot, const void* x) {
   return T >= kTcMinT && (reinterpret_cast<uintptr_t>(x) & 15) == 0 && c->ws.tc_scratch_bytes > 0 &&
          fused_gemm_supported(td.d_out, td.d_in) &&
-         fused_gemm_scratch_bytes(T, td.d_in, rtot) <= c->ws.tc_scratch_bytes;
+         fused_gemm_scratch_bytes(T, td.d_in, fused_vcols(rtot)) <= c->ws.tc_scratch_bytes;
+}
+
+void tc_tensor(const ovl_ctx* c, const ovl_tensor_desc& td, float* y, const LoraRef* terms, uint32_t nl,
+               uint32_t rtot, FusedTensor* out) {
+  out->qs = c->base + td.qs_off;
+  out->dpl = c->base + td.d_off;
+  out->m = td.d_out;
+  out->y = y;
+  out->nl = nl;
+  out->rtot = rtot;
+  for (uint32_t k = 0; k < nl; ++k) out->lora[k] = terms[k];
+}
+
+void tc_common(const ovl_ctx* c, uint32_t n, const void* x, uint32_t xdt, uint32_t T, FusedLaunch* L) {
+  L->quant = c->quant;
+  L->n = n;
+  L->x = x;
+  L->xdt = xdt;
+  L->T = T;
+  L->scratch = c->ws.tc_scratch;
+  L->scratch_bytes = c->ws.tc_scratch_bytes;
+  L->status = c->ws.status;
 }
 
 cudaError_t launch_tc(const ovl_ctx* c, const ovl_tensor_desc& td, const void* x, uint32_t xdt, uint32_t T, float* y,
                       const LoraRef* terms, uint32_t nl, uint32_t rtot, const int8_t* tok, cudaStream_t st) {
   FusedLaunch L{};
-  L.qs = c->base + td.qs_off;
-  L.dpl = c->base + td.d_off;
-  L.quant = c->quant;
-  L.m = td.d_out;
-  L.n = td.d_in;
-  L.x = x;
-  L.xdt = xdt;
-  L.T = T;
-  L.y = y;
-  L.nl = nl;
-  L.rtot = rtot;
-  for (uint32_t k = 0; k < nl; ++k) L.lora[k] = terms[k];
+  L.nt = 1;
+  tc_tensor(c, td, y, terms, nl, rtot, &L.t[0]);
+  tc_common(c, td.d_in, x, xdt, T, &L);
   L.tok_sel = tok != nullptr;
   L.tok_host = tok;
-  L.scratch = c->ws.tc_scratch;
-  L.scratch_bytes = c->ws.tc_scratch_bytes;
-  L.status = c->ws.status;
   return launch_fused_gemm(L, st);
 }
 
@@ -772,25 +782,33 @@ ovl_status ovl_linear_forward_multi(ovl_ctx* ctx, uint32_t n, const uint32_t* te
   if (!x) return fail(ctx, OVL_E_ARG, "null activation");
   DeviceGuard g(ctx->device);
   {
-    // multi-token: one tensor-core launch per tensor when every tensor allows it
+    // multi-token: one tensor-core launch over all the tensors when every
+    // tensor allows it and their s v vectors fit the scratch together
     bool tc_all = T >= kTcMinT;   // single-token decode never takes the tensor-core route: skip the term lookups
+    uint32_t vcols = 0;
     for (uint32_t i = 0; i < n && tc_all; ++i) {
       LoraRef terms[OVL_MAX_STACK];
       uint32_t rt;
       std::vector<Adapter*> tmp;
-      stack_terms(ctx, *ctx->active, tensors[i], terms, &rt, &tmp);
+      const uint32_t nl = stack_terms(ctx, *ctx->active, tensors[i], terms, &rt, &tmp);
       tc_all = use_tc(ctx, T, ctx->tensors[tensors[i]], rt, x);
+      if (nl) vcols += fused_vcols(rt);
     }
+    if (tc_all) tc_all = fused_gemm_scratch_bytes(T, ctx->tensors[tensors[0]].d_in, vcols) <= ctx->ws.tc_scratch_bytes;
     if (tc_all) {
       cudaStream_t st = static_cast<cudaStream_t>(stream);
       std::vector<Adapter*> used;
+      FusedLaunch L{};
+      L.nt = n;
       for (uint32_t i = 0; i < n; ++i) {
         LoraRef terms[OVL_MAX_STACK];
         uint32_t rt;
         const uint32_t nl = stack_terms(ctx, *ctx->active, tensors[i], terms, &rt, &used);
-        cudaError_t e = launch_tc(ctx, ctx->tensors[tensors[i]], x, x_dtype, T, ys[i], terms, nl, rt, nullptr, st);
-        if (e != cudaSuccess) return cuda_fail(ctx, e, "tensor-core launch");
+        tc_tensor(ctx, ctx->tensors[tensors[i]], ys[i], terms, nl, rt, &L.t[i]);
       }
+      tc_common(ctx, ctx->tensors[tensors[0]].d_in, x, x_dtype, T, &L);
+      cudaError_t e = launch_fused_gemm(L, st);
+      if (e != cudaSuccess) return cuda_fail(ctx, e, "tensor-core launch");
       if (ovl_status s = record_use(ctx, used, st)) return s;
       return ok(ctx);
     }

@@ -90,18 +90,24 @@ struct DualArgs {
   const int8_t* tok_host;  // host array of T entries (launcher only)
 };
 
-// Dual path on the tensor cores (K4) for multi-token launches of one tensor:
-// token chunks of kTokTile, each widen -> shrink -> fused dequantizing GEMM.
-struct FusedLaunch {
+// Dual path on the tensor cores (K4) for multi-token launches of one to four
+// tensors that share x (same d_in): token chunks of kTokTile, each one widen +
+// shrink launch and one fused dequantizing GEMM launch over all the tensors.
+struct FusedTensor {
   const uint8_t* qs;
   const uint8_t* dpl;
-  uint32_t quant, m, n;
-  const void* x;            // [T][n], fp32 or bf16
-  uint32_t xdt, T;
+  uint32_t m;
   float* y;                 // [T][m]
   uint32_t nl, rtot;
   LoraRef lora[OVL_MAX_TABLE];
-  uint32_t tok_sel;         // segmented: token t adds only term tok_host[t] (-1: none)
+};
+struct FusedLaunch {
+  uint32_t nt;              // tensors, 1..4; their terms together at most OVL_MAX_TABLE
+  FusedTensor t[4];
+  uint32_t quant, n;
+  const void* x;            // [T][n], fp32 or bf16, 16-byte aligned
+  uint32_t xdt, T;
+  uint32_t tok_sel;         // segmented (one tensor): token t adds only term tok_host[t] (-1: none)
   const int8_t* tok_host;   // host, T entries
   float* scratch;           // widened activations + low-rank vectors
   size_t scratch_bytes;
@@ -109,7 +115,9 @@ struct FusedLaunch {
 };
 // d_in a multiple of 256 (the f16 scale rows feed 16-byte tensor-map boxes).
 bool fused_gemm_supported(uint32_t m, uint32_t n);
-size_t fused_gemm_scratch_bytes(uint32_t T, uint32_t n, uint32_t rtot);
+// vcols: the tensors' total ranks, each rounded up to a multiple of 32.
+size_t fused_gemm_scratch_bytes(uint32_t T, uint32_t n, uint32_t vcols);
+inline uint32_t fused_vcols(uint32_t rtot) { return (rtot + 31) / 32 * 32; }
 cudaError_t launch_fused_gemm(const FusedLaunch& L, cudaStream_t st);
 
 // Materialize S = deq(W) + sum_k s_k B_k A_k into fp32 scratch [m][n].

@@ -217,7 +217,7 @@ def test_activation_scale_extremes_stay_within_bound():
 
 
 # ----------------------------------------------------------------- multi-tensor launches
-@pytest.mark.parametrize("T", [1, 3])
+@pytest.mark.parametrize("T", [1, 3, 4, 37])   # 4 and 37: one tensor-core launch over the group
 def test_multi_tensor_launch_qkv_and_gate_up(block_q8, T):
     import quantized_base_lora_gb300 as q
     base, ad, rt = block_q8
