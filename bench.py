@@ -52,6 +52,14 @@ SCALE = 2.0
 N_COPIES = 3
 
 
+# DRAM bytes (read + write) per k_dualpath launch of the decode step, mean over
+# its four launches (q+k+v, o, gate+up, down: 28.03 + 18.46 + 127.29 + 63.85 MB
+# per step), measured by ncu with --metrics dram__bytes_read.sum,
+# dram__bytes_write.sum on this workload.  Set to None whenever k_dualpath
+# changes until it is measured again.
+K1_TRAFFIC_PER_LAUNCH = 59_408_736
+
+
 def peaks():
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
@@ -332,7 +340,10 @@ def run_ours(args, world, rank, local):
         "tok_s": world * args.steps / (t_max / 1e3),
         "tok_s_per_gpu": args.steps / (t_max / 1e3),
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                     "frac": achieved / peak, "traffic": None,
+                     "frac": achieved / peak, "traffic": K1_TRAFFIC_PER_LAUNCH,
+                     "algorithmic_bytes_per_launch": alg / len(groups),
+                     "traffic_note": "dram__bytes_read.sum + dram__bytes_write.sum per k_dualpath launch, mean over "
+                                     "the step's launches, from one ncu capture of this kernel build on this workload",
                      "kernel": "k_dualpath (4 launches per step: qkv, o, gate+up, down)",
                      "note": f"peak = {peak_kind} HBM copy bandwidth; achieved = algorithmic bytes per step / mean "
                              f"step, CUDA events on the launching stream around the timed region (a step is "
