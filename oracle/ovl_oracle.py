@@ -18,6 +18,12 @@ Function -> pin (tests/test_oracle_pins.py):
 * f16_to_float            exhaustive vs numpy's binary16 decoder (all 65536 patterns)
 * dequantize_q8_0/q4_0    exhaustive (every finite scale x every code) vs exact
                           products; exact rationals on a sample; hand-built nibbles
+* q4_k_header_fields      every 6-bit value in every sub-block slot vs headers
+                          packed bit by bit; random headers vs a bit-string decode
+* dequantize_q4_k         reduces bitwise to dequantize_q4_0 (sc = 1, m = 8,
+                          dmin = d); hand-evaluated sub-block staircase; exact
+                          rationals on every (sc, m, code) with sampled scales;
+                          4.5 bits per weight
 * dual_path / merged_path exact-rational brute force on tiny shapes; dual == merged
                           identity; zero-B and unit outer-product closed forms
 * effective_weight        closed forms (zero-B, e_i e_j^T), order invariance in
@@ -39,8 +45,10 @@ from dataclasses import dataclass, field
 import numpy as np
 
 QK = 32
+QK_K = 256           # weights per q4_K super-block
 Q8_0 = 1
 Q4_0 = 2
+Q4_K = 3
 MODE_STACK = 1
 MODE_TABLE = 2
 LEAF = 65536
@@ -112,11 +120,60 @@ def dequantize_q4_0(packed: np.ndarray, d_bits: np.ndarray) -> np.ndarray:
     return np.repeat(d, QK, axis=1) * (codes - 8).astype(np.float64)
 
 
+# --------------------------------------------------------------------------
+# q4_K super-blocks.
+# [DTD] §5 "Quantized-Base Numerical Analysis": a q4_K super-block holds 256
+# weights in 8 sub-blocks of 32; every sub-block has a 6-bit scale and a 6-bit
+# minimum (zero-point), and two f16 scales govern the whole super-block, for
+# 4.5 bits per weight.  Reading: the sub-block scale multiplies the f16 scale d
+# and the sub-block minimum multiplies the f16 scale dmin, and the minimum is
+# subtracted, w = d*sc_j*code - dmin*m_j with a 4-bit code.  The pages give no
+# byte packing; the header of each super-block is 16 bytes:
+#   bytes 0-1  d (binary16), bytes 2-3 dmin (binary16),
+#   bytes 4-9  the eight sc_j as one 48-bit little-endian field, sc_j in bits 6j..6j+5,
+#   bytes 10-15 the eight m_j the same way.
+# Codes use the q4_0 nibble order within the row.
+# --------------------------------------------------------------------------
+def q4_k_header_fields(hdr: np.ndarray):
+    """Split 16-byte headers [..][16] into (d, dmin, sc[..][8], m[..][8]).
+
+    d and dmin are float64 values; sc and m are integers 0..63.
+    """
+    h = np.asarray(hdr, dtype=np.uint8).astype(np.int64)
+    d = f16_to_float(h[..., 0] + 256 * h[..., 1])
+    dmin = f16_to_float(h[..., 2] + 256 * h[..., 3])
+
+    def field48(bytes6):
+        # the six bytes as one little-endian integer, then eight 6-bit slices
+        v = np.zeros(bytes6.shape[:-1], dtype=np.int64)
+        for k in range(6):
+            v += bytes6[..., k] << (8 * k)
+        return np.stack([(v >> (6 * j)) & 63 for j in range(8)], axis=-1)
+
+    return d, dmin, field48(h[..., 4:10]), field48(h[..., 10:16])
+
+
+def dequantize_q4_k(packed: np.ndarray, hdr: np.ndarray) -> np.ndarray:
+    """w[i][c] = d * sc_j * code[i][c] - dmin * m_j, j = (c mod 256) / 32, in float64.
+
+    packed: uint8 [m][n/2] codes (q4_0 nibble order); hdr: uint8 [m][n/256][16]
+    (or [m][n/16]).  Exact: every product has at most 11+6+4 significant bits.
+    """
+    codes = q4_0_codes(packed).astype(np.float64)
+    m, n = codes.shape
+    d, dmin, sc, mn = q4_k_header_fields(np.asarray(hdr, np.uint8).reshape(m, n // QK_K, 16))
+    scale = (d[..., None] * sc).reshape(m, n // QK)       # per 32-weight sub-block
+    minimum = (dmin[..., None] * mn).reshape(m, n // QK)
+    return np.repeat(scale, QK, axis=1) * codes - np.repeat(minimum, QK, axis=1)
+
+
 def dequantize(quant: int, qs, d_bits) -> np.ndarray:
     if quant == Q8_0:
         return dequantize_q8_0(qs, d_bits)
     if quant == Q4_0:
         return dequantize_q4_0(qs, d_bits)
+    if quant == Q4_K:
+        return dequantize_q4_k(qs, d_bits)
     raise ValueError("unknown quant profile")
 
 

@@ -17,6 +17,11 @@ Byte layout (the library's written format; see the header ``include/ovl.h``):
   q4_0: ``qs`` is uint8 ``[d_out][d_in/2]``; byte ``p`` of a row holds element
   ``2p`` in bits 0-3 and element ``2p+1`` in bits 4-7, codes 0..15.
   ``d`` is IEEE binary16 ``[d_out][d_in/32]`` (one scale per 32-block).
+  q4_K: ``qs`` as q4_0; the ``d`` plane holds one 16-byte header per
+  256-weight super-block, ``[d_out][d_in/256][16]``: binary16 d, binary16 dmin,
+  then the eight 6-bit sub-block scales as one 48-bit little-endian field
+  (scale j in bits 6j..6j+5) and the eight 6-bit sub-block minimums the same
+  way.  Same plane sizes as q4_0 (4.5 bits per weight).
 * adapter payload: per target an fp32 ``A [r][d_in]`` and fp32 ``B [d_out][r]``,
   each starting on a 256-byte boundary.
 """
@@ -28,11 +33,13 @@ from dataclasses import dataclass, field
 import numpy as np
 
 QK = 32                      # weights per quantization block
+QK_K = 256                   # weights per q4_K super-block
 ALIGN = 256                  # plane / factor alignment inside a buffer
 LEAF = 65536                 # leaf size of the content digest (bytes)
 
 Q8_0 = 1
 Q4_0 = 2
+Q4_K = 3
 
 PROJ = ("q", "k", "v", "o", "gate", "up", "down")
 # (d_out, d_in) of the seven projections of one decoder block at 8B shape
@@ -121,6 +128,57 @@ def quantize_q4_0(w: np.ndarray):
     return packed, d16.view(np.uint16)
 
 
+def pack6x8(v: np.ndarray) -> np.ndarray:
+    """[..][8] integers 0..63 -> [..][6] bytes: one 48-bit little-endian field,
+    value j in bits 6j..6j+5."""
+    v = np.asarray(v, dtype=np.uint64)
+    f = np.zeros(v.shape[:-1], dtype=np.uint64)
+    for j in range(8):
+        f |= v[..., j] << np.uint64(6 * j)
+    return np.stack([((f >> np.uint64(8 * k)) & np.uint64(0xFF)).astype(np.uint8) for k in range(6)], axis=-1)
+
+
+def quantize_q4_k(w: np.ndarray):
+    """float32 [m][n] -> (qs uint8 [m][n/2] packed nibbles, headers uint8 [m][n/16]).
+
+    Per 32-weight sub-block j (fp32 arithmetic): lo_j = min(min w, 0),
+    step_j = (max w - lo_j) / 15, zero-point mu_j = -lo_j.  Per super-block:
+    d = fp16(max_j step_j / 63), dmin = fp16(max_j mu_j / 63),
+    sc_j = clamp(round_half_away(step_j / d), 0, 63),
+    m_j = clamp(round_half_away(mu_j / dmin), 0, 63) (0 where d or dmin is 0);
+    code = clamp(round_half_away((w + dmin*m_j) / (d*sc_j)), 0, 15) (0 where
+    d*sc_j is 0), value d*sc_j*code - dmin*m_j.
+    """
+    w = np.ascontiguousarray(w, dtype=np.float32)
+    m, n = w.shape
+    assert n % QK_K == 0
+    blk = w.reshape(m, n // QK_K, 8, QK)
+    lo = np.minimum(blk.min(axis=3), np.float32(0))
+    step = (blk.max(axis=3) - lo) / np.float32(15.0)
+    mu = -lo
+    d16 = (step.max(axis=2) / np.float32(63.0)).astype(np.float16)
+    dm16 = (mu.max(axis=2) / np.float32(63.0)).astype(np.float16)
+    d32 = d16.astype(np.float32)[..., None]
+    dm32 = dm16.astype(np.float32)[..., None]
+    with np.errstate(divide="ignore", invalid="ignore"):
+        sc = np.where(d32 > 0, round_half_away(step / d32), np.float32(0))
+        mq = np.where(dm32 > 0, round_half_away(mu / dm32), np.float32(0))
+    sc = np.clip(sc, 0, 63)
+    mq = np.clip(mq, 0, 63)
+    eff_scale = (d32 * sc)[..., None]
+    eff_min = (dm32 * mq)[..., None]
+    with np.errstate(divide="ignore", invalid="ignore"):
+        q = np.where(eff_scale > 0, round_half_away((blk + eff_min) / eff_scale), np.float32(0))
+    code = np.clip(q, 0, 15).astype(np.uint8).reshape(m, n)
+    packed = (code[:, 0::2] | (code[:, 1::2] << 4)).astype(np.uint8)
+    hdr = np.zeros((m, n // QK_K, 16), dtype=np.uint8)
+    hdr[..., 0:2] = d16.view(np.uint16)[..., None].view(np.uint8).reshape(m, n // QK_K, 2)
+    hdr[..., 2:4] = dm16.view(np.uint16)[..., None].view(np.uint8).reshape(m, n // QK_K, 2)
+    hdr[..., 4:10] = pack6x8(sc.astype(np.int64))
+    hdr[..., 10:16] = pack6x8(mq.astype(np.int64))
+    return packed, hdr.reshape(m, n // 16)
+
+
 def to_bf16_bits(x: np.ndarray) -> np.ndarray:
     """float32 -> bfloat16 bit patterns (uint16), round-to-nearest-even."""
     u = np.ascontiguousarray(x, dtype=np.float32).view(np.uint32).astype(np.uint64)
@@ -164,7 +222,7 @@ def d_bytes(d_out: int, d_in: int) -> int:
 
 def build_base(quant: int, items) -> Base:
     """items: iterable of (layer, proj, w_float32[d_out][d_in]) -> Base."""
-    qz = quantize_q8_0 if quant == Q8_0 else quantize_q4_0
+    qz = {Q8_0: quantize_q8_0, Q4_0: quantize_q4_0, Q4_K: quantize_q4_k}[quant]
     enc = []
     off = 0
     descs = []
@@ -195,6 +253,9 @@ def base_planes(base: Base, i: int):
         qs = qs.view(np.int8).reshape(t.d_out, t.d_in)
     else:
         qs = qs.reshape(t.d_out, t.d_in // 2)
+    if base.quant == Q4_K:
+        hdr = base.buf[t.d_off:t.d_off + d_bytes(t.d_out, t.d_in)]
+        return qs, hdr.reshape(t.d_out, t.d_in // QK_K, 16)
     d = base.buf[t.d_off:t.d_off + d_bytes(t.d_out, t.d_in)].view(np.uint16)
     return qs, d.reshape(t.d_out, t.d_in // QK)
 

@@ -104,6 +104,124 @@ def test_quantizer_q4_round_trip_through_oracle_dequant():
     assert np.array_equal(p2, packed)
 
 
+# ---------------------------------------------------------------- q4_K
+def _hdr_bitwise(d_bits: int, dmin_bits: int, sc, mn) -> np.ndarray:
+    """One 16-byte q4_K header built bit by bit (independent of any packer):
+    value j of a 6-bit field sets bits 6j..6j+5 of its six bytes, LSB first."""
+    out = [d_bits & 0xFF, d_bits >> 8, dmin_bits & 0xFF, dmin_bits >> 8] + [0] * 12
+    for base, vals in ((4, sc), (10, mn)):
+        for j, v in enumerate(vals):
+            for b in range(6):
+                if (int(v) >> b) & 1:
+                    pos = 6 * j + b
+                    out[base + pos // 8] |= 1 << (pos % 8)
+    return np.array(out, dtype=np.uint8)
+
+
+def test_q4_k_header_every_value_in_every_slot():
+    hdrs, want = [], []
+    for j in range(8):
+        for v in range(64):
+            sc = [0] * 8
+            mn = [0] * 8
+            sc[j] = v
+            mn[7 - j] = 63 - v
+            hdrs.append(_hdr_bitwise(0x3C00, 0x4000, sc, mn))
+            want.append((sc, mn))
+    d, dmin, sc, mn = O.q4_k_header_fields(np.stack(hdrs))
+    assert np.all(d == 1.0) and np.all(dmin == 2.0)
+    assert np.array_equal(sc, np.array([w[0] for w in want]))
+    assert np.array_equal(mn, np.array([w[1] for w in want]))
+
+
+def test_q4_k_header_random_vs_bit_string():
+    rng = np.random.default_rng(11)
+    h = rng.integers(0, 256, size=(300, 16)).astype(np.uint8)
+    _, _, sc, mn = O.q4_k_header_fields(h)
+    for i in range(300):
+        for base, got in ((4, sc[i]), (10, mn[i])):
+            # bit string, least significant bit of byte `base` first
+            bits = "".join(format(int(b), "08b")[::-1] for b in h[i, base:base + 6])
+            vals = [int(bits[6 * j:6 * j + 6][::-1], 2) for j in range(8)]
+            assert list(got) == vals
+
+
+def test_q4_k_reduces_to_q4_0():
+    # sc_j = 1, m_j = 8 and dmin = d give d*code - 8d = d*(code - 8): q4_0 exactly
+    rng = np.random.default_rng(12)
+    m, n = 9, 512
+    packed = rng.integers(0, 256, size=(m, n // 2)).astype(np.uint8)
+    dfin = _finite_f16_bits()
+    dbits = rng.choice(dfin, size=(m, n // 256))
+    hdr = np.stack([np.stack([_hdr_bitwise(int(dbits[i, k]), int(dbits[i, k]), [1] * 8, [8] * 8)
+                              for k in range(n // 256)]) for i in range(m)])
+    d32 = np.repeat(dbits, 8, axis=1)                         # the same d for every 32-block
+    assert np.array_equal(O.dequantize_q4_k(packed, hdr), O.dequantize_q4_0(packed, d32))
+
+
+def test_q4_k_sub_block_staircase_hand_evaluated():
+    # d = 1, dmin = 0.5, sc_j = j + 1, m_j = 2j, every code 3:
+    # sub-block j of every super-block holds 3(j + 1) - j = 2j + 3
+    hdr = _hdr_bitwise(0x3C00, 0x3800, [j + 1 for j in range(8)], [2 * j for j in range(8)])
+    packed = np.full((1, 256), 0x33, dtype=np.uint8)          # two super-blocks
+    w = O.dequantize_q4_k(packed, np.stack([hdr, hdr])[None])[0]
+    want = np.repeat(np.array([2 * j + 3 for j in range(8)] * 2, dtype=np.float64), 32)
+    assert np.array_equal(w, want)
+    # nibble order inside a sub-block: byte 0 = 0x51 -> element 0 code 1, element 1 code 5
+    packed[0, 0] = 0x51
+    w = O.dequantize_q4_k(packed, np.stack([hdr, hdr])[None])[0]
+    assert w[0] == 1.0 and w[1] == 5.0 and w[2] == 3.0
+
+
+def test_q4_k_exact_rationals_every_scale_min_code():
+    rng = np.random.default_rng(13)
+    dfin = _finite_f16_bits()
+    rows = []
+    want = []
+    for sc in range(64):
+        d_bits, dm_bits = int(rng.choice(dfin)), int(rng.choice(dfin))
+        dv = Fraction(float(np.array([d_bits], np.uint16).view(np.float16)[0]))
+        dmv = Fraction(float(np.array([dm_bits], np.uint16).view(np.float16)[0]))
+        mins = [(sc + 8 * j) % 64 for j in range(8)]          # every m over the 64 rows x 8 slots
+        hdr = _hdr_bitwise(d_bits, dm_bits, [sc] * 8, mins)
+        codes = np.tile(np.arange(16, dtype=np.uint8), 16)     # every code in every sub-block
+        rows.append((codes[0::2] | (codes[1::2] << 4), hdr))
+        want.append([dv * sc * int(codes[c]) - dmv * mins[c // 32] for c in range(256)])
+    packed = np.stack([r[0] for r in rows])
+    hdr = np.stack([r[1] for r in rows])[:, None, :]
+    w = O.dequantize_q4_k(packed, hdr)
+    for i in range(64):
+        assert [Fraction(float(v)) for v in w[i]] == want[i]
+
+
+def test_q4_k_is_4_5_bits_per_weight():
+    m, n = 3, 1024
+    qs, hdr = S.quantize_q4_k(np.zeros((m, n), np.float32))
+    assert (qs.nbytes + hdr.nbytes) * 8 == 4.5 * m * n
+    assert S.qs_bytes(S.Q4_K, m, n) + S.d_bytes(m, n) == qs.nbytes + hdr.nbytes
+
+
+def test_q4_k_quantizer_round_trip_through_oracle_dequant():
+    # weights that are exactly representable with full-range codes re-quantize
+    # to the same bytes: sc = 63 and m = 63 in some sub-block fix d and dmin
+    rng = np.random.default_rng(14)
+    m, n = 4, 512
+    codes = rng.integers(0, 16, size=(m, n)).astype(np.uint8)
+    codes[:, ::32] = 0
+    codes[:, 1::32] = 15                                     # every sub-block spans 0..15
+    sc = rng.integers(1, 64, size=(m, n // 256, 8))
+    mn = rng.integers(1, 64, size=(m, n // 256, 8))
+    sc[..., 0] = 63
+    mn[..., 0] = 63
+    d = np.float16(0.001)
+    hdr = np.stack([np.stack([_hdr_bitwise(int(d.view(np.uint16)), int(d.view(np.uint16)), sc[i, k], mn[i, k])
+                              for k in range(n // 256)]) for i in range(m)])
+    packed = (codes[:, 0::2] | (codes[:, 1::2] << 4)).astype(np.uint8)
+    w = O.dequantize_q4_k(packed, hdr)
+    p2, h2 = S.quantize_q4_k(w.astype(np.float32))
+    assert np.array_equal(O.dequantize_q4_k(p2, h2), w)
+
+
 # ---------------------------------------------------------------- GEMV / LoRA
 def _tiny_problem(seed, m=6, n=64, T=2, ranks=(2, 3)):
     rng = np.random.default_rng(seed)
