@@ -483,6 +483,36 @@ def workload_q4_stacked(args):
 WORKLOADS["q4-stacked"] = workload_q4_stacked
 
 
+def workload_q4k_decode(args):
+    """The 8B-shape block with a q4_K base (256-weight super-blocks, 4.5 bits per
+    weight) and one rank-16 adapter (s = 2.0) on all 7 projections, batch-1
+    decode, x bf16: the same step as the headline decode line, q4_K bytes."""
+    import torch
+    base = S.block_base(S.Q4_K)
+    ad = S.block_adapter(base, adapter=0, rank=RANK)
+    rts = _contexts(base, [ad], [2.0], N_COPIES, 96)
+    stream = torch.cuda.Stream()
+    sh = int(stream.cuda_stream)
+    planes = sum(S.qs_bytes(base.quant, t.d_out, t.d_in) + S.d_bytes(t.d_out, t.d_in) for t in base.tensors)
+    lora = sum(RANK * (t.d_in + t.d_out) * 4 for t in base.tensors)
+    T = 1
+    xs = {d: torch.from_numpy(S.to_bf16_bits(S.activations(T, d)).view(np.int16)).cuda().view(torch.bfloat16)
+          for d in (4096, 14336)}
+    ybufs = [torch.empty((T, t.d_out), dtype=torch.float32, device="cuda") for t in base.tensors]
+    step = _block_step(base, rts, {d: v.data_ptr() for d, v in xs.items()}, [y.data_ptr() for y in ybufs], T, sh)
+    ms = timed_steps(step, args.steps, args.warmup, stream)
+    _check_all(rts, sh)
+    alg = planes + lora + sum(T * (t.d_in * 2 + t.d_out * 4) for t in base.tensors)
+    emit({"workload": "q4k-decode", "metric": "decode effective weight GB/s & tok/s (8B shape, q4_K + r16 LoRA)",
+          "unit": "GB/s", "value": (planes + lora) / (ms / 1e3) / 1e9, "ms_per_step": ms, "tok_s": 1e3 / ms,
+          "steps": args.steps, "roofline": hbm_roofline(alg, ms, "k_dualpath (4 launches per step)"),
+          "config": {"base": f"8B-shape block q4_K ({planes / 1e6:.1f} MB)", "adapter": "r16 s=2.0 on all 7",
+                     "x": "bf16", "l2": f"{N_COPIES} base copies rotated"}})
+
+
+WORKLOADS["q4k-decode"] = workload_q4k_decode
+
+
 def workload_segmented(args):
     import torch
     import quantized_base_lora_gb300 as q

@@ -43,7 +43,18 @@
  *             and element 2p+1 in bits 4-7; codes 0..15; weight = d * (code - 8).
  *       d   = IEEE binary16, little-endian, [d_out][d_in/32], one scale per 32 weights.
  *     ([DTD] §5 "Quantized-Base Numerical Analysis": 32-weight blocks, one f16 scale.)
- *     The d plane, rounded up to a multiple of 16 bytes, must lie inside the buffer.
+ *       q4_K: qs as q4_0.  The d plane holds one 16-byte header per 256-weight
+ *             super-block, [d_out][d_in/256][16]: bytes 0-1 d and bytes 2-3 dmin
+ *             (IEEE binary16), bytes 4-9 the eight 6-bit sub-block scales sc_j as
+ *             one 48-bit little-endian field (sc_j in bits 6j..6j+5), bytes 10-15
+ *             the eight 6-bit sub-block minimums m_j the same way.  Weight c of a
+ *             row = d * sc_j * code - dmin * m_j with j = (c mod 256) / 32.
+ *             ([DTD] §5: 256-weight super-blocks of 8 sub-blocks of 32, a 6-bit
+ *             scale and a 6-bit minimum per sub-block, two f16 super-block
+ *             scales, 4.5 bits per weight; the byte packing is this library's.)
+ *             d_in must be a multiple of 256.
+ *     The d plane, rounded up to a multiple of 16 bytes, must lie inside the buffer
+ *     (d_out * d_in / 16 bytes for every profile).
  *     d_in must be a multiple of 32.
  *   Adapter payload (host, copied into the arena by ovl_stage_adapter):
  *     per target tensor t: A_t = float32 [rank][d_in] at a_off, B_t = float32
@@ -99,7 +110,7 @@ enum {
   OVL_E_DEVICE_TIMEOUT = -13 /* a bounded device-side wait ran out */
 };
 
-enum { OVL_Q8_0 = 1, OVL_Q4_0 = 2 };                 /* quantization profile */
+enum { OVL_Q8_0 = 1, OVL_Q4_0 = 2, OVL_Q4_K = 3 };   /* quantization profile */
 enum { OVL_F32 = 1, OVL_BF16 = 2 };                  /* activation dtype */
 enum { OVL_MODE_STACK = 1, OVL_MODE_TABLE = 2 };     /* composition mode */
 enum { OVL_PATH_DUAL = 1, OVL_PATH_JIT = 2 };        /* evaluation path */
@@ -125,7 +136,7 @@ typedef struct {
 } ovl_tensor_desc;
 
 typedef struct {
-  uint32_t quant;             /* OVL_Q8_0 or OVL_Q4_0 */
+  uint32_t quant;             /* OVL_Q8_0, OVL_Q4_0 or OVL_Q4_K */
   uint32_t n_tensors;
   const ovl_tensor_desc* tensors;   /* host array of n_tensors, copied */
 } ovl_base_desc;
@@ -287,7 +298,8 @@ ovl_status ovl_segmented_forward(ovl_ctx* ctx, uint32_t tensor, const void* x, u
  * array's status word on `stream` and then reuses its contents;
  * calls that overlap on the GPU (different streams, or other threads) race on
  * the array and must be serialized by the caller.
- * Errors: OVL_E_QUANT, OVL_E_SHAPE (d_in, alignment, rank, total rank), OVL_E_ARG
+ * Errors: OVL_E_QUANT (also for OVL_Q4_K, which this entry point does not
+ * take), OVL_E_SHAPE (d_in, alignment, rank, total rank), OVL_E_ARG
  * (null pointers, dtype, T > OVL_MAX_T, n_terms > OVL_MAX_STACK, non-finite
  * scale), OVL_E_OOM (the low-rank partial sums would need more than the 2 MiB
  * array), OVL_E_CUDA.  T = 0 is a no-op.  Device-side timeouts are latched in

@@ -33,7 +33,7 @@ OVL_E_CUDA = -12
 OVL_E_DEVICE_TIMEOUT = -13
 STATUS_NAMES = {v: k for k, v in list(globals().items()) if k.startswith("OVL_E_") or k == "OVL_OK"}
 
-OVL_Q8_0, OVL_Q4_0 = 1, 2
+OVL_Q8_0, OVL_Q4_0, OVL_Q4_K = 1, 2, 3
 OVL_F32, OVL_BF16 = 1, 2
 OVL_MODE_STACK, OVL_MODE_TABLE = 1, 2
 OVL_PATH_DUAL, OVL_PATH_JIT = 1, 2

@@ -633,7 +633,10 @@ template <int QUANT, int TT, int RG>
 __global__ void __launch_bounds__(K1Shape<TT, RG>::threads, K1Shape<TT, RG>::min_blocks)
     k_dualpath(const DualArgs a, const DualCfg c) {
   constexpr int NREG = K1Shape<TT, RG>::reg_records;
-  constexpr bool Q4 = QUANT == OVL_Q4_0;
+  // q4_K shares q4_0's codes, records and stage layout; only the per-block
+  // scale (and its minimum term) differ.
+  constexpr bool QK4 = QUANT == OVL_Q4_K;
+  constexpr bool Q4 = QUANT == OVL_Q4_0 || QK4;
   constexpr int N = TT * RG;
   constexpr int LN = Log2<N>::v;
   constexpr uint32_t kBlockBytes = Q4 ? 16 : 32;
@@ -927,12 +930,36 @@ __global__ void __launch_bounds__(K1Shape<TT, RG>::threads, K1Shape<TT, RG>::min
     for (int i = 0; i < N; ++i) acc[i] = 0.f;
     auto block = [&](uint32_t b, const uint4 (&r)[7], int t) {
       const float xs = __uint_as_float(r[6].x);
+      if constexpr (QK4) {
+        // Sub-block j = b mod 8 of a 256-weight super-block: weight
+        // d*sc_j*code - dmin*m_j, so the block sum is
+        // xs*(d*sc_j*sum(code*X) - dmin*m_j*sum(X)).  The record's accumulator
+        // starts hold -8*sum(X) in limbs, so dot_q4 gives sum((code-8)*X).
+        const float sx8 = -limb_combine(static_cast<int>(r[6].y), static_cast<int>(r[6].z), static_cast<int>(r[6].w));
+        const uint32_t j6 = 6u * (b & 7u);
+        const uint8_t* hb = reinterpret_cast<const uint8_t*>(sd) + (b >> 3) * 16u;
 #pragma unroll
-      for (int rr = 0; rr < RG; ++rr) {
-        const uint8_t* wp = sq + rr * c.rowbytes + b * kBlockBytes;
-        const float P = Q4 ? dot_q4(wp, r) : dot_q8(wp, r);
-        const float d = __half2float(sd[rr * c.nb + b]);
-        acc[t * RG + rr] = fmaf(d * xs, P, acc[t * RG + rr]);
+        for (int rr = 0; rr < RG; ++rr) {
+          const uint8_t* wp = sq + rr * c.rowbytes + b * kBlockBytes;
+          const float P = dot_q4(wp, r) + sx8;                       // sum(code*X)
+          const uint4 h = *reinterpret_cast<const uint4*>(hb + static_cast<size_t>(rr) * c.nb * 2);
+          const uint64_t scf = (static_cast<uint64_t>(h.z & 0xFFFFu) << 32) | h.y;
+          const uint64_t mnf = (static_cast<uint64_t>(h.w) << 16) | (h.z >> 16);
+          const float dsc = __half2float(__ushort_as_half(static_cast<unsigned short>(h.x & 0xFFFFu))) *
+                            static_cast<float>(static_cast<uint32_t>(scf >> j6) & 63u);
+          const float dmn = __half2float(__ushort_as_half(static_cast<unsigned short>(h.x >> 16))) *
+                            static_cast<float>(static_cast<uint32_t>(mnf >> j6) & 63u);
+          acc[t * RG + rr] = fmaf(dsc * xs, P, acc[t * RG + rr]);
+          acc[t * RG + rr] = fmaf(-dmn * xs, 0.125f * sx8, acc[t * RG + rr]);
+        }
+      } else {
+#pragma unroll
+        for (int rr = 0; rr < RG; ++rr) {
+          const uint8_t* wp = sq + rr * c.rowbytes + b * kBlockBytes;
+          const float P = Q4 ? dot_q4(wp, r) : dot_q8(wp, r);
+          const float d = __half2float(sd[rr * c.nb + b]);
+          acc[t * RG + rr] = fmaf(d * xs, P, acc[t * RG + rr]);
+        }
       }
     };
     if (TT == 1) {
@@ -1084,6 +1111,8 @@ KernelFn pick(uint32_t quant, int tt, int rg) {
   OVL_K(OVL_Q8_0, 2, 2) OVL_K(OVL_Q8_0, 4, 2) OVL_K(OVL_Q8_0, 8, 2)
   OVL_K(OVL_Q4_0, 1, 2) OVL_K(OVL_Q4_0, 1, 4) OVL_K(OVL_Q4_0, 1, 8)
   OVL_K(OVL_Q4_0, 2, 2) OVL_K(OVL_Q4_0, 4, 2) OVL_K(OVL_Q4_0, 8, 2)
+  OVL_K(OVL_Q4_K, 1, 2) OVL_K(OVL_Q4_K, 1, 4) OVL_K(OVL_Q4_K, 1, 8)
+  OVL_K(OVL_Q4_K, 2, 2) OVL_K(OVL_Q4_K, 4, 2) OVL_K(OVL_Q4_K, 8, 2)
 #undef OVL_K
   return nullptr;
 }

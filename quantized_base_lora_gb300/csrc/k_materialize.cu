@@ -35,7 +35,25 @@ __global__ void __launch_bounds__(256) k_materialize(const MatArgs a) {
     const uint32_t r = row0 + ty * 4 + i;
 #pragma unroll
     for (int j = 0; j < 4; ++j) acc[i][j] = 0.f;
-    if (r < a.m && c < a.n) {
+    if (r < a.m && c < a.n && a.quant == OVL_Q4_K) {
+      // 16-byte super-block header: d, dmin, 6-bit sc_j and m_j of sub-block
+      // j = (c mod 256) / 32 (all four columns lie in one sub-block).
+      const uint4 h = *reinterpret_cast<const uint4*>(a.dpl + static_cast<size_t>(r) * (a.n / 16) + (c / kQKK) * 16);
+      const uint32_t j6 = 6u * ((c % kQKK) / kQK);
+      const uint64_t scf = (static_cast<uint64_t>(h.z & 0xFFFFu) << 32) | h.y;
+      const uint64_t mnf = (static_cast<uint64_t>(h.w) << 16) | (h.z >> 16);
+      const float dsc = __half2float(__ushort_as_half(static_cast<unsigned short>(h.x & 0xFFFFu))) *
+                        static_cast<float>(static_cast<uint32_t>(scf >> j6) & 63u);
+      const float dmn = __half2float(__ushort_as_half(static_cast<unsigned short>(h.x >> 16))) *
+                        static_cast<float>(static_cast<uint32_t>(mnf >> j6) & 63u);
+      const uchar2 q = *reinterpret_cast<const uchar2*>(a.qs + static_cast<size_t>(r) * (a.n / 2) + c / 2);
+      // d*sc*code (<= 21 significant bits) and dmin*m (<= 17) are exact in
+      // fp32; the fused multiply-add rounds their difference once.
+      acc[i][0] = fmaf(dsc, static_cast<float>(q.x & 0xF), -dmn);
+      acc[i][1] = fmaf(dsc, static_cast<float>(q.x >> 4), -dmn);
+      acc[i][2] = fmaf(dsc, static_cast<float>(q.y & 0xF), -dmn);
+      acc[i][3] = fmaf(dsc, static_cast<float>(q.y >> 4), -dmn);
+    } else if (r < a.m && c < a.n) {
       const __half dh = reinterpret_cast<const __half*>(a.dpl)[static_cast<size_t>(r) * (a.n / kQK) + c / kQK];
       const float d = __half2float(dh);
       if (a.quant == OVL_Q8_0) {

@@ -396,13 +396,16 @@ ovl_status ovl_load_base(ovl_ctx* ctx, const ovl_base_desc* desc, const void* ba
   if (ctx->base_loaded) return fail(ctx, OVL_E_STATE, "base already loaded");
   if (!desc || !base_dev || !digest || (desc->n_tensors && !desc->tensors))
     return fail(ctx, OVL_E_ARG, "null argument");
-  if (desc->quant != OVL_Q8_0 && desc->quant != OVL_Q4_0) return fail(ctx, OVL_E_QUANT, "unknown quantization profile");
+  if (desc->quant != OVL_Q8_0 && desc->quant != OVL_Q4_0 && desc->quant != OVL_Q4_K)
+    return fail(ctx, OVL_E_QUANT, "unknown quantization profile");
   if (desc->n_tensors == 0) return fail(ctx, OVL_E_SHAPE, "base has no tensors");
   if ((reinterpret_cast<uintptr_t>(base_dev) & 15) != 0) return fail(ctx, OVL_E_SHAPE, "base must be 16-byte aligned");
   for (uint32_t i = 0; i < desc->n_tensors; ++i) {
     const ovl_tensor_desc& t = desc->tensors[i];
     const std::string who = "tensor " + std::to_string(i) + ": ";
     if (t.d_out == 0 || t.d_in == 0 || t.d_in % kQK != 0) return fail(ctx, OVL_E_SHAPE, who + "d_in must be a positive multiple of 32");
+    if (desc->quant == OVL_Q4_K && t.d_in % kQKK != 0)
+      return fail(ctx, OVL_E_SHAPE, who + "q4_K: d_in must be a multiple of 256");
     if (t.qs_off % 16 || t.d_off % 16) return fail(ctx, OVL_E_SHAPE, who + "plane offsets must be multiples of 16");
     const uint64_t qsb = desc->quant == OVL_Q8_0 ? uint64_t(t.d_out) * t.d_in : uint64_t(t.d_out) * t.d_in / 2;
     const uint64_t db = (uint64_t(t.d_out) * (t.d_in / kQK) * 2 + 15) / 16 * 16;
@@ -615,9 +618,11 @@ uint32_t stack_terms(ovl_ctx* c, const Composition& comp, uint32_t tensor, LoraR
 // the q4_0 block: 204 vs 184 us at 4 tokens, 431 vs 191 us at 8).
 constexpr uint32_t kTcMinT = 4;
 
-// The tensor-core kernel reads the activations 16 bytes at a time.
+// The tensor-core kernel reads the activations 16 bytes at a time, and reads
+// per-block f16 scales (q8_0, q4_0); q4_K super-blocks always take K1.
 bool use_tc(const ovl_ctx* c, uint32_t T, const ovl_tensor_desc& td, uint32_t rtot, const void* x) {
-  return T >= kTcMinT && (reinterpret_cast<uintptr_t>(x) & 15) == 0 && c->ws.tc_scratch_bytes > 0 &&
+  return T >= kTcMinT && c->quant != OVL_Q4_K && (reinterpret_cast<uintptr_t>(x) & 15) == 0 &&
+         c->ws.tc_scratch_bytes > 0 &&
          fused_gemm_supported(td.d_out, td.d_in) &&
          fused_gemm_scratch_bytes(T, td.d_in, fused_vcols(rtot)) <= c->ws.tc_scratch_bytes;
 }

@@ -10,6 +10,7 @@
 namespace ovl {
 
 constexpr int kQK = 32;                 // weights per quantization block
+constexpr int kQKK = 256;               // weights per q4_K super-block (16-byte header each)
 constexpr size_t kLeaf = 65536;         // content-digest leaf size
 
 // Device status word codes (latched by kernels, read by ovl_check_device).

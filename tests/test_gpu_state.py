@@ -180,7 +180,8 @@ def test_base_load_errors():
     tt = tensor_tuples(base)
     rt = Runtime(arena_bytes=32 << 20)
     assert rt.load_base(base.quant, tt, base.buf, bytes(32)) == q.OVL_E_HASH
-    assert rt.load_base(3, tt, base.buf, S.content_digest(base.buf)) == q.OVL_E_QUANT
+    for unknown in (0, 4, 9):
+        assert rt.load_base(unknown, tt, base.buf, S.content_digest(base.buf)) == q.OVL_E_QUANT
     bad = [(0, 0, 256, 256, 0, base.buf.nbytes)]
     assert rt.load_base(base.quant, bad, base.buf, S.content_digest(base.buf)) == q.OVL_E_SHAPE
     bad = [(0, 0, 256, 250, 0, 65536)]
