@@ -29,6 +29,12 @@ Function -> pin (tests/test_oracle_pins.py):
 * effective_weight        closed forms (zero-B, e_i e_j^T), order invariance in
                           exact arithmetic
 * error_bound             hand-evaluated 2x2 example
+* SparseTerm / sparse_delta and the sparse terms of effective_weight,
+  dual_path            one entry moves exactly one weight by s*v (closed form);
+                          a sparse overlay equal to a rank-1 outer product gives
+                          the same W' and y as that LoRA term; exact-rational
+                          brute force on tiny shapes; dual == merged with mixed
+                          stacks
 * segmented               reduces to dual_path per token (brute force)
 * tree_digest             single-leaf closed form SHA256(SHA256(data)); FIPS 180
                           test vectors for the primitive
@@ -187,19 +193,68 @@ def dequantize(quant: int, qs, d_bits) -> np.ndarray:
 # [OVR] §"Native/WASM Kernel Implications": direct low-rank addition
 # y = xW + x(BA) (two small matmuls) vs pre-merged W' = W + BA.
 # --------------------------------------------------------------------------
+# --------------------------------------------------------------------------
+# Sparse overlays.
+# [OVR] §"Runtime Strategy Comparison Matrix" (Sparse Overlay): only the
+# non-zero elements of the update are stored, as indices and values, and they
+# are added at those indices at use time; the base is unchanged.
+# [OVR] §"Memory, Byte, and Latency Formulas" (Sparse Adapter) and [DTD] §7
+# (Sparse Overlay Bytes): 32-bit indices and 16-bit (f16) values, k*(4+2)
+# bytes.  [DTD] §11 (Deep Compatibility Checks): indices strictly monotonic,
+# no NaN or Inf in the f16 payload.  Reading: index = row*d_in + col of the
+# tensor the target names; the term's scale s multiplies every value.
+# --------------------------------------------------------------------------
+@dataclass(frozen=True)
+class SparseTerm:
+    idx: np.ndarray        # uint32 flat indices row * d_in + col, strictly increasing
+    val_bits: np.ndarray   # uint16 binary16 values
+    s: float
+
+
+def sparse_delta(term: SparseTerm, m: int, n: int) -> np.ndarray:
+    """Dense float64 [m][n] with delta[idx[k] / n][idx[k] mod n] = f16(val[k])."""
+    D = np.zeros(m * n, dtype=np.float64)
+    D[np.asarray(term.idx, np.int64)] = f16_to_float(term.val_bits)
+    return D.reshape(m, n)
+
+
+def _term_matrix(term, m: int, n: int) -> np.ndarray:
+    """s * dW of one overlay term: (A, B, s) low-rank or SparseTerm."""
+    if isinstance(term, SparseTerm):
+        return float(term.s) * sparse_delta(term, m, n)
+    A, B, s = term
+    return float(s) * (np.asarray(B, np.float64) @ np.asarray(A, np.float64))
+
+
 def effective_weight(deq: np.ndarray, adapters) -> np.ndarray:
-    """W' = deq + sum_k s_k * B_k A_k, adapters [(A [r][n], B [m][r], s)] in order."""
+    """W' = deq + sum_k s_k * dW_k in order; a term is (A [r][n], B [m][r], s)
+    (dW = B A) or a SparseTerm (dW = its scattered values)."""
     W = np.array(deq, dtype=np.float64, copy=True)
-    for A, B, s in adapters:
-        W += float(s) * (np.asarray(B, np.float64) @ np.asarray(A, np.float64))
+    m, n = W.shape
+    for term in adapters:
+        W += _term_matrix(term, m, n)
     return W
 
 
 def dual_path(deq: np.ndarray, adapters, x: np.ndarray) -> np.ndarray:
-    """y[t] = deq x[t] + sum_k s_k B_k (A_k x[t]); x [T][n] -> y [T][m], float64."""
+    """y[t] = deq x[t] + sum_k s_k dW_k x[t]; x [T][n] -> y [T][m], float64.
+
+    Low-rank terms go through the rank-r side product s B (A x); sparse terms
+    add s * sum over the stored entries of the row of val * x[col]."""
     x = np.asarray(x, dtype=np.float64)
-    y = x @ np.asarray(deq, np.float64).T
-    for A, B, s in adapters:
+    deq = np.asarray(deq, np.float64)
+    m, n = deq.shape
+    y = x @ deq.T
+    for term in adapters:
+        if isinstance(term, SparseTerm):
+            idx = np.asarray(term.idx, np.int64)
+            rows, cols = idx // n, idx % n
+            contrib = np.zeros((x.shape[0], m), dtype=np.float64)
+            # entry-by-entry accumulation (np.add.at: unbuffered, repeated rows add up)
+            np.add.at(contrib.T, rows, (f16_to_float(term.val_bits)[:, None] * x[:, cols].T))
+            y = y + float(term.s) * contrib
+            continue
+        A, B, s = term
         v = x @ np.asarray(A, np.float64).T            # [T][r]   shrink
         y = y + float(s) * (v @ np.asarray(B, np.float64).T)   # [T][m] expand
     return y
@@ -222,8 +277,14 @@ def materialize_bound(deq: np.ndarray, adapters, ulps: float = 4.0) -> np.ndarra
     ulps * 2^-24 * (rank+2) * (|deq| + sum_k |s_k| |B_k| |A_k|).
     """
     mag = np.abs(np.asarray(deq, np.float64)).copy()
+    m, n = mag.shape
     terms = 2
-    for A, B, s in adapters:
+    for term in adapters:
+        if isinstance(term, SparseTerm):
+            mag += np.abs(_term_matrix(term, m, n))
+            terms += 2
+            continue
+        A, B, s = term
         mag += abs(float(s)) * (np.abs(np.asarray(B, np.float64)) @ np.abs(np.asarray(A, np.float64)))
         terms += np.asarray(A).shape[0] + 1
     return ulps * 2.0 ** -24 * terms * mag

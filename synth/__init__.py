@@ -69,6 +69,10 @@ def adapter_seed(adapter: int, layer: int, proj: int) -> int:
     return 1_000_000 + 10_000 * adapter + 8 * layer + proj
 
 
+def sparse_seed(adapter: int, layer: int, proj: int) -> int:
+    return 5_000_000 + 10_000 * adapter + 8 * layer + proj
+
+
 def x_seed(T: int, d_in: int) -> int:
     return 2000 + 16 * T + (0 if d_in == 4096 else 1)
 
@@ -288,6 +292,68 @@ def build_adapter(base: Base, targets, ranks, factors, required_base=None) -> Ad
                    [(np.ascontiguousarray(A, np.float32), np.ascontiguousarray(B, np.float32))
                     for A, B in factors],
                    required_base if required_base is not None else b"\0" * 32)
+
+
+@dataclass
+class SparseAdapter:
+    targets: list              # tensor indices into the base
+    nnz: list
+    idx_off: list
+    val_off: list
+    payload: np.ndarray        # uint8
+    entries: list              # [(idx uint32 [nnz], val_bits uint16 [nnz])] per target
+    required_base: bytes = b"\0" * 32
+
+
+def build_sparse_adapter(targets, entries, required_base=None) -> SparseAdapter:
+    """Pack index-value pairs [(idx uint32, val_bits uint16)] per target into one
+    payload: per target a uint32 index plane and a binary16 value plane, each
+    starting on a 256-byte boundary."""
+    off = 0
+    io, vo = [], []
+    for idx, val in entries:
+        io.append(off)
+        off = _align(off + 4 * len(idx))
+        vo.append(off)
+        off = _align(off + 2 * len(val))
+    payload = np.zeros(max(off, ALIGN), dtype=np.uint8)
+    for (idx, val), a, b in zip(entries, io, vo):
+        payload[a:a + 4 * len(idx)] = np.ascontiguousarray(idx, np.uint32).view(np.uint8)
+        payload[b:b + 2 * len(val)] = np.ascontiguousarray(val, np.uint16).view(np.uint8)
+    return SparseAdapter(list(targets), [len(i) for i, _ in entries], io, vo, payload,
+                         [(np.ascontiguousarray(i, np.uint32), np.ascontiguousarray(v, np.uint16)) for i, v in entries],
+                         required_base if required_base is not None else b"\0" * 32)
+
+
+def dare_entries(rng: np.random.Generator, d_out: int, d_in: int, keep: float = 0.01, sigma: float = 1e-4):
+    """A DARE-style sparse task vector: a dense delta ~ N(0, sigma) of which each
+    element is kept with probability `keep` (a Bernoulli process, drawn as
+    geometric gaps between kept positions) and rescaled by 1/keep, stored as
+    strictly increasing flat indices row*d_in + col and binary16 values."""
+    total = d_out * d_in
+    pos = []
+    at = -1
+    while True:
+        gaps = rng.geometric(keep, size=max(16, int(total * keep * 1.1) + 16))
+        cand = at + np.cumsum(gaps)
+        pos.append(cand[cand < total])
+        if cand[-1] >= total:
+            break
+        at = int(cand[-1])
+    idx = np.concatenate(pos).astype(np.uint32)
+    val = (gaussian(rng, (idx.size,), sigma) / np.float32(keep)).astype(np.float16)
+    return idx, val.view(np.uint16)
+
+
+def block_sparse_adapter(base: Base, adapter: int, keep: float = 0.01, which=None) -> SparseAdapter:
+    """DARE-style sparse overlay (density `keep`) on every tensor of `base` (or `which`)."""
+    idx = list(range(len(base.tensors))) if which is None else list(which)
+    entries = []
+    for i in idx:
+        t = base.tensors[i]
+        rng = np.random.default_rng(sparse_seed(adapter, t.layer, t.proj))
+        entries.append(dare_entries(rng, t.d_out, t.d_in, keep))
+    return build_sparse_adapter(idx, entries)
 
 
 def content_digest(buf: np.ndarray) -> bytes:

@@ -222,6 +222,97 @@ def test_q4_k_quantizer_round_trip_through_oracle_dequant():
     assert np.array_equal(O.dequantize_q4_k(p2, h2), w)
 
 
+# ---------------------------------------------------------------- sparse overlays
+def _f16(vals):
+    return np.asarray(vals, np.float16).view(np.uint16)
+
+
+def test_sparse_single_entry_moves_exactly_one_weight():
+    rng = np.random.default_rng(41)
+    m, n = 5, 64
+    qs, d = S.quantize_q8_0(S.gaussian(rng, (m, n), 0.02))
+    deq = O.dequantize_q8_0(qs, d)
+    i, j, v, s = 3, 17, 0.375, 2.0
+    term = O.SparseTerm(np.array([i * n + j], np.uint32), _f16([v]), s)
+    Wp = O.effective_weight(deq, [term])
+    diff = Wp - deq
+    assert diff[i, j] == s * v and np.count_nonzero(diff) == 1
+    x = S.gaussian(rng, (2, n), 1.0).astype(np.float64)
+    y0, y1 = O.dual_path(deq, [], x), O.dual_path(deq, [term], x)
+    assert np.array_equal(np.delete(y1, i, axis=1), np.delete(y0, i, axis=1))
+    assert np.allclose(y1[:, i] - y0[:, i], s * v * x[:, j], rtol=1e-13, atol=0)
+
+
+def test_sparse_index_is_row_major_flat():
+    # idx = row * d_in + col: entries 0, 4, 7 of a 3x4 tensor are (0,0), (1,0), (1,3)
+    term = O.SparseTerm(np.array([0, 4, 7], np.uint32), _f16([1.0, 2.0, -3.0]), 1.0)
+    D = O.sparse_delta(term, 3, 4)
+    want = np.zeros((3, 4))
+    want[0, 0], want[1, 0], want[1, 3] = 1.0, 2.0, -3.0
+    assert np.array_equal(D, want)
+
+
+def test_sparse_outer_product_equals_rank_one_lora():
+    # a dense "sparse" overlay holding u w^T (f16-exact values) is the LoRA term B = u, A = w^T
+    m, n = 6, 32
+    u = np.array([0.5, -1.0, 0.25, 2.0, -0.125, 1.5])
+    w = (np.arange(n) % 7 - 3) * 0.0625
+    idx = np.arange(m * n, dtype=np.uint32)
+    term = O.SparseTerm(idx, _f16(np.outer(u, w).ravel()), 1.5)
+    lora = (w[None, :], u[:, None], 1.5)
+    deq = np.zeros((m, n))
+    assert np.array_equal(O.effective_weight(deq, [term]), O.effective_weight(deq, [lora]))
+    x = np.linspace(-1, 1, 2 * n).reshape(2, n)
+    assert np.allclose(O.dual_path(deq, [term], x), O.dual_path(deq, [lora], x), rtol=1e-13, atol=1e-15)
+
+
+def test_sparse_dual_path_exact_rationals():
+    rng = np.random.default_rng(43)
+    m, n, T = 4, 64, 2
+    qs, d = S.quantize_q8_0(S.gaussian(rng, (m, n), 0.02))
+    deq = O.dequantize_q8_0(qs, d)
+    idx = np.sort(rng.choice(m * n, size=20, replace=False)).astype(np.uint32)
+    val = _f16(rng.standard_normal(20) * 0.01)
+    s = 0.75
+    term = O.SparseTerm(idx, val, s)
+    x = S.gaussian(rng, (T, n), 1.0).astype(np.float64)
+    y = O.dual_path(deq, [term], x)
+    vv = val.view(np.float16).astype(np.float64)
+    for t in range(T):
+        for i in range(m):
+            acc = sum(Fraction(float(deq[i, j])) * Fraction(float(x[t, j])) for j in range(n))
+            for k in range(20):
+                if int(idx[k]) // n == i:
+                    acc += Fraction(s) * Fraction(float(vv[k])) * Fraction(float(x[t, int(idx[k]) % n]))
+            assert abs(Fraction(float(y[t, i])) - acc) <= Fraction(1, 10 ** 12) * (abs(acc) + 1)
+
+
+def test_sparse_and_lora_mixed_dual_equals_merged():
+    rng = np.random.default_rng(45)
+    m, n, T = 64, 256, 3
+    qs, d = S.quantize_q4_0(S.gaussian(rng, (m, n), 0.02))
+    deq = O.dequantize_q4_0(qs, d)
+    idx, val = S.dare_entries(rng, m, n, keep=0.05)
+    terms = [(S.gaussian(rng, (8, n), 0.01), S.gaussian(rng, (m, 8), 0.01), 2.0),
+             O.SparseTerm(idx, val, 0.5)]
+    x = S.gaussian(rng, (T, n), 1.0).astype(np.float64)
+    Wp = O.effective_weight(deq, terms)
+    dual = O.dual_path(deq, terms, x)
+    merged = O.merged_path(Wp, x)
+    assert (np.abs(dual - merged) <= 1e-12 * (np.abs(x) @ np.abs(Wp).T)).all()
+    # order of the stack does not change W' in exact arithmetic; here fp64 agrees closely
+    assert np.allclose(O.effective_weight(deq, terms[::-1]), Wp, rtol=0, atol=1e-15)
+
+
+def test_dare_entries_shape_and_order():
+    rng = np.random.default_rng(47)
+    idx, val = S.dare_entries(rng, 300, 512, keep=0.02)
+    assert idx.dtype == np.uint32 and val.dtype == np.uint16
+    assert np.all(np.diff(idx.astype(np.int64)) > 0) and int(idx[-1]) < 300 * 512
+    assert abs(idx.size / (300 * 512) - 0.02) < 0.003
+    assert np.isfinite(val.view(np.float16)).all()
+
+
 # ---------------------------------------------------------------- GEMV / LoRA
 def _tiny_problem(seed, m=6, n=64, T=2, ranks=(2, 3)):
     rng = np.random.default_rng(seed)
