@@ -513,6 +513,56 @@ def workload_q4k_decode(args):
 WORKLOADS["q4k-decode"] = workload_q4k_decode
 
 
+def workload_sparse_decode(args):
+    """The headline decode step (8B-shape q8_0 block, rank-16 LoRA s = 2.0 on all
+    7 projections, T = 1, x bf16) with a DARE-style sparse overlay stacked after
+    the LoRA on all 7 (1 % of the weights, f16 values, s = 1.0): four k_dualpath
+    launches, each followed by one k_sparse_apply over the same tensors."""
+    import torch
+    import quantized_base_lora_gb300 as q
+    from quantized_base_lora_gb300.runtime import Runtime
+    base = S.block_base(S.Q8_0)
+    ad = S.block_adapter(base, adapter=0, rank=RANK)
+    sp = S.block_sparse_adapter(base, adapter=0, keep=0.01)
+    tt = [(t.layer, t.proj, t.d_out, t.d_in, t.qs_off, t.d_off) for t in base.tensors]
+    dg, ad_dg, sp_dg = S.content_digest(base.buf), S.content_digest(ad.payload), S.content_digest(sp.payload)
+    rts = []
+    for _ in range(N_COPIES):
+        rt = Runtime(arena_bytes=128 << 20)
+        q.check(rt.load_base(base.quant, tt, base.buf, dg), rt.ctx)
+        st, ha = rt.stage(ad, ad_dg)
+        q.check(st, rt.ctx)
+        st, hs = rt.stage_sparse(sp, sp_dg)
+        q.check(st, rt.ctx)
+        q.check(rt.activate([ha, hs], [SCALE, 1.0])[0], rt.ctx)
+        rts.append(rt)
+    stream = torch.cuda.Stream()
+    sh = int(stream.cuda_stream)
+    xs = {d: torch.from_numpy(S.to_bf16_bits(S.activations(1, d)).view(np.int16)).cuda().view(torch.bfloat16)
+          for d in (4096, 14336)}
+    ybufs = [torch.empty((1, t.d_out), dtype=torch.float32, device="cuda") for t in base.tensors]
+    step = _block_step(base, rts, {d: v.data_ptr() for d, v in xs.items()}, [y.data_ptr() for y in ybufs], 1, sh)
+    ms = timed_steps(step, args.steps, args.warmup, stream)
+    _check_all(rts, sh)
+    nnz = sum(sp.nnz)
+    sparse_bytes = nnz * 6 + sum((t.d_out + 1) * 4 for t in base.tensors)
+    eff = effective_bytes(base, ad) + sparse_bytes
+    # the sparse pass also reads and rewrites y
+    alg = algorithmic_bytes(base, ad) + sparse_bytes + sum(8 * t.d_out for t in base.tensors)
+    emit({"workload": "sparse-decode",
+          "metric": "decode effective weight GB/s & tok/s (8B shape, q8_0 + r16 LoRA + 1% sparse overlay)",
+          "unit": "GB/s", "value": eff / (ms / 1e3) / 1e9, "ms_per_step": ms, "tok_s": 1e3 / ms,
+          "steps": args.steps, "nnz": nnz,
+          "roofline": hbm_roofline(alg, ms, "k_dualpath (4 launches) + k_sparse_apply (4 launches) per step"),
+          "config": {"base": "8B-shape block q8_0", "adapters": "r16 s=2.0 then DARE 1% sparse s=1.0 on all 7",
+                     "x": "bf16", "l2": f"{N_COPIES} base copies rotated"}})
+    for rt in rts:
+        rt.close()
+
+
+WORKLOADS["sparse-decode"] = workload_sparse_decode
+
+
 def workload_segmented(args):
     import torch
     import quantized_base_lora_gb300 as q

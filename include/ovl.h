@@ -205,6 +205,40 @@ ovl_status ovl_load_base(ovl_ctx* ctx, const ovl_base_desc* desc, const void* ba
 ovl_status ovl_stage_adapter(ovl_ctx* ctx, const ovl_adapter_desc* desc, const void* payload_host,
                              size_t nbytes, const uint8_t digest[32], ovl_adapter_h* out);
 
+/* Stage a sparse overlay: only the non-zero elements of each target's weight
+ * update, as index-value pairs added at their positions at use time, the base
+ * unchanged ([OVR] §"Runtime Strategy Comparison Matrix", Sparse Overlay;
+ * [OVR] §"Memory, Byte, and Latency Formulas", Sparse Adapter: 32-bit indices
+ * and 16-bit values, k*(4+2) bytes; [DTD] §7 Sparse Overlay Bytes; [DTD] §11
+ * AdapterManifestV0 adapter type Sparse (DARE)).
+ * Payload (host, nbytes bytes, read during the call only): per target a uint32
+ * index plane [nnz] at idx_off and an IEEE binary16 value plane [nnz] at
+ * val_off (offsets multiples of 16).  Pair k adds scale * val[k] to the weight at
+ * row idx[k] / d_in, column idx[k] % d_in of the target tensor.
+ * Phases and errors as ovl_stage_adapter.  Validation: targets exist
+ * (OVL_E_NOTARGET), no duplicate target (OVL_E_DUPLICATE), d_out * d_in < 2^32,
+ * nnz <= d_out * d_in, planes aligned and inside the payload, indices strictly
+ * increasing and below d_out * d_in ([DTD] §11 Deep Compatibility Checks)
+ * (OVL_E_SHAPE), required base digest and payload digest (OVL_E_HASH).
+ * Allocation: the payload plus the row offsets [d_out + 1] per target that the
+ * library builds (OVL_E_OOM).  Checksum: device-copy digest (OVL_E_HASH), then
+ * every value finite (OVL_E_NONFINITE, [DTD] §11).  Any failure frees the
+ * allocation and changes nothing.  The handle is activated with ovl_activate
+ * like a low-rank adapter, in STACK compositions only; ovl_get_entry reports
+ * total_rank 0 for it.  adapter_key = SHA256("OVLS" | payload_digest |
+ * u32 n_targets | per target u32 tensor, nnz | u64 idx_off, val_off). */
+typedef struct {
+  uint32_t n_targets;
+  const uint32_t* target_tensor;    /* host arrays of n_targets, copied */
+  const uint32_t* nnz;              /* index-value pairs per target (0 allowed) */
+  const uint64_t* idx_off;
+  const uint64_t* val_off;
+  uint8_t required_base_digest[32]; /* all-zero = no requirement */
+} ovl_sparse_desc;
+
+ovl_status ovl_stage_sparse(ovl_ctx* ctx, const ovl_sparse_desc* desc, const void* payload_host, size_t nbytes,
+                            const uint8_t digest[32], ovl_adapter_h* out);
+
 /* Release a staged adapter's arena block.  OVL_E_STATE if it is part of the
  * active or the rollback composition; OVL_E_BUSY (REJECT policy) if forward work
  * that read it is still in flight; OVL_E_ARG for an unknown handle. */
@@ -218,7 +252,8 @@ ovl_status ovl_unstage_adapter(ovl_ctx* ctx, ovl_adapter_h h);
  * composition (deactivation, [OVR] same section, Deactivation).  Re-activating
  * the active composition is a no-op that returns its id ([OVR] Idempotency).
  * The replaced composition becomes the rollback target.  Errors: OVL_E_ARG
- * (unknown handle, non-finite scale, bad mode, n over the limit), OVL_E_DUPLICATE,
+ * (unknown handle, non-finite scale, bad mode, n over the limit, a sparse
+ * overlay in a TABLE composition), OVL_E_DUPLICATE,
  * OVL_E_SHAPE (total rank on a tensor over OVL_MAX_TOTAL_RANK), OVL_E_BUSY.
  * composition_id_out (host, 32 bytes, may be NULL) receives the active id. */
 ovl_status ovl_activate(ovl_ctx* ctx, const ovl_adapter_h* h, const float* scale, uint32_t n,

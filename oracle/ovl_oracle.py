@@ -347,6 +347,18 @@ def adapter_key(digest: bytes, targets) -> bytes:
     return h.digest()
 
 
+def sparse_adapter_key(digest: bytes, targets) -> bytes:
+    """Identity of a sparse overlay; targets: iterable of (tensor_index, nnz, idx_off, val_off)."""
+    targets = list(targets)
+    h = hashlib.sha256()
+    h.update(b"OVLS")
+    h.update(digest)
+    h.update(struct.pack("<I", len(targets)))
+    for (ti, nnz, io, vo) in targets:
+        h.update(struct.pack("<IIQQ", ti, nnz, io, vo))
+    return h.digest()
+
+
 def f32_bits(s: float) -> int:
     return struct.unpack("<I", struct.pack("<f", float(s)))[0]
 

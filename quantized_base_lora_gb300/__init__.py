@@ -58,6 +58,12 @@ class ovl_adapter_desc(C.Structure):
                 ("b_off", C.POINTER(C.c_uint64)), ("required_base_digest", C.c_uint8 * 32)]
 
 
+class ovl_sparse_desc(C.Structure):
+    _fields_ = [("n_targets", C.c_uint32), ("target_tensor", C.POINTER(C.c_uint32)),
+                ("nnz", C.POINTER(C.c_uint32)), ("idx_off", C.POINTER(C.c_uint64)),
+                ("val_off", C.POINTER(C.c_uint64)), ("required_base_digest", C.c_uint8 * 32)]
+
+
 class ovl_state(C.Structure):
     _fields_ = [("composition_id", C.c_uint8 * 32), ("base_digest", C.c_uint8 * 32),
                 ("quant", C.c_uint32), ("mode", C.c_uint32), ("n_entries", C.c_uint32),
@@ -81,6 +87,7 @@ def _load():
         "ovl_destroy": ([P], I32),
         "ovl_load_base": ([P, C.POINTER(ovl_base_desc), P, SZ, B32, P], I32),
         "ovl_stage_adapter": ([P, C.POINTER(ovl_adapter_desc), P, SZ, B32, C.POINTER(U64)], I32),
+        "ovl_stage_sparse": ([P, C.POINTER(ovl_sparse_desc), P, SZ, B32, C.POINTER(U64)], I32),
         "ovl_unstage_adapter": ([P, U64], I32),
         "ovl_activate": ([P, C.POINTER(U64), C.POINTER(C.c_float), U32, U32, B32], I32),
         "ovl_rollback": ([P, B32], I32),
@@ -109,7 +116,7 @@ def _load():
 
 
 lib = _load()
-EXPORTED = ("ovl_create", "ovl_destroy", "ovl_load_base", "ovl_stage_adapter", "ovl_unstage_adapter",
+EXPORTED = ("ovl_create", "ovl_destroy", "ovl_load_base", "ovl_stage_adapter", "ovl_stage_sparse", "ovl_unstage_adapter",
             "ovl_activate", "ovl_rollback", "ovl_linear_forward", "ovl_linear_forward_multi", "ovl_materialize_layer",
             "ovl_segmented_forward", "ovl_base_digest", "ovl_get_state", "ovl_get_entry",
             "ovl_check_device", "ovl_debug_inject", "ovl_last_error", "ovl_sha256",
@@ -204,6 +211,17 @@ def ovl_stage_adapter(ctx, targets, ranks, a_off, b_off, payload, digest: bytes,
     h = C.c_uint64(0)
     st = lib.ovl_stage_adapter(ctx, C.byref(desc), C.c_void_p(payload.ctypes.data), int(payload.nbytes),
                                _b32(digest), C.byref(h))
+    return st, int(h.value)
+
+
+def ovl_stage_sparse(ctx, targets, nnz, idx_off, val_off, payload, digest: bytes, required_base: bytes | None = None):
+    """payload: C-contiguous numpy uint8 array (host).  Returns (status, handle)."""
+    n = len(targets)
+    desc = ovl_sparse_desc(n, _u32s(targets), _u32s(nnz), _u64s(idx_off), _u64s(val_off),
+                           _b32(required_base or b"\0" * 32))
+    h = C.c_uint64(0)
+    st = lib.ovl_stage_sparse(ctx, C.byref(desc), C.c_void_p(payload.ctypes.data), int(payload.nbytes),
+                              _b32(digest), C.byref(h))
     return st, int(h.value)
 
 

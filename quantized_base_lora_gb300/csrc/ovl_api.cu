@@ -103,8 +103,19 @@ struct Target {
   uint64_t a_off, b_off;
 };
 
+// A sparse overlay target: index and value planes inside the payload, and the
+// row offsets [d_out + 1] the library builds at staging (offset from the
+// adapter's arena allocation).
+struct SparseTarget {
+  uint32_t tensor, nnz;
+  uint64_t idx_off, val_off;
+  uint64_t rp_off;
+};
+
 struct Adapter {
   ovl_adapter_h h = 0;
+  bool sparse = false;               // index-value overlay instead of low-rank factors
+  std::vector<SparseTarget> sp;      // sparse targets (sparse adapters only)
   std::vector<Target> targets;
   size_t off = 0, bytes = 0;
   uint8_t digest[32];
@@ -218,6 +229,16 @@ void compute_base_key(ovl_ctx* c) {
 
 void compute_adapter_key(Adapter& a) {
   Sha256Stream h;
+  if (a.sparse) {
+    h.update("OVLS", 4);
+    h.update(a.digest, 32);
+    h.u32(static_cast<uint32_t>(a.sp.size()));
+    for (const auto& t : a.sp) {
+      h.u32(t.tensor); h.u32(t.nnz); h.u64(t.idx_off); h.u64(t.val_off);
+    }
+    h.final(a.key);
+    return;
+  }
   h.update("OVLA", 4);
   h.update(a.digest, 32);
   h.u32(static_cast<uint32_t>(a.targets.size()));
@@ -506,6 +527,96 @@ ovl_status ovl_stage_adapter(ovl_ctx* ctx, const ovl_adapter_desc* desc, const v
   return ok(ctx);
 }
 
+ovl_status ovl_stage_sparse(ovl_ctx* ctx, const ovl_sparse_desc* desc, const void* payload_host, size_t nbytes,
+                            const uint8_t digest[32], ovl_adapter_h* out) {
+  if (!ctx) return OVL_E_ARG;
+  std::lock_guard<std::mutex> lk(ctx->mu);
+  if (out) *out = 0;
+  // ---- VALIDATION: shapes, strictly increasing in-range indices ([DTD] §11
+  // Deep Compatibility Checks), base requirement, digest of the host bytes
+  if (ovl_status s = injected(ctx, OVL_PHASE_VALIDATION)) return s;
+  if (!ctx->base_loaded) return fail(ctx, OVL_E_STATE, "no base loaded");
+  if (!desc || !payload_host || !digest || !out) return fail(ctx, OVL_E_ARG, "null argument");
+  if (desc->n_targets == 0 || !desc->target_tensor || !desc->nnz || !desc->idx_off || !desc->val_off)
+    return fail(ctx, OVL_E_ARG, "overlay has no targets");
+  const uint8_t* P = static_cast<const uint8_t*>(payload_host);
+  Adapter ad;
+  ad.sparse = true;
+  bool nonfinite = false;
+  size_t rp_total = 0;
+  std::vector<std::vector<uint32_t>> rps;
+  for (uint32_t i = 0; i < desc->n_targets; ++i) {
+    SparseTarget t{desc->target_tensor[i], desc->nnz[i], desc->idx_off[i], desc->val_off[i], 0};
+    const std::string who = "target " + std::to_string(i) + ": ";
+    if (t.tensor >= ctx->tensors.size()) return fail(ctx, OVL_E_NOTARGET, who + "no such base tensor");
+    for (const auto& o : ad.sp)
+      if (o.tensor == t.tensor) return fail(ctx, OVL_E_DUPLICATE, who + "tensor targeted twice");
+    const ovl_tensor_desc& td = ctx->tensors[t.tensor];
+    const uint64_t cells = uint64_t(td.d_out) * td.d_in;
+    if (cells > 0xFFFFFFFFull) return fail(ctx, OVL_E_SHAPE, who + "tensor too large for 32-bit indices");
+    if (t.nnz > cells) return fail(ctx, OVL_E_SHAPE, who + "more pairs than weights");
+    if (t.idx_off % 16 || t.val_off % 16) return fail(ctx, OVL_E_SHAPE, who + "plane offsets must be multiples of 16");
+    const uint64_t ib = uint64_t(t.nnz) * 4, vb = uint64_t(t.nnz) * 2;
+    if (t.idx_off > nbytes || ib > nbytes - t.idx_off || t.val_off > nbytes || vb > nbytes - t.val_off)
+      return fail(ctx, OVL_E_SHAPE, who + "pairs exceed the payload");
+    std::vector<uint32_t> rp(size_t(td.d_out) + 1, 0);
+    uint32_t prev = 0;
+    for (uint32_t k = 0; k < t.nnz; ++k) {
+      uint32_t idx;
+      uint16_t v;
+      std::memcpy(&idx, P + t.idx_off + 4ull * k, 4);
+      std::memcpy(&v, P + t.val_off + 2ull * k, 2);
+      if (k && idx <= prev) return fail(ctx, OVL_E_SHAPE, who + "indices must be strictly increasing");
+      if (idx >= cells) return fail(ctx, OVL_E_SHAPE, who + "index beyond the tensor");
+      if ((v & 0x7C00u) == 0x7C00u) nonfinite = true;   // binary16 Inf or NaN
+      ++rp[idx / td.d_in + 1];
+      prev = idx;
+    }
+    for (size_t r = 1; r < rp.size(); ++r) rp[r] += rp[r - 1];
+    t.rp_off = rp_total;   // relative to the row-offset area for now
+    rp_total += (rp.size() * 4 + kArenaAlign - 1) / kArenaAlign * kArenaAlign;
+    ad.sp.push_back(t);
+    rps.push_back(std::move(rp));
+  }
+  static const uint8_t zero[32] = {0};
+  if (std::memcmp(desc->required_base_digest, zero, 32) != 0 &&
+      std::memcmp(desc->required_base_digest, ctx->base_digest, 32) != 0)
+    return fail(ctx, OVL_E_HASH, "overlay requires a different base");
+  host_content_digest(payload_host, nbytes, ad.digest);
+  if (std::memcmp(ad.digest, digest, 32) != 0) return fail(ctx, OVL_E_HASH, "overlay digest mismatch");
+  // ---- ALLOCATION: payload, then the row offsets of every target
+  if (ovl_status s = injected(ctx, OVL_PHASE_ALLOCATION)) return s;
+  const size_t pay = (nbytes + kArenaAlign - 1) / kArenaAlign * kArenaAlign;
+  if (!ctx->alloc.alloc(pay + rp_total, &ad.off)) return fail(ctx, OVL_E_OOM, "arena budget exceeded");
+  ad.bytes = nbytes;
+  for (auto& t : ad.sp) t.rp_off += pay;
+  auto release = [&](ovl_status code) {
+    ctx->alloc.release(ad.off);
+    return code;
+  };
+  // ---- STAGING
+  DeviceGuard g(ctx->device);
+  if (ovl_status s = injected(ctx, OVL_PHASE_STAGING)) return release(s);
+  cudaError_t e = cudaMemcpyAsync(ctx->arena + ad.off, payload_host, nbytes, cudaMemcpyHostToDevice, ctx->stream);
+  for (size_t i = 0; i < ad.sp.size() && e == cudaSuccess; ++i)
+    e = cudaMemcpyAsync(ctx->arena + ad.off + ad.sp[i].rp_off, rps[i].data(), rps[i].size() * 4,
+                        cudaMemcpyHostToDevice, ctx->stream);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(ctx->stream);
+  if (e != cudaSuccess) return release(cuda_fail(ctx, e, "staging copy"));
+  // ---- CHECKSUM: digest of the device copy; finiteness of the f16 values
+  // ([DTD] §11: no NaN or Inf in the f16 payloads)
+  if (ovl_status s = injected(ctx, OVL_PHASE_CHECKSUM)) return release(s);
+  uint8_t dev_digest[32];
+  if (ovl_status s = device_digest(ctx, ctx->arena + ad.off, nbytes, ctx->stream, dev_digest)) return release(s);
+  if (std::memcmp(dev_digest, ad.digest, 32) != 0) return release(fail(ctx, OVL_E_HASH, "staged copy corrupted"));
+  if (nonfinite) return release(fail(ctx, OVL_E_NONFINITE, "overlay values hold NaN or Inf"));
+  compute_adapter_key(ad);
+  ad.h = ctx->next_h++;
+  *out = ad.h;
+  ctx->staged.emplace(ad.h, ad);
+  return ok(ctx);
+}
+
 ovl_status ovl_unstage_adapter(ovl_ctx* ctx, ovl_adapter_h h) {
   if (!ctx) return OVL_E_ARG;
   std::lock_guard<std::mutex> lk(ctx->mu);
@@ -547,6 +658,8 @@ ovl_status ovl_activate(ovl_ctx* ctx, const ovl_adapter_h* h, const float* scale
     for (uint32_t j = 0; j < i; ++j)
       if (h[j] == h[i]) return fail(ctx, OVL_E_DUPLICATE, "adapter listed twice");
     if (!finite_f32(scale[i])) return fail(ctx, OVL_E_ARG, "scale must be finite");
+    if (mode == OVL_MODE_TABLE && ctx->staged.at(h[i]).sparse)
+      return fail(ctx, OVL_E_ARG, "sparse overlays are applied in STACK compositions only");
     comp->entries.push_back({h[i], scale[i]});
   }
   if (comp->mode == OVL_MODE_STACK) {
@@ -611,6 +724,57 @@ uint32_t stack_terms(ovl_ctx* c, const Composition& comp, uint32_t tensor, LoraR
     used->push_back(&a);
   }
   return nl;
+}
+
+// Sparse overlay terms of `comp` that touch `tensor` (STACK), in composition order.
+uint32_t sparse_terms(ovl_ctx* c, const Composition& comp, uint32_t tensor, SparseRef* out,
+                      std::vector<Adapter*>* used) {
+  uint32_t n = 0;
+  for (const auto& e : comp.entries) {
+    Adapter& a = c->staged.at(e.h);
+    if (!a.sparse) continue;
+    for (const auto& t : a.sp) {
+      if (t.tensor != tensor) continue;
+      out[n].idx = reinterpret_cast<const uint32_t*>(c->arena + a.off + t.idx_off);
+      out[n].val = reinterpret_cast<const uint16_t*>(c->arena + a.off + t.val_off);
+      out[n].rp = reinterpret_cast<const uint32_t*>(c->arena + a.off + t.rp_off);
+      out[n].nnz = t.nnz;
+      out[n].s = e.s;
+      ++n;
+      used->push_back(&a);
+    }
+  }
+  return n;
+}
+
+// Adds the sparse terms of tensors[0..n) (which share x) to the outputs the
+// dense dual path wrote, in one launch; nothing is launched without any.
+cudaError_t apply_sparse(ovl_ctx* c, const uint32_t* tensors, uint32_t n, const void* x, uint32_t xdt, uint32_t T,
+                         float* const* ys, std::vector<Adapter*>* used, cudaStream_t st) {
+  SparseApply sa{};
+  for (uint32_t i = 0; i < n; ++i) {
+    const uint32_t k0 = sa.nt;
+    sa.nt += sparse_terms(c, *c->active, tensors[i], sa.t + sa.nt, used);
+    if (sa.nt == k0) continue;
+    const ovl_tensor_desc& td = c->tensors[tensors[i]];
+    sa.seg[sa.nseg++] = SparseSeg{ys[i], td.d_out, sa.mtot, k0, sa.nt};
+    sa.mtot += td.d_out;
+  }
+  if (sa.nt == 0) return cudaSuccess;
+  sa.x = x;
+  sa.n = c->tensors[tensors[0]].d_in;
+  sa.T = T;
+  sa.xdt = xdt;
+  return launch_sparse_apply(sa, st);
+}
+
+// Adds the sparse terms of `tensor` into a materialized fp32 scratch, in order.
+cudaError_t scatter_sparse(ovl_ctx* c, uint32_t tensor, float* S, std::vector<Adapter*>* used, cudaStream_t st) {
+  SparseRef sp[OVL_MAX_STACK];
+  const uint32_t n = sparse_terms(c, *c->active, tensor, sp, used);
+  cudaError_t e = cudaSuccess;
+  for (uint32_t k = 0; k < n && e == cudaSuccess; ++k) e = launch_sparse_scatter(S, sp[k], st);
+  return e;
 }
 
 // Launches of four or more tokens run on the tensor cores (K4) when the shape
@@ -698,6 +862,7 @@ ovl_status ovl_materialize_layer(ovl_ctx* ctx, uint32_t tensor, float* scratch, 
   m.nl = stack_terms(ctx, *ctx->active, tensor, m.lora, &rtot, &used);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   cudaError_t e = launch_materialize(m, st);
+  if (e == cudaSuccess) e = scatter_sparse(ctx, tensor, scratch, &used, st);
   if (e != cudaSuccess) return cuda_fail(ctx, e, "materialize launch");
   if (ovl_status s = record_use(ctx, used, st)) return s;
   return ok(ctx);
@@ -724,6 +889,7 @@ ovl_status ovl_linear_forward(ovl_ctx* ctx, uint32_t tensor, const void* x, uint
   const uint32_t nl = stack_terms(ctx, *ctx->active, tensor, terms, &rtot, &used);
   if (path == OVL_PATH_DUAL && use_tc(ctx, T, td, rtot, x)) {
     cudaError_t e = launch_tc(ctx, td, x, x_dtype, T, y, terms, nl, rtot, nullptr, st);
+    if (e == cudaSuccess) e = apply_sparse(ctx, &tensor, 1, x, x_dtype, T, &y, &used, st);
     if (e != cudaSuccess) return cuda_fail(ctx, e, "tensor-core launch");
   } else if (path == OVL_PATH_DUAL) {
     DualArgs a{};
@@ -743,6 +909,7 @@ ovl_status ovl_linear_forward(ovl_ctx* ctx, uint32_t tensor, const void* x, uint
     for (uint32_t i = 0; i < nl; ++i) a.lora[i] = terms[i];
     a.ws = ctx->ws;
     cudaError_t e = launch_dualpath(a, st);
+    if (e == cudaSuccess) e = apply_sparse(ctx, &tensor, 1, x, x_dtype, T, &y, &used, st);
     if (e != cudaSuccess) return cuda_fail(ctx, e, "dual-path launch");
   } else {
     const size_t need = size_t(td.d_out) * td.d_in * 4;
@@ -759,6 +926,7 @@ ovl_status ovl_linear_forward(ovl_ctx* ctx, uint32_t tensor, const void* x, uint
     m.nl = nl;
     for (uint32_t i = 0; i < nl; ++i) m.lora[i] = terms[i];
     cudaError_t e = launch_materialize(m, st);
+    if (e == cudaSuccess) e = scatter_sparse(ctx, tensor, scratch, &used, st);
     if (e != cudaSuccess) return cuda_fail(ctx, e, "materialize launch");
     float* xs = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(scratch) + (need + 127) / 128 * 128);
     e = launch_jit_gemm(scratch, x, x_dtype, T, td.d_out, td.d_in, y, xs, ctx->ws, st);
@@ -813,6 +981,7 @@ ovl_status ovl_linear_forward_multi(ovl_ctx* ctx, uint32_t n, const uint32_t* te
       }
       tc_common(ctx, ctx->tensors[tensors[0]].d_in, x, x_dtype, T, &L);
       cudaError_t e = launch_fused_gemm(L, st);
+      if (e == cudaSuccess) e = apply_sparse(ctx, tensors, n, x, x_dtype, T, ys, &used, st);
       if (e != cudaSuccess) return cuda_fail(ctx, e, "tensor-core launch");
       if (ovl_status s = record_use(ctx, used, st)) return s;
       return ok(ctx);
@@ -848,6 +1017,7 @@ ovl_status ovl_linear_forward_multi(ovl_ctx* ctx, uint32_t n, const uint32_t* te
   a.ws = ctx->ws;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   cudaError_t e = launch_dualpath(a, st);
+  if (e == cudaSuccess) e = apply_sparse(ctx, tensors, n, x, x_dtype, T, ys, &used, st);
   if (e != cudaSuccess) return cuda_fail(ctx, e, "multi-tensor launch");
   if (ovl_status s = record_use(ctx, used, st)) return s;
   return ok(ctx);

@@ -131,7 +131,41 @@ struct MatArgs {
   float* S;
 };
 
+// One sparse overlay term on one tensor: nnz index-value pairs (flat index
+// row * n + col, strictly increasing; binary16 values) and the row offsets the
+// library builds at staging (rp[row] .. rp[row + 1] are the row's pairs).
+struct SparseRef {
+  const uint32_t* idx;
+  const uint16_t* val;
+  const uint32_t* rp;     // [m + 1]
+  uint32_t nnz;
+  float s;
+};
+
+// One tensor of a sparse launch: rows [row0, row0 + m) of the launch, output
+// y [T][m], terms t[k0, k1).
+struct SparseSeg {
+  float* y;
+  uint32_t m, row0;
+  uint32_t k0, k1;
+};
+
+// y[t][row] += sum_k s_k * sum_{pairs of row in term k} val * x[t][col], terms in
+// order, after the dense dual path has written y.  Up to kMaxMulti tensors that
+// share x (and d_in) in one launch.
+struct SparseApply {
+  const void* x;          // [T][n], fp32 or bf16
+  uint32_t n, T, xdt;
+  uint32_t nseg, mtot;
+  SparseSeg seg[kMaxMulti];
+  uint32_t nt;
+  SparseRef t[kMaxMulti * OVL_MAX_STACK];
+};
+
 cudaError_t launch_dualpath(const DualArgs& a, cudaStream_t st);
+cudaError_t launch_sparse_apply(const SparseApply& a, cudaStream_t st);
+// S[idx[k]] += s * val[k] for every pair of one term (fp32 scratch [m][n]).
+cudaError_t launch_sparse_scatter(float* S, const SparseRef& t, cudaStream_t st);
 cudaError_t launch_materialize(const MatArgs& a, cudaStream_t st);
 // Y[T][m] = X[T][n] * S[m][n]^T with TF32 tensor-core operands, fp32 accumulate.
 cudaError_t launch_jit_gemm(const float* S, const void* x, uint32_t xdt, uint32_t T, uint32_t m,

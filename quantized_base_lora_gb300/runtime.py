@@ -8,7 +8,8 @@ import torch
 
 from . import (OVL_BF16, OVL_F32, OVL_MODE_STACK, OVL_PATH_DUAL, OVL_SWITCH_REJECT, OvlError, check,
                ovl_activate, ovl_base_digest, ovl_check_device, ovl_create, ovl_destroy, ovl_get_state,
-               ovl_linear_forward, ovl_load_base, ovl_rollback, ovl_stage_adapter, ovl_unstage_adapter)
+               ovl_linear_forward, ovl_load_base, ovl_rollback, ovl_stage_adapter, ovl_stage_sparse,
+               ovl_unstage_adapter)
 
 
 def stream_handle(stream=None) -> int:
@@ -52,6 +53,10 @@ class Runtime:
     def stage(self, ad, digest: bytes, required_base: bytes | None = None):
         return ovl_stage_adapter(self.ctx, ad.targets, ad.ranks, ad.a_off, ad.b_off, ad.payload, digest,
                                  required_base)
+
+    def stage_sparse(self, sp, digest: bytes, required_base: bytes | None = None):
+        return ovl_stage_sparse(self.ctx, sp.targets, sp.nnz, sp.idx_off, sp.val_off, sp.payload, digest,
+                                required_base)
 
     def unstage(self, h):
         return ovl_unstage_adapter(self.ctx, h)

@@ -304,6 +304,19 @@ def test_sparse_and_lora_mixed_dual_equals_merged():
     assert np.allclose(O.effective_weight(deq, terms[::-1]), Wp, rtol=0, atol=1e-15)
 
 
+def test_sparse_adapter_key_brute_recomputation():
+    # the byte string of the identity, assembled field by field with hashlib
+    dg = bytes(range(32))
+    want = hashlib.sha256(b"OVLS" + dg + (2).to_bytes(4, "little")
+                          + (3).to_bytes(4, "little") + (100).to_bytes(4, "little")
+                          + (0).to_bytes(8, "little") + (512).to_bytes(8, "little")
+                          + (6).to_bytes(4, "little") + (7).to_bytes(4, "little")
+                          + (768).to_bytes(8, "little") + (1024).to_bytes(8, "little")).digest()
+    assert O.sparse_adapter_key(dg, [(3, 100, 0, 512), (6, 7, 768, 1024)]) == want
+    # a sparse overlay and a low-rank adapter with the same numbers are different identities
+    assert O.sparse_adapter_key(dg, [(3, 100, 0, 512)]) != O.adapter_key(dg, [(3, 100, 0, 512)])
+
+
 def test_dare_entries_shape_and_order():
     rng = np.random.default_rng(47)
     idx, val = S.dare_entries(rng, 300, 512, keep=0.02)
