@@ -200,7 +200,11 @@ def cpu_baseline(base, ad, xs, budget_s=12.0):
 def run_reference(args, world, rank):
     if rank != 0:
         return
-    base = S.block_base(S.Q8_0)
+    # Step i runs projection i mod 7; a run of fewer than 7 steps builds only the
+    # projections it uses (every projection has its own seeds, so they are the
+    # same bytes as in the whole block).
+    n_proj = min(7, max(1, args.steps, args.warmup))
+    base = S.block_base(S.Q8_0, projs=S.PROJ[:n_proj])
     ad = S.block_adapter(base, adapter=0, rank=RANK)
     xs = {d: S.bf16_bits_to_f32(S.to_bf16_bits(S.activations(1, d))).astype(np.float64) for d in (4096, 14336)}
     for i in range(args.warmup):
