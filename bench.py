@@ -499,19 +499,34 @@ def workload_q4k_decode(args):
     sh = int(stream.cuda_stream)
     planes = sum(S.qs_bytes(base.quant, t.d_out, t.d_in) + S.d_bytes(t.d_out, t.d_in) for t in base.tensors)
     lora = sum(RANK * (t.d_in + t.d_out) * 4 for t in base.tensors)
-    T = 1
-    xs = {d: torch.from_numpy(S.to_bf16_bits(S.activations(T, d)).view(np.int16)).cuda().view(torch.bfloat16)
-          for d in (4096, 14336)}
-    ybufs = [torch.empty((T, t.d_out), dtype=torch.float32, device="cuda") for t in base.tensors]
-    step = _block_step(base, rts, {d: v.data_ptr() for d, v in xs.items()}, [y.data_ptr() for y in ybufs], T, sh)
-    ms = timed_steps(step, args.steps, args.warmup, stream)
-    _check_all(rts, sh)
-    alg = planes + lora + sum(T * (t.d_in * 2 + t.d_out * 4) for t in base.tensors)
+    per_T = {}
+    for T in (1, 64):
+        xs = {d: torch.from_numpy(S.to_bf16_bits(S.activations(T, d)).view(np.int16)).cuda().view(torch.bfloat16)
+              for d in (4096, 14336)}
+        ybufs = [torch.empty((T, t.d_out), dtype=torch.float32, device="cuda") for t in base.tensors]
+        step = _block_step(base, rts, {d: v.data_ptr() for d, v in xs.items()}, [y.data_ptr() for y in ybufs], T,
+                           sh)
+        ms = timed_steps(step, args.steps, args.warmup, stream)
+        _check_all(rts, sh)
+        alg = planes + lora + sum(T * (t.d_in * 2 + t.d_out * 4) for t in base.tensors)
+        if T == 1:
+            roof = hbm_roofline(alg, ms, "k_dualpath (4 launches per step)")
+        else:
+            flops = sum(2 * T * t.d_out * t.d_in for t in base.tensors)
+            tf = flops / (ms / 1e3) / 1e12
+            roof = {"bound": "tensor", "achieved": tf, "peak": tf32_peak()[0], "unit": "TFLOP/s",
+                    "frac": tf / tf32_peak()[0], "traffic": None,
+                    "kernel": "k_widen_shrink + k_fused_gemm per group of tensors that share x",
+                    "note": f"peak = {tf32_peak()[1]}"}
+        per_T[T] = {"ms_per_step": ms, "effective_gbs": (planes + lora) / (ms / 1e3) / 1e9, "tok_s": T * 1e3 / ms,
+                    "roofline": roof}
+    one = per_T[1]
     emit({"workload": "q4k-decode", "metric": "decode effective weight GB/s & tok/s (8B shape, q4_K + r16 LoRA)",
-          "unit": "GB/s", "value": (planes + lora) / (ms / 1e3) / 1e9, "ms_per_step": ms, "tok_s": 1e3 / ms,
-          "steps": args.steps, "roofline": hbm_roofline(alg, ms, "k_dualpath (4 launches per step)"),
+          "unit": "GB/s", "value": one["effective_gbs"], "ms_per_step": one["ms_per_step"], "tok_s": one["tok_s"],
+          "steps": args.steps, "roofline": one["roofline"], "per_T": per_T,
           "config": {"base": f"8B-shape block q4_K ({planes / 1e6:.1f} MB)", "adapter": "r16 s=2.0 on all 7",
-                     "x": "bf16", "l2": f"{N_COPIES} base copies rotated"}})
+                     "x": "bf16", "tokens": "1 (K1) and 64 (tensor-core route)",
+                     "l2": f"{N_COPIES} base copies rotated"}})
 
 
 WORKLOADS["q4k-decode"] = workload_q4k_decode

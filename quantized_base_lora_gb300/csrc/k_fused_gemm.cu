@@ -165,6 +165,33 @@ __device__ __forceinline__ void dequant_kblock(const uint8_t* codes, uint32_t qu
   }
 }
 
+// q4_K: sub-block kbg of the group's super-block, weight d sc code - dmin m,
+// rounded once: the code is formed exactly (2^15 + code, minus 2^15) and one
+// fused multiply-add applies the scale and the minimum.  `hdr` is the row's
+// 16-byte super-block header (the group starts on a super-block boundary).
+__device__ __forceinline__ void dequant_kblock_q4k(const uint8_t* codes, const uint8_t* hdr, uint32_t r, uint32_t kbg,
+                                                   uint32_t (&bits)[32]) {
+  const uint4 h4 = *reinterpret_cast<const uint4*>(hdr);
+  const uint32_t j6 = 6u * kbg;
+  const uint64_t scf = (static_cast<uint64_t>(h4.z & 0xFFFFu) << 32) | h4.y;
+  const uint64_t mnf = (static_cast<uint64_t>(h4.w) << 16) | (h4.z >> 16);
+  const float dsc = __half2float(__ushort_as_half(static_cast<unsigned short>(h4.x & 0xFFFFu))) *
+                    static_cast<float>(static_cast<uint32_t>(scf >> j6) & 63u);
+  const float ndm = -(__half2float(__ushort_as_half(static_cast<unsigned short>(h4.x >> 16))) *
+                      static_cast<float>(static_cast<uint32_t>(mnf >> j6) & 63u));
+  const uint4 q = *reinterpret_cast<const uint4*>(codes + sw128_off(r, kbg));
+  const uint32_t words[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const uint32_t lo = words[i] & 0x0F0F0F0Fu, hi = (words[i] >> 4) & 0x0F0F0F0Fu;
+#pragma unroll
+    for (int b = 0; b < 4; ++b) {
+      bits[8 * i + 2 * b] = __float_as_uint(fmaf(magic15(lo, b) - 32768.f, dsc, ndm));
+      bits[8 * i + 2 * b + 1] = __float_as_uint(fmaf(magic15(hi, b) - 32768.f, dsc, ndm));
+    }
+  }
+}
+
 __global__ void __launch_bounds__(kThreads, 1)
     k_fused_gemm(const __grid_constant__ FusedMaps maps, const __grid_constant__ FusedArgs g) {
   extern __shared__ __align__(1024) uint8_t sm_raw[];
@@ -354,10 +381,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (base) {
         const uint8_t* grp = gring + ds * g.gbytes;
         const uint32_t kbg = (s & 1u) * kSub + h;   // this warp's K-block within the group
-        const float d =
-            __half2float(*reinterpret_cast<const __half*>(grp + BM * kDGroup * g.qrow + r * (kDGroup * 2) + kbg * 2));
+        const uint8_t* hdr = grp + BM * kDGroup * g.qrow + r * (kDGroup * 2);   // row r's 8 scales or q4_K header
         uint32_t bits[32];
-        dequant_kblock(grp, g.quant, r, kbg, d, bits);
+        if (g.quant == OVL_Q4_K) {
+          dequant_kblock_q4k(grp, hdr, r, kbg, bits);
+        } else {
+          const float d = __half2float(*reinterpret_cast<const __half*>(hdr + kbg * 2));
+          dequant_kblock(grp, g.quant, r, kbg, d, bits);
+        }
         __syncwarp();   // every lane is done with this stage's codes and scales
         if (lane == 0 && ((s & 1u) == 1 || s + 1 == g.bstages)) mbar_arrive(&dempty[ds]);
         tmem_st32_async(col + BK * h, bits);

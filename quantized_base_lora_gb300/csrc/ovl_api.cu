@@ -782,11 +782,9 @@ cudaError_t scatter_sparse(ovl_ctx* c, uint32_t tensor, float* S, std::vector<Ad
 // the q4_0 block: 204 vs 184 us at 4 tokens, 431 vs 191 us at 8).
 constexpr uint32_t kTcMinT = 4;
 
-// The tensor-core kernel reads the activations 16 bytes at a time, and reads
-// per-block f16 scales (q8_0, q4_0); q4_K super-blocks always take K1.
+// The tensor-core kernel reads the activations 16 bytes at a time.
 bool use_tc(const ovl_ctx* c, uint32_t T, const ovl_tensor_desc& td, uint32_t rtot, const void* x) {
-  return T >= kTcMinT && c->quant != OVL_Q4_K && (reinterpret_cast<uintptr_t>(x) & 15) == 0 &&
-         c->ws.tc_scratch_bytes > 0 &&
+  return T >= kTcMinT && (reinterpret_cast<uintptr_t>(x) & 15) == 0 && c->ws.tc_scratch_bytes > 0 &&
          fused_gemm_supported(td.d_out, td.d_in) &&
          fused_gemm_scratch_bytes(T, td.d_in, fused_vcols(rtot)) <= c->ws.tc_scratch_bytes;
 }

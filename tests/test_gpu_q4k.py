@@ -1,6 +1,7 @@
 """GPU parity of the q4_K base (256-weight super-blocks: 6-bit sub-block scales
 and minimums under two f16 scales) against the fp64 oracle, through the C ABI:
-the 8B-shape block with a rank-16 adapter at T = 1 and multi-token tiles,
+the 8B-shape block with a rank-16 adapter at T = 1, multi-token K1 tiles and
+the tensor-core route (4 tokens and more),
 multi-tensor launches, ragged shapes, a zero-B adapter, the JIT
 materialization (correctly rounded dequantization for an empty stack) and the
 JIT prefill GEMM, a segmented batch, and the d_in rule of the format."""
@@ -42,7 +43,7 @@ def test_block_q4k_decode_bf16(block_q4k, proj):
     assert_within_bound(y, deq_of(base, proj), lora_terms([(ad, 2.0)], proj), x64, S.PROJ[proj])
 
 
-@pytest.mark.parametrize("T", [2, 3, 4, 8, 13])
+@pytest.mark.parametrize("T", [2, 3, 4, 8, 13, 64, 100])   # 4 and up: the tensor-core route
 @pytest.mark.parametrize("proj", [1, 6])
 def test_block_q4k_multi_token(block_q4k, proj, T):
     base, ad, rt = block_q4k
