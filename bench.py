@@ -626,9 +626,10 @@ WORKLOADS["segmented"] = workload_segmented
 
 
 def workload_prefill_dual(args):
-    """The dual path at T = 64 and 256 tokens (tensor-core route, K4): the
+    """The dual path at T = 64, 256 and 512 tokens (tensor-core route, K4): the
     8B-shape q8_0 block with a rank-16 adapter on all seven projections, the
-    same four launches per step as decode."""
+    same four launches per step as decode.  At T = 512 it is the prefill of
+    the per-layer JIT workload without any materialized scratch."""
     import torch
     base = S.block_base(S.Q8_0)
     ads = [S.block_adapter(base, adapter=0, rank=16)]
@@ -639,12 +640,12 @@ def workload_prefill_dual(args):
     lora = sum(16 * (t.d_in + t.d_out) * 4 for t in base.tensors)
     tpeak, tkind = tf32_peak()
     per_T = {}
-    for T in (64, 256):
+    for T in (64, 256, 512):
         xs = {d: torch.from_numpy(S.to_bf16_bits(S.activations(T, d)).view(np.int16)).cuda().view(torch.bfloat16)
               for d in (4096, 14336)}
         ybufs = [torch.empty((T, t.d_out), dtype=torch.float32, device="cuda") for t in base.tensors]
         step = _block_step(base, rts, {d: v.data_ptr() for d, v in xs.items()}, [y.data_ptr() for y in ybufs], T, sh)
-        ms = timed_steps(step, args.steps, args.warmup, stream)
+        ms = timed_steps(step, args.steps if T < 512 else max(3, min(args.steps, 20)), args.warmup, stream)
         _check_all(rts, sh)
         flops = sum(2 * T * t.d_out * t.d_in for t in base.tensors) + sum(2 * T * 16 * (t.d_in + t.d_out)
                                                                           for t in base.tensors)
@@ -657,7 +658,7 @@ def workload_prefill_dual(args):
     emit({"workload": "prefill-dual", "metric": "dual-path multi-token step (8B shape, q8_0 + r16, tensor cores)",
           "unit": "tok/s", "value": per_T[64]["tok_s"], "per_T": per_T, "steps": args.steps,
           "config": {"base": "8B-shape block q8_0 (231.7 MB)", "adapter": "r16 s=2.0 on all 7", "x": "bf16",
-                     "T": [64, 256], "l2": f"{N_COPIES} base copies rotated"}})
+                     "T": [64, 256, 512], "l2": f"{N_COPIES} base copies rotated"}})
 
 
 WORKLOADS["prefill-dual"] = workload_prefill_dual
