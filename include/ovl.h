@@ -2,11 +2,15 @@
  * ovl.h — C ABI of the dual-path quantized-base + LoRA overlay library (libovl).
  *
  * The library evaluates the linear layers of a transformer whose base weights
- * are an immutable block-quantized buffer, with an ordered stack of low-rank
- * adapters applied as overlays that are never merged into the base:
+ * are an immutable block-quantized buffer (q8_0, q4_0 or q4_K), with an ordered
+ * stack of overlays - low-rank adapters or sparse index-value overlays - applied
+ * without ever being merged into the base:
  *
- *     y = deq(W_q) x + sum_k s_k B_k (A_k x)                        (dual path)
- *     S = deq(W_q) + sum_k s_k B_k A_k ;  y = S x   (per-layer JIT, S discarded)
+ *     y = deq(W_q) x + sum_k s_k dW_k x                              (dual path)
+ *     S = deq(W_q) + sum_k s_k dW_k ;  y = S x      (per-layer JIT, S discarded)
+ *
+ * with dW_k = B_k A_k for a low-rank adapter (evaluated as B_k (A_k x) on the
+ * dual path) and dW_k = the scattered values of a sparse overlay.
  *
  * Sources, cited by page title and section:
  *   [OVR]    "We propose a content-addressed overlay system ..." report
