@@ -182,7 +182,8 @@ ovl_status ovl_create(ovl_ctx** out, int device, void* arena_dev, size_t arena_b
                       uint32_t switch_policy);
 
 /* Destroy the context after synchronizing its internal stream.  Frees host
- * state only; the arena and the base remain the caller's.  NULL is a no-op. */
+ * state only; the arena and the base remain the caller's.  NULL is a no-op.
+ * (Housekeeping of this library; the pages define no counterpart.) */
 ovl_status ovl_destroy(ovl_ctx* ctx);
 
 /* Register the immutable base ([OVR] §"Immutable base"; [DTD] §2 Oracle
@@ -209,6 +210,16 @@ ovl_status ovl_load_base(ovl_ctx* ctx, const ovl_base_desc* desc, const void* ba
 ovl_status ovl_stage_adapter(ovl_ctx* ctx, const ovl_adapter_desc* desc, const void* payload_host,
                              size_t nbytes, const uint8_t digest[32], ovl_adapter_h* out);
 
+/* Descriptor of a sparse overlay (see ovl_stage_sparse). */
+typedef struct {
+  uint32_t n_targets;
+  const uint32_t* target_tensor;    /* host arrays of n_targets, copied */
+  const uint32_t* nnz;              /* index-value pairs per target (0 allowed) */
+  const uint64_t* idx_off;
+  const uint64_t* val_off;
+  uint8_t required_base_digest[32]; /* all-zero = no requirement */
+} ovl_sparse_desc;
+
 /* Stage a sparse overlay: only the non-zero elements of each target's weight
  * update, as index-value pairs added at their positions at use time, the base
  * unchanged ([OVR] §"Runtime Strategy Comparison Matrix", Sparse Overlay;
@@ -231,19 +242,13 @@ ovl_status ovl_stage_adapter(ovl_ctx* ctx, const ovl_adapter_desc* desc, const v
  * like a low-rank adapter, in STACK compositions only; ovl_get_entry reports
  * total_rank 0 for it.  adapter_key = SHA256("OVLS" | payload_digest |
  * u32 n_targets | per target u32 tensor, nnz | u64 idx_off, val_off). */
-typedef struct {
-  uint32_t n_targets;
-  const uint32_t* target_tensor;    /* host arrays of n_targets, copied */
-  const uint32_t* nnz;              /* index-value pairs per target (0 allowed) */
-  const uint64_t* idx_off;
-  const uint64_t* val_off;
-  uint8_t required_base_digest[32]; /* all-zero = no requirement */
-} ovl_sparse_desc;
-
 ovl_status ovl_stage_sparse(ovl_ctx* ctx, const ovl_sparse_desc* desc, const void* payload_host, size_t nbytes,
                             const uint8_t digest[32], ovl_adapter_h* out);
 
-/* Release a staged adapter's arena block.  OVL_E_STATE if it is part of the
+/* Release a staged adapter's arena block, marking it free in the arena
+ * allocator (as [DTD] §6 ROLLBACK frees a staging block; [OVR] §"Proposed
+ * Activation/Deactivation State Machine", Final State: staging memory that is no
+ * longer needed is freed).  OVL_E_STATE if it is part of the
  * active or the rollback composition; OVL_E_BUSY (REJECT policy) if forward work
  * that read it is still in flight; OVL_E_ARG for an unknown handle. */
 ovl_status ovl_unstage_adapter(ovl_ctx* ctx, ovl_adapter_h h);
@@ -353,15 +358,20 @@ ovl_status ovl_dualpath_forward_noalloc(const void* qs, const void* d, uint32_t 
  * bit-identical across switches ([DTD] §2 Oracle Invariant). */
 ovl_status ovl_base_digest(ovl_ctx* ctx, uint8_t digest_out[32], void* stream);
 
-/* Snapshot of the observable state. */
+/* Snapshot of the observable state: composition id, base digest, quant
+ * profile, mode, entry count, rollback availability, epoch, arena use ([MODELD]
+ * §"Observability": which base is active, which adapters are attached). */
 ovl_status ovl_get_state(ovl_ctx* ctx, ovl_state* out);
 
-/* Entry i (< n_entries) of the active composition, in order. */
+/* Entry i (< n_entries) of the active composition, in order: handle, adapter
+ * key, scale, total rank (0 for a sparse overlay) ([MODELD] §"Observability":
+ * adapter digests and scales). */
 ovl_status ovl_get_entry(ovl_ctx* ctx, uint32_t i, ovl_entry* out);
 
 /* Synchronize `stream`, read and clear the device status word.  Returns OVL_OK,
  * OVL_E_DEVICE_TIMEOUT (a bounded device wait ran out; outputs of that launch are
- * invalid) or OVL_E_CUDA. */
+ * invalid) or OVL_E_CUDA.  (The pages define no counterpart: it reports the
+ * library's own bounded device-side waits.) */
 ovl_status ovl_check_device(ovl_ctx* ctx, void* stream);
 
 /* Fault injection for tests ([OVR] §"TDD and Fault-Injection Matrix"): the next
@@ -370,15 +380,22 @@ ovl_status ovl_check_device(ovl_ctx* ctx, void* stream);
 ovl_status ovl_debug_inject(ovl_ctx* ctx, uint32_t phase, ovl_status code);
 
 /* Message of the last failed call on ctx (static storage owned by ctx; "" after
- * success).  ctx NULL returns the message of the last failed ovl_create. */
+ * success).  ctx NULL returns the message of the last failed ovl_create.
+ * ([MODELD] §"Observability": why an adapter failed to load.) */
 const char* ovl_last_error(ovl_ctx* ctx);
 
-/* Host utilities (no device needed): FIPS 180-4 SHA-256 of n bytes, and the
- * content digest defined above, both computed by the library's own code. */
+/* Host utility (no device needed): FIPS 180-4 SHA-256 of n bytes, computed by
+ * the library's own code. */
 ovl_status ovl_sha256(const void* data, size_t n, uint8_t out[32]);
+
+/* Host utility (no device needed): the content digest defined above (64 KiB
+ * leaves), the value a caller declares for a base or a payload ([OVR]
+ * §"Checksum Verification"; [DTD] §6 CHECKSUM VERIFICATION). */
 ovl_status ovl_content_digest(const void* data, size_t n, uint8_t out[32]);
 
-/* Library version string (static). */
+/* Library version string (static); the same runtime version enters every
+ * composition id ([OVR] §"Composition Identity and Manifest Schema": the
+ * identity includes the runtime version). */
 const char* ovl_version(void);
 
 #ifdef __cplusplus

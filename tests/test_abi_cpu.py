@@ -35,6 +35,25 @@ def header_symbols():
     return sorted(set(re.findall(r"\b(ovl_[a-z0-9_]+)\s*\(", text)))
 
 
+def test_every_entry_point_cites_its_passage_or_says_it_has_none():
+    """The comment block directly above each declaration cites the passage that
+    defines the operation, or states that the pages define no counterpart."""
+    with open(os.path.join(ROOT, "include", "ovl.h")) as f:
+        text = f.read()
+    decls = list(re.finditer(r"\n(?:ovl_status|const char\*) (ovl_\w+)\(", text))
+    assert len(decls) >= 20
+    for i, m in enumerate(decls):
+        # the doc comment: the last /* ... */ that ends before this declaration
+        # and after the previous one
+        lo = decls[i - 1].end() if i else 0
+        head = text[lo:m.start()]
+        blocks = re.findall(r"/\*.*?\*/", head, flags=re.S)
+        assert blocks, m.group(1)
+        doc = blocks[-1]
+        assert any(t in doc for t in ("[OVR]", "[DTD]", "[MODELD]", "FIPS")) or "no counterpart" in doc.lower(), \
+            m.group(1)
+
+
 def test_every_declared_symbol_is_exported(ovl):
     syms = header_symbols()
     assert len(syms) >= 19
