@@ -121,7 +121,8 @@ enum { OVL_PATH_DUAL = 1, OVL_PATH_JIT = 2 };        /* evaluation path */
 enum { OVL_SWITCH_REJECT = 1, OVL_SWITCH_DRAIN = 2 };/* switch vs in-flight forward */
 enum {                                                /* activation phases ([DTD] §6) */
   OVL_PHASE_VALIDATION = 1, OVL_PHASE_ALLOCATION = 2, OVL_PHASE_STAGING = 3,
-  OVL_PHASE_CHECKSUM = 4, OVL_PHASE_SWAP = 5
+  OVL_PHASE_CHECKSUM = 4, OVL_PHASE_SWAP = 5,
+  OVL_PHASE_DEVICE_WAIT = 6   /* a bounded device-side wait of the next decode launch (tests) */
 };
 
 enum {
@@ -323,10 +324,12 @@ ovl_status ovl_segmented_forward(ovl_ctx* ctx, uint32_t tensor, const void* x, u
                                  uint32_t n_seg, const int32_t* perm, float* y, void* stream);
 
 /* Allocation-free dual-path forward.  No counterpart in the source pages: it
- * serves callers that can neither lend an arena (ovl_create) nor allocate device
- * memory at call time -- code running while a stream capture is in progress in
- * the global capture mode, where cudaMalloc is refused, or an embedder whose
- * device memory belongs entirely to its own pooled allocator.
+ * serves callers that can neither lend an arena (ovl_create) nor allocate
+ * device memory when they call -- an embedder whose device memory belongs
+ * entirely to its own pooled allocator (a cudaMalloc behind its back would
+ * escape its budget and can stall every stream of the device while the
+ * driver maps the new memory), or a caller on a latency-critical path that
+ * must not take that stall at all.
  *   y = deq(W) x + sum_k scale[k] B[k] (A[k] x), exactly the computation of
  *   ovl_linear_forward on the dual path for the STACK composition (B[0..n), ...).
  * qs, d: device pointers to one tensor's planes in the layout above (16-byte
@@ -337,17 +340,20 @@ ovl_status ovl_segmented_forward(ovl_ctx* ctx, uint32_t tensor, const void* x, u
  * Scratch: a file-scope device array of 2 MiB per device (held by every GPU
  * that loads the library until the process exits) instead of cudaMalloc; the
  * call allocates nothing and calls no allocating routine.  The first call on a
- * device looks up the array's address and clears it (synchronizing the device),
- * so make that first call before any stream capture.  Every call clears the
- * array's status word on `stream` and then reuses its contents;
- * calls that overlap on the GPU (different streams, or other threads) race on
- * the array and must be serialized by the caller.
+ * device looks up the array's device address and clears it (synchronizing the
+ * device), so make that first call before any stream capture.  Every call
+ * then clears, on `stream`, the status word and the part of the array its
+ * launches use, and numbers those launches' partial sums afresh: nothing of
+ * an earlier call is read.  Calls that overlap on the GPU (different streams,
+ * or other threads) race on the shared array and must be serialized by the
+ * caller.
  * Errors: OVL_E_QUANT (also for OVL_Q4_K, which this entry point does not
  * take), OVL_E_SHAPE (d_in, alignment, rank, total rank), OVL_E_ARG
  * (null pointers, dtype, T > OVL_MAX_T, n_terms > OVL_MAX_STACK, non-finite
  * scale), OVL_E_OOM (the low-rank partial sums would need more than the 2 MiB
- * array), OVL_E_CUDA.  T = 0 is a no-op.  Device-side timeouts are latched in
- * the array's status word only. */
+ * array), OVL_E_CUDA.  T = 0 is a no-op.  If a bounded device-side wait runs
+ * out (other work holding the SMs the launch needs), the outputs it covers
+ * are written as NaN. */
 ovl_status ovl_dualpath_forward_noalloc(const void* qs, const void* d, uint32_t quant, uint32_t d_out,
                                         uint32_t d_in, const float* const* A, const float* const* B,
                                         const uint32_t* rank, const float* scale, uint32_t n_terms,
@@ -376,7 +382,14 @@ ovl_status ovl_check_device(ovl_ctx* ctx, void* stream);
 
 /* Fault injection for tests ([OVR] §"TDD and Fault-Injection Matrix"): the next
  * stage/activate/rollback that reaches `phase` fails there with `code` (< 0),
- * with the same cleanup as a real failure.  code 0 clears a pending injection. */
+ * with the same cleanup as a real failure.  code 0 clears a pending injection.
+ * OVL_PHASE_DEVICE_WAIT (code must be OVL_E_DEVICE_TIMEOUT): the next
+ * ovl_linear_forward / ovl_linear_forward_multi that runs the decode kernel
+ * with a low-rank term withholds the partial sums of its first CTA and limits
+ * the gather's poll to about a millisecond, so that bounded wait runs out: the
+ * call returns OVL_OK, the launch's outputs are NaN, and the following
+ * ovl_check_device returns OVL_E_DEVICE_TIMEOUT.  No state changes; nothing
+ * faults or hangs; the next forward is normal. */
 ovl_status ovl_debug_inject(ovl_ctx* ctx, uint32_t phase, ovl_status code);
 
 /* Message of the last failed call on ctx (static storage owned by ctx; "" after

@@ -39,7 +39,7 @@ OVL_MODE_STACK, OVL_MODE_TABLE = 1, 2
 OVL_PATH_DUAL, OVL_PATH_JIT = 1, 2
 OVL_SWITCH_REJECT, OVL_SWITCH_DRAIN = 1, 2
 (OVL_PHASE_VALIDATION, OVL_PHASE_ALLOCATION, OVL_PHASE_STAGING,
- OVL_PHASE_CHECKSUM, OVL_PHASE_SWAP) = 1, 2, 3, 4, 5
+ OVL_PHASE_CHECKSUM, OVL_PHASE_SWAP, OVL_PHASE_DEVICE_WAIT) = 1, 2, 3, 4, 5, 6
 OVL_MAX_STACK, OVL_MAX_TABLE, OVL_MAX_RANK, OVL_MAX_TOTAL_RANK, OVL_MAX_T, OVL_MAX_SEGMENTS = 8, 32, 128, 256, 512, 64
 
 

@@ -16,13 +16,19 @@
 //    (cp.async.bulk, TMA engine, L2 evict-first) into an NS-deep shared-memory
 //    ring guarded by mbarriers.  No multicast.
 //  * Every consumer lane owns fixed 32-weight column blocks for the whole
-//    kernel.  The activation block is rewritten once per launch as an exact
-//    integer: x_j = X_j * 2^-s_b with |X_j| < 2^22 split into three byte limbs
-//    (h signed, m and l unsigned).  The base dot product of a block is then
-//    exact integer arithmetic on the dp4a units (no per-weight conversion):
-//    P = 65536 * sum(q h) + 256 * sum(q m) + sum(q l), and acc += d * 2^-s_b * P
-//    in fp32.  q4_0 codes are used unsigned with the -8 offset folded into the
-//    accumulator start (-8 * sum of limbs).
+//    kernel.  The activation block is rewritten once per launch on a fixed-point
+//    grid: x_j ~ X_j * 2^-s_b with |X_j| <= 2^22 (22 bits below the block's
+//    largest element) split into three byte limbs (h signed, m and l unsigned).
+//    The base dot product of a block is then exact integer arithmetic on the
+//    dp4a units (no per-weight conversion): P = 65536 * sum(q h) + 256 *
+//    sum(q m) + sum(q l), and acc += d * 2^-s_b * P in fp32.  q4_0 codes are
+//    used unsigned with the -8 offset folded into the accumulator start (-8 *
+//    sum of limbs).  The grid represents an element exactly when it lies
+//    within 2^14 of the block maximum (bf16 input) and to 2^-12 of itself when
+//    it lies within 2^10 (fp32 input); a block with any smaller nonzero element
+//    is marked when its record is built, and the epilogue adds its exact fp32
+//    residual sum_j w_j (x_j - X_j 2^-s), so every element keeps 12 bits
+//    relative to itself whatever the block's dynamic range.
 //  * The low-rank shrink v = A x is a side product: each CTA reduces one
 //    contiguous chunk of the flattened [sum r_k][n] factor space and publishes
 //    partial sums; after its rows are streamed the CTA waits (bounded) for all
@@ -97,7 +103,11 @@ struct DualCfg {
   uint32_t b_areg;               // 1: the helper copies B rows into the A/x-window area after its shrink
   uint32_t div32;                // 1: rtot * n * gs < 2^32, chunk arithmetic fits 32 bits
   uint32_t smem;
+  uint32_t off_mk;               // marked-block map: 1 + TT * map_words(nb) words
 };
+
+// Words per token of the marked-block map.
+__host__ __device__ __forceinline__ uint32_t map_words(uint32_t nb) { return (nb + 31) / 32; }
 
 __device__ __forceinline__ void latch(uint32_t* status, uint32_t code) {
   atomicCAS(status, 0u, code);
@@ -111,29 +121,60 @@ __device__ __forceinline__ float load_x(const void* x, uint32_t xdt, size_t i) {
 }
 
 // Activation records.  Record (t, b) describes the 32-block b of token t as
-// an exact integer vector X with x_j = X_j * 2^-s (|X_j| <= 2^22), split in
-// three byte limbs X = 65536 h + 256 m + l with h signed (byte 2 of X) and m, l
+// an integer vector X with x_j ~ X_j * 2^-s (|X_j| <= 2^22), split in three
+// byte limbs X = 65536 h + 256 m + l with h signed (byte 2 of X) and m, l
 // unsigned (bytes 1 and 0): words 0-7 = h, 8-15 = m, 16-23 = l, then
 // {2^-s as f32 bits, start_h, start_m, start_l}.  Limb word k holds the four
 // elements that weight word k consumes: elements 4k..4k+3 for q8_0; for q4_0
 // word 2g carries the low nibbles (elements 8g, 8g+2, 8g+4, 8g+6) and word
 // 2g+1 the high nibbles (8g+1, ...).  The q4_0 starts are -8 * sum of the limbs,
 // which folds the code offset into the integer accumulators.
-// Block exponent of a record: x_j = X_j * 2^-s with |X_j| <= 2^22.  Blocks
-// whose largest magnitude is below 2^-104 (including subnormal-only blocks) are
-// flushed to zero: their whole contribution is below 2^-104 * 127 * 32 *
-// max|d|, far under the absolute 1e-5 term of the output bound.  Finite fp32
-// inputs cannot need a downward shift beyond the normal range.
+//
+// Precision.  s = 21 - E with 2^E <= max|x| < 2^(E+1), so an element is
+// rounded to the nearest multiple of 2^(E-21): the error is at most 2^(E-22).
+// A bf16 element (8 significant bits) at or above 2^(E-14) lies on the grid
+// and is exact; an fp32 element at or above 2^(E-10) keeps a rounding error of
+// at most 2^-12 of itself.  A block holding a smaller nonzero element (or a
+// non-finite one, or a largest magnitude below 2^-104, where the grid would
+// leave the normal range) is marked: its bit is set in the CTA's marked-block
+// map (word 0: any block marked; then one row of words per token) and nothing
+// else changes on the integer path.  The epilogue adds, in plain fp32, the
+// marked blocks' residual products sum_j w_j (x_j - X_j 2^-s) (block_residual),
+// re-reading only their weights.  The residual of each element is exact in
+// fp32 and no larger than the element, so the sum of the two parts keeps each
+// element to fp32 precision without cancellation against the integer part.
+// Typical activations mark no block, and the hot loop carries no branch for it.
 struct BlockScale {
-  float sc;   // 2^s
-  float xs;   // 2^-s (0 for a flushed block)
+  float sc;   // 2^s (0 when the block is below 2^-104 or all zero)
+  float xs;   // 2^-s
 };
 __device__ __forceinline__ BlockScale block_scale(uint32_t mx) {
   const int E = static_cast<int>(mx >> 23) - 127;   // mx >= 2^-104 is normal
   const int s = 21 - E;
-  if (mx < 0x0B800000u) return BlockScale{0.f, 0.f};  // 2^-104: flush
+  if (mx < 0x0B800000u) return BlockScale{0.f, 0.f};  // all zero, or marked below
   return BlockScale{__uint_as_float(static_cast<uint32_t>(s + 127) << 23),
                     __uint_as_float(static_cast<uint32_t>(127 - s) << 23)};
+}
+
+// Smallest element magnitude (as fp32 bits) that the grid of a block with
+// largest magnitude mx carries to 2^-12 of itself: 2^(E-14) for bf16 input,
+// 2^(E-10) for fp32 input.
+__device__ __forceinline__ uint32_t grid_floor_bits(uint32_t mx, uint32_t xdt) {
+  return (mx & 0x7F800000u) - ((xdt == OVL_BF16 ? 14u : 10u) << 23);
+}
+
+// True when the block must take the fp32 route: mx = largest magnitude bits,
+// mn1 = (smallest nonzero magnitude bits) - 1 (0xFFFFFFFF if none).
+__device__ __forceinline__ bool block_marked(uint32_t mx, uint32_t mn1, uint32_t xdt) {
+  if (mx == 0) return false;
+  if (mx >= 0x7F800000u || mx < 0x0B800000u) return true;   // Inf/NaN, or below 2^-104
+  return mn1 + 1u < grid_floor_bits(mx, xdt);
+}
+
+// Record a marked block (t, b) in the CTA's map.
+__device__ __forceinline__ void mark_block(uint32_t* mk, uint32_t mkw, uint32_t t, uint32_t b) {
+  atomicOr(mk, 1u);
+  atomicOr(mk + 1 + t * mkw + (b >> 5), 1u << (b & 31));
 }
 
 // Exact round-to-nearest-even of v * 2^s to an integer, |result| <= 2^22:
@@ -195,18 +236,28 @@ __device__ __forceinline__ void load_word_inputs(const void* xsrc, uint32_t xdt,
 }
 
 template <bool Q4>
-__device__ __forceinline__ void build_record(uint8_t* rec, uint32_t ri, bool live, uint32_t k, const float (&v)[4]) {
-  uint32_t mx = 0;
+__device__ __forceinline__ void build_record(uint8_t* rec, uint32_t ri, bool live, uint32_t k, const float (&v)[4],
+                                             uint32_t xdt, uint32_t* mk, uint32_t mkw, uint32_t t, uint32_t b) {
+  uint32_t mx = 0, mn1 = 0xFFFFFFFFu;
 #pragma unroll
-  for (int i = 0; i < 4; ++i) mx = max(mx, __float_as_uint(v[i]) & 0x7FFFFFFFu);
-  mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-  mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-  mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+  for (int i = 0; i < 4; ++i) {
+    const uint32_t av = __float_as_uint(v[i]) & 0x7FFFFFFFu;
+    mx = max(mx, av);
+    mn1 = min(mn1, av - 1u);
+  }
+#pragma unroll
+  for (int o = 1; o <= 4; o <<= 1) {
+    mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    mn1 = min(mn1, __shfl_xor_sync(0xffffffffu, mn1, o));
+  }
   const BlockScale bs = block_scale(mx);
-  const float xs = bs.xs;
   int X[4];
 #pragma unroll
   for (int i = 0; i < 4; ++i) X[i] = round_scaled(v[i], bs.sc);
+  const float xs = bs.xs;
+  // The record is the same whether or not the block is marked; a marked
+  // block only sets its bit in the map (the epilogue adds its residual).
+  if (block_marked(mx, mn1, xdt) && live && k == 0) mark_block(mk, mkw, t, b);
   uint32_t hw, mw, lw;
   limb_words(X, hw, mw, lw);
   int sh = 0, sm = 0, sl = 0;
@@ -235,7 +286,8 @@ __device__ __forceinline__ void build_record(uint8_t* rec, uint32_t ri, bool liv
 // The record of one block built by a single lane straight into registers
 // (single-token launches) from activations staged in shared memory.
 template <bool Q4>
-__device__ __forceinline__ void lane_record(uint4 (&r)[7], const void* xsrc, uint32_t xdt, bool vec, size_t row) {
+__device__ __forceinline__ void lane_record(uint4 (&r)[7], const void* xsrc, uint32_t xdt, bool vec, size_t row,
+                                            uint32_t* mk, uint32_t mkw) {
   float v[32];
   if (vec && xdt == OVL_BF16) {
     const uint4* p = reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(xsrc) + row);
@@ -258,17 +310,22 @@ __device__ __forceinline__ void lane_record(uint4 (&r)[7], const void* xsrc, uin
 #pragma unroll
     for (int j = 0; j < 32; ++j) v[j] = load_x(xsrc, xdt, row + j);
   }
-  uint32_t mx = 0;
+  uint32_t mx = 0, mn1 = 0xFFFFFFFFu;
 #pragma unroll
-  for (int j = 0; j < 32; ++j) mx = max(mx, __float_as_uint(v[j]) & 0x7FFFFFFFu);
+  for (int j = 0; j < 32; ++j) {
+    const uint32_t av = __float_as_uint(v[j]) & 0x7FFFFFFFu;
+    mx = max(mx, av);
+    mn1 = min(mn1, av - 1u);
+  }
   const BlockScale bs = block_scale(mx);
+  const float sc = bs.sc;
   int sh = 0, sm = 0, sl = 0;
   uint32_t hw[8], mw[8], lw[8];
 #pragma unroll
   for (int w = 0; w < 8; ++w) {
     int X[4];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) X[i] = round_scaled(v[Q4 ? (8 * (w >> 1) + (w & 1) + 2 * i) : (4 * w + i)], bs.sc);
+    for (int i = 0; i < 4; ++i) X[i] = round_scaled(v[Q4 ? (8 * (w >> 1) + (w & 1) + 2 * i) : (4 * w + i)], sc);
     limb_words(X, hw[w], mw[w], lw[w]);
     if (Q4) {
       sh = dp4a_ss(static_cast<int>(hw[w]), 0x01010101, sh);
@@ -282,14 +339,19 @@ __device__ __forceinline__ void lane_record(uint4 (&r)[7], const void* xsrc, uin
   r[3] = make_uint4(mw[4], mw[5], mw[6], mw[7]);
   r[4] = make_uint4(lw[0], lw[1], lw[2], lw[3]);
   r[5] = make_uint4(lw[4], lw[5], lw[6], lw[7]);
-  r[6] = Q4 ? make_uint4(__float_as_uint(bs.xs), static_cast<uint32_t>(-8 * sh), static_cast<uint32_t>(-8 * sm),
+  const float xs = bs.xs;
+  // The record is the same whether or not the block is marked; a marked
+  // block only sets its bit in the map (the epilogue adds its residual).
+  if (block_marked(mx, mn1, xdt)) mark_block(mk, mkw, 0, static_cast<uint32_t>(row >> 5));
+  r[6] = Q4 ? make_uint4(__float_as_uint(xs), static_cast<uint32_t>(-8 * sh), static_cast<uint32_t>(-8 * sm),
                          static_cast<uint32_t>(-8 * sl))
-            : make_uint4(__float_as_uint(bs.xs), 0u, 0u, 0u);
+            : make_uint4(__float_as_uint(xs), 0u, 0u, 0u);
 }
 
 template <bool Q4>
 __device__ __forceinline__ void prep_records(uint8_t* rec, const DualArgs& a, const void* xsrc, bool vec, uint32_t nb,
-                                             uint32_t warp, uint32_t nwarps, uint32_t lane) {
+                                             uint32_t warp, uint32_t nwarps, uint32_t lane, uint32_t* mk,
+                                             uint32_t mkw) {
   const uint32_t k = lane & 7;
   const uint32_t total = a.T * nb;
   for (uint32_t base = warp * 8; base < total; base += nwarps * 8) {
@@ -300,13 +362,59 @@ __device__ __forceinline__ void prep_records(uint8_t* rec, const DualArgs& a, co
     float v0[4] = {0.f, 0.f, 0.f, 0.f}, v1[4] = {0.f, 0.f, 0.f, 0.f};
     if (live0) load_word_inputs<Q4>(xsrc, a.xdt, vec, static_cast<size_t>(t0) * a.n + static_cast<size_t>(b0) * 32, k, v0);
     if (live1) load_word_inputs<Q4>(xsrc, a.xdt, vec, static_cast<size_t>(t1) * a.n + static_cast<size_t>(b1) * 32, k, v1);
-    build_record<Q4>(rec, ri0, live0, k, v0);
-    build_record<Q4>(rec, ri1, live1, k, v1);
+    build_record<Q4>(rec, ri0, live0, k, v0, a.xdt, mk, mkw, t0, b0);
+    build_record<Q4>(rec, ri1, live1, k, v1, a.xdt, mk, mkw, t1, b1);
   }
 }
 
+// P = 65536 sh + 256 sm + sl from the exact limb sums (|sh| < 2^19, |sm|, |sl|
+// < 2^21): U = 256 sh + sm is exact in int32 and rounds once to fp32, then
+// one FMA adds sl (exact in fp32), so |P~ - P| <= 2^-24 (2 |P| + |sl|) + 2^-24
+// |P|: relative to P itself plus a fraction of one unit, with no cancellation
+// between limbs whatever the signs of the elements.
 __device__ __forceinline__ float limb_combine(int sh, int sm, int sl) {
-  return fmaf(__int2float_rn(sh), 65536.f, __int2float_rn(sm * 256 + sl));
+  return fmaf(__int2float_rn(sh * 256 + sm), 256.f, __int2float_rn(sl));
+}
+
+// d * sc_j and dmin * m_j of sub-block j (j6 = 6 j) from a q4_K super-block
+// header {d, dmin (binary16), sc_0..7 (6 bits each), m_0..7 (6 bits each)}.
+// Both products are exact in fp32.
+__device__ __forceinline__ void q4k_scales(const uint4 h, uint32_t j6, float* dsc, float* dmn) {
+  const uint64_t scf = (static_cast<uint64_t>(h.z & 0xFFFFu) << 32) | h.y;
+  const uint64_t mnf = (static_cast<uint64_t>(h.w) << 16) | (h.z >> 16);
+  *dsc = __half2float(__ushort_as_half(static_cast<unsigned short>(h.x & 0xFFFFu))) *
+         static_cast<float>(static_cast<uint32_t>(scf >> j6) & 63u);
+  *dmn = __half2float(__ushort_as_half(static_cast<unsigned short>(h.x >> 16))) *
+         static_cast<float>(static_cast<uint32_t>(mnf >> j6) & 63u);
+}
+
+// The residual product of a marked block with one row: sum_j w_j r_j, where
+// r_j = x_j - X_j 2^-s is what the block's record left out of element j (the
+// record's X_j and 2^-s are recomputed from x exactly as the record was built)
+// and w_j = fma(code_j, dq, -dm) (q8_0: code = q, dq = d, dm = 0; q4_0: code
+// 0..15, dq = d, dm = 8 d -- both exact; q4_K: dq = d sc_j, dm = dmin m_j, one
+// rounding).  r_j is exact in fp32 (a multiple of the element's own unit in the
+// last place, below half a grid step) and |r_j| <= |x_j|.  Four fixed FMA chains,
+// combined in a fixed order.  Error <= 10 * 2^-24 * sum|w_j r_j|.
+template <bool Q4>
+__device__ __forceinline__ float block_residual(const uint4 (&wq)[2], float dq, float dm, const void* xsrc,
+                                                uint32_t xdt, size_t xoff) {
+  uint32_t mx = 0;
+  for (int j = 0; j < 32; ++j) mx = max(mx, __float_as_uint(load_x(xsrc, xdt, xoff + j)) & 0x7FFFFFFFu);
+  const BlockScale bs = block_scale(mx);
+  const uint32_t* wb = reinterpret_cast<const uint32_t*>(wq);
+  float c[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 4
+  for (int j = 0; j < 32; ++j) {
+    const float v = load_x(xsrc, xdt, xoff + j);
+    const float Xf = static_cast<float>(round_scaled(v, bs.sc));
+    const float r = fmaf(-Xf, bs.xs, v);
+    const uint32_t byte = (wb[(Q4 ? (j >> 1) : j) >> 2] >> (8 * ((Q4 ? (j >> 1) : j) & 3))) & 0xFFu;
+    const float code = Q4 ? static_cast<float>((byte >> (4 * (j & 1))) & 15u)
+                          : static_cast<float>(static_cast<int8_t>(static_cast<uint8_t>(byte)));
+    c[j & 3] = fmaf(fmaf(code, dq, -dm), r, c[j & 3]);
+  }
+  return (c[0] + c[1]) + (c[2] + c[3]);
 }
 
 __device__ __forceinline__ float dot_q8(const uint8_t* wp, const uint4 (&r)[7]) {
@@ -496,6 +604,14 @@ __device__ __forceinline__ uint32_t row_token_mask(const DualArgs& a, const EpTe
   return m;
 }
 
+// Epoch tag of a shrink CTA's partial sums.  With the test-only withhold flag
+// CTA 0 tags them with a value no reader accepts, so the gather's bounded
+// wait runs out.
+__device__ __forceinline__ uint32_t launch_epoch(const DualArgs& a) { return a.epoch & ~kEpochWithhold; }
+__device__ __forceinline__ uint32_t slot_tag(const DualArgs& a, uint32_t cta) {
+  return ((a.epoch & kEpochWithhold) && cta == 0) ? a.epoch : launch_epoch(a);
+}
+
 // Partial shrink sums of this CTA's chunk of the flattened [rtot][n] factor
 // space, computed by one warp: slot (t * rtot + rho) * gs + cta receives
 // sum_{j in chunk, row rho} A[rho][j] x[t][j] for every token t that needs
@@ -550,7 +666,7 @@ __device__ void shrink_chunk_warp(const DualArgs& a, const DualCfg& c, uint32_t 
       const float v = warp_sum(acc[t]);
       if (lane == 0)
         st_relaxed_u64(slots + (static_cast<size_t>(t) * a.rtot + rho) * c.gs + cta,
-                       (static_cast<unsigned long long>(a.epoch) << 32) | __float_as_uint(v));
+                       (static_cast<unsigned long long>(slot_tag(a, cta)) << 32) | __float_as_uint(v));
     }
   }
 }
@@ -561,9 +677,12 @@ __device__ void shrink_chunk_warp(const DualArgs& a, const DualCfg& c, uint32_t 
 // launch's epoch.  Each row is summed over its slots in CTA order.
 template <int NP, int PER>
 __device__ __forceinline__ void gather_rows(const DualArgs& a, const DualCfg& c, float* vsm, uint32_t base,
-                                            const EpTerm* ep, uint32_t nterm, uint32_t lane) {
+                                            const EpTerm* ept, uint32_t nterm, uint32_t lane) {
+  bool ok = true;
   const unsigned long long* slots = reinterpret_cast<const unsigned long long*>(a.ws.partial);
   const uint32_t npairs = a.T * a.rtot;
+  const uint32_t ep = launch_epoch(a);
+  const uint32_t limit = (a.epoch & kEpochWithhold) ? (1u << 10) : (1u << 21);
   uint32_t cf[NP], cl[NP];
   bool live[NP];
   const unsigned long long* pp[NP];
@@ -574,7 +693,7 @@ __device__ __forceinline__ void gather_rows(const DualArgs& a, const DualCfg& c,
     live[h] = i < npairs;
     const uint32_t t = live[h] ? i / a.rtot : 0, rho = live[h] ? i - t * a.rtot : 0;
     // segmented batches: a token needs only the rows of its own term
-    if (live[h] && a.tok_sel && a.tok_term[t] != static_cast<int>(term_of_row(ep, nterm, rho))) live[h] = false;
+    if (live[h] && a.tok_sel && a.tok_term[t] != static_cast<int>(term_of_row(ept, nterm, rho))) live[h] = false;
     partial_range(a, c, rho, &cf[h], &cl[h]);
     pp[h] = slots + (static_cast<size_t>(t) * a.rtot + rho) * c.gs;
     sum[h] = 0.f;
@@ -594,12 +713,13 @@ __device__ __forceinline__ void gather_rows(const DualArgs& a, const DualCfg& c,
           const uint32_t qq = cf[h] + q + u;
           const bool use = live[h] && qq <= cl[h];
           v[h][u] = use ? ld_relaxed_u64(pp[h] + qq) : 0ull;
-          all = all && (!use || static_cast<uint32_t>(v[h][u] >> 32) == a.epoch);
+          all = all && (!use || static_cast<uint32_t>(v[h][u] >> 32) == ep);
         }
       }
       if (all) break;
-      if (it > (1u << 21)) {
+      if (it > limit) {
         latch(a.ws.status, kDevTimeoutShrink);
+        ok = false;
         break;
       }
       __nanosleep(64);
@@ -610,9 +730,11 @@ __device__ __forceinline__ void gather_rows(const DualArgs& a, const DualCfg& c,
       for (int u = 0; u < PER; ++u)
         if (live[h] && cf[h] + q + u <= cl[h]) sum[h] += __uint_as_float(static_cast<uint32_t>(v[h][u]));
   }
+  // A row whose poll gave up is stored as NaN: every output that uses it
+  // becomes NaN instead of silently missing part of its low-rank term.
 #pragma unroll
   for (int h = 0; h < NP; ++h)
-    if (live[h]) vsm[base + lane + 32 * h] = sum[h];
+    if (live[h]) vsm[base + lane + 32 * h] = ok ? sum[h] : __uint_as_float(0x7FC00000u);
 }
 
 // The B rows [row0, row0 + nrows) of one low-rank term as a 16-byte aligned
@@ -627,6 +749,40 @@ __device__ __forceinline__ BSpan b_span(const float* B, uint32_t r, uint32_t row
   const uintptr_t lo = s & ~static_cast<uintptr_t>(15);
   return BSpan{reinterpret_cast<const uint8_t*>(lo), static_cast<uint32_t>(((e + 15) & ~static_cast<uintptr_t>(15)) - lo),
                static_cast<uint32_t>(s - lo)};
+}
+
+// Sum over the marked blocks of token t (ascending block order) of their
+// residual products with row `row` of the CTA's tensor, in plain fp32: each
+// block's weights are re-read from the immutable base planes in global memory.
+template <int QUANT>
+__device__ __noinline__ float marked_sum(const uint32_t* mk, const DualArgs& a, const DualCfg& c, const DualSeg& sg,
+                                         uint32_t t, uint32_t row, const void* xsrc) {
+  constexpr bool QK4 = QUANT == OVL_Q4_K;
+  constexpr bool Q4 = QUANT != OVL_Q8_0;
+  const uint32_t mkw = map_words(c.nb);
+  float sum = 0.f;
+  for (uint32_t w = 0; w < mkw; ++w) {
+    uint32_t bits = mk[1 + t * mkw + w];
+    while (bits) {
+      const uint32_t b = 32 * w + static_cast<uint32_t>(__ffs(static_cast<int>(bits)) - 1);
+      bits &= bits - 1;
+      const uint8_t* wp = sg.qs + static_cast<size_t>(row) * c.rowbytes + static_cast<size_t>(b) * (Q4 ? 16u : 32u);
+      uint4 wq[2];
+      wq[0] = *reinterpret_cast<const uint4*>(wp);
+      wq[1] = Q4 ? make_uint4(0u, 0u, 0u, 0u) : *reinterpret_cast<const uint4*>(wp + 16);
+      float dq, dm;
+      if constexpr (QK4) {
+        const uint4 h =
+            *reinterpret_cast<const uint4*>(sg.dpl + static_cast<size_t>(row) * c.nb * 2 + (b >> 3) * 16u);
+        q4k_scales(h, 6u * (b & 7u), &dq, &dm);
+      } else {
+        dq = __half2float(*reinterpret_cast<const __half*>(sg.dpl + (static_cast<size_t>(row) * c.nb + b) * 2));
+        dm = Q4 ? 8.f * dq : 0.f;
+      }
+      sum += block_residual<Q4>(wq, dq, dm, xsrc, a.xdt, static_cast<size_t>(t) * a.n + static_cast<size_t>(b) * 32);
+    }
+  }
+  return sum;
 }
 
 template <int QUANT, int TT, int RG>
@@ -651,6 +807,7 @@ __global__ void __launch_bounds__(K1Shape<TT, RG>::threads, K1Shape<TT, RG>::min
   float* vsm = reinterpret_cast<float*>(sm + c.off_v);
   EpTerm* ep = reinterpret_cast<EpTerm*>(sm + c.off_ep);
   float* sA = reinterpret_cast<float*>(sm + c.off_a);
+  uint32_t* mk = reinterpret_cast<uint32_t*>(sm + c.off_mk);
 
   const uint32_t warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t ncw = c.nwc * c.ng;               // consumer warps
@@ -666,6 +823,7 @@ __global__ void __launch_bounds__(K1Shape<TT, RG>::threads, K1Shape<TT, RG>::min
   const uint32_t nrows = row1 - row0;
   const uint32_t nst = (nrows + RG - 1) / RG;
 
+  for (uint32_t i = threadIdx.x; i < 1 + TT * map_words(c.nb); i += blockDim.x) mk[i] = 0u;
   if (threadIdx.x == 0) {
     for (uint32_t i = 0; i < c.ns; ++i) {
       mbar_init(&full[i], 1);
@@ -839,7 +997,7 @@ __global__ void __launch_bounds__(K1Shape<TT, RG>::threads, K1Shape<TT, RG>::min
         const float v = warp_sum((c4[0] + c4[1]) + (c4[2] + c4[3]));
         if (lane == 0)
           st_relaxed_u64(slots + static_cast<size_t>(rho) * c.gs + cta,
-                         (static_cast<unsigned long long>(a.epoch) << 32) | __float_as_uint(v));
+                         (static_cast<unsigned long long>(slot_tag(a, cta)) << 32) | __float_as_uint(v));
       }
     } else if (cta < c.gs) {
       shrink_chunk_warp<TT>(a, c, cta, sA, xsrc, ep, sg.k1 - sg.k0, lane);
@@ -897,7 +1055,7 @@ __global__ void __launch_bounds__(K1Shape<TT, RG>::threads, K1Shape<TT, RG>::min
   //    records in registers; any further blocks (and multi-token launches) use
   //    records built cooperatively in shared memory.
   if (TT > 1 || c.bpl > static_cast<uint32_t>(NREG)) {
-    prep_records<Q4>(rec, a, xsrc, c.xvec != 0, c.nb, warp, ncw, lane);
+    prep_records<Q4>(rec, a, xsrc, c.xvec != 0, c.nb, warp, ncw, lane, mk, map_words(c.nb));
     named_bar(1, nthr);
   }
   uint4 rreg[NREG][7];
@@ -906,7 +1064,7 @@ __global__ void __launch_bounds__(K1Shape<TT, RG>::threads, K1Shape<TT, RG>::min
     for (int k = 0; k < NREG; ++k) {
       const uint32_t b = L + k * ncol;
       if (k < static_cast<int>(c.bpl) && b < c.nb)
-        lane_record<Q4>(rreg[k], xsrc, a.xdt, c.xvec != 0, static_cast<size_t>(b) * 32);
+        lane_record<Q4>(rreg[k], xsrc, a.xdt, c.xvec != 0, static_cast<size_t>(b) * 32, mk, map_words(c.nb));
     }
   }
 
@@ -943,12 +1101,8 @@ __global__ void __launch_bounds__(K1Shape<TT, RG>::threads, K1Shape<TT, RG>::min
           const uint8_t* wp = sq + rr * c.rowbytes + b * kBlockBytes;
           const float P = dot_q4(wp, r) + sx8;                       // sum(code*X)
           const uint4 h = *reinterpret_cast<const uint4*>(hb + static_cast<size_t>(rr) * c.nb * 2);
-          const uint64_t scf = (static_cast<uint64_t>(h.z & 0xFFFFu) << 32) | h.y;
-          const uint64_t mnf = (static_cast<uint64_t>(h.w) << 16) | (h.z >> 16);
-          const float dsc = __half2float(__ushort_as_half(static_cast<unsigned short>(h.x & 0xFFFFu))) *
-                            static_cast<float>(static_cast<uint32_t>(scf >> j6) & 63u);
-          const float dmn = __half2float(__ushort_as_half(static_cast<unsigned short>(h.x >> 16))) *
-                            static_cast<float>(static_cast<uint32_t>(mnf >> j6) & 63u);
+          float dsc, dmn;
+          q4k_scales(h, j6, &dsc, &dmn);
           acc[t * RG + rr] = fmaf(dsc * xs, P, acc[t * RG + rr]);
           acc[t * RG + rr] = fmaf(-dmn * xs, 0.125f * sx8, acc[t * RG + rr]);
         }
@@ -1010,6 +1164,12 @@ __global__ void __launch_bounds__(K1Shape<TT, RG>::threads, K1Shape<TT, RG>::min
   float rv[kMaxThreads / 32];
   EpTerm e0{};
   uint32_t rot0 = 0;
+  // A stage that never arrived (the producer or a consumer warp gave up) left
+  // rows of this CTA without their base sums: the flag was set before the
+  // barrier above, so it is read here, off the critical path.
+  if (*abort_flag) ok = false;
+  const bool any_marked = mk[0] != 0u;
+  float corr = 0.f;   // fast path: the marked blocks' residual products (before the waits)
   if (fast) {
     const uint32_t lr = threadIdx.x;
 #pragma unroll
@@ -1019,6 +1179,7 @@ __global__ void __launch_bounds__(K1Shape<TT, RG>::threads, K1Shape<TT, RG>::min
       e0 = ep[0];
       rot0 = lr % e0.r;
     }
+    if (any_marked && lr < nrows) corr = marked_sum<QUANT>(mk, a, c, sg, 0, row0 + lr, xsrc);
   }
   // 4. the low-rank vector from the helper warp and the B rows from the
   //    producer (bounded waits)
@@ -1031,8 +1192,16 @@ __global__ void __launch_bounds__(K1Shape<TT, RG>::threads, K1Shape<TT, RG>::min
     ok = false;
   }
 
-  // 5. epilogue, one output per thread: y = base + sum_k s_k (B_k v_k)
-  if (!ok) return;
+  // 5. epilogue, one output per thread: y = base + sum_k s_k (B_k v_k).  If
+  //    any bounded wait of this CTA gave up (the status word holds the code),
+  //    its outputs are written as NaN rather than left stale or partial.
+  if (!ok) {
+    for (uint32_t i = threadIdx.x; i < a.T * nrows; i += nthr) {
+      const uint32_t t = i / nrows, lr = i - t * nrows;
+      sg.y[static_cast<size_t>(t) * sg.m + row0 + lr] = __uint_as_float(0x7FC00000u);
+    }
+    return;
+  }
   if (fast) {
     const uint32_t lr = threadIdx.x;
     if (lr >= nrows) return;
@@ -1040,6 +1209,7 @@ __global__ void __launch_bounds__(K1Shape<TT, RG>::threads, K1Shape<TT, RG>::min
 #pragma unroll
     for (int w = 0; w < kMaxThreads / 32; ++w)
       if (w < static_cast<int>(c.nwc)) yv += rv[w];
+    yv += corr;
     if (nterm) {
       const uint32_t r = e0.r;
       const float* Brow = reinterpret_cast<const float*>(sBst + e0.here) + lr * r;
@@ -1066,6 +1236,7 @@ __global__ void __launch_bounds__(K1Shape<TT, RG>::threads, K1Shape<TT, RG>::min
     const uint32_t row = row0 + lr;
     float yv = 0.f;
     for (uint32_t w = 0; w < c.nwc; ++w) yv += red[(w * TT + t) * c.rows_max + lr];
+    if (any_marked) yv += marked_sum<QUANT>(mk, a, c, sg, t, row, xsrc);
     uint32_t rbase = sg.rb0;   // global rank offset of the term
     for (uint32_t k = sg.k0; k < sg.k1; ++k) {
       const EpTerm e = ep[k - sg.k0];
@@ -1143,6 +1314,8 @@ bool plan(DualCfg& c, const DualArgs& a, int tt, int rg, uint32_t rows_max, uint
   off = round_up(off + tt * a.rtot * 4 + 4, 128);
   c.off_ep = off;
   off = round_up(off + a.nl * static_cast<uint32_t>(sizeof(EpTerm)), 128);
+  c.off_mk = off;
+  off = round_up(off + (1 + tt * map_words(c.nb)) * 4, 128);
   c.off_x = off;
   if (c.stage_x) off = round_up(off + tt * a.n * (a.xdt == OVL_BF16 ? 2 : 4), 128);
   c.off_a = off;
@@ -1318,12 +1491,13 @@ cudaError_t launch_dualpath(const DualArgs& a_in, cudaStream_t st) {
       // A fresh epoch per launch; on wrap-around clear the slots first so no
       // slot can carry a reused epoch.
       uint32_t ep = ++*a0.ws.epoch_counter;
-      if (ep == 0) {
+      if (ep >= kEpochWithhold) {
         e = cudaMemsetAsync(a0.ws.partial, 0, a0.ws.partial_floats * sizeof(float), st);
         if (e != cudaSuccess) return e;
+        *a0.ws.epoch_counter = 0;
         ep = ++*a0.ws.epoch_counter;
       }
-      a.epoch = ep;
+      a.epoch = ep | (a0.epoch & kEpochWithhold);
     }
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = dim3(G_used);

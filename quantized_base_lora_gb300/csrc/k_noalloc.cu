@@ -2,13 +2,12 @@
 //
 // The regular entry point (ovl_linear_forward) takes its kernel scratch -- the
 // low-rank partial sums and the device status word -- from the arena that the
-// caller lent to ovl_create.  Some callers have no
-// arena to lend and cannot allocate device memory when they call: code that
-// runs while a stream capture is in progress in the global capture mode (where
-// cudaMalloc is refused), or an embedder whose device memory is owned entirely
-// by its own pooled allocator.  For them this file keeps the scratch in one
-// file-scope device array, sized once at load time, so a call needs nothing but
-// the caller's inputs and outputs.
+// caller lent to ovl_create.  Some callers have no arena to lend and cannot
+// allocate device memory when they call: an embedder whose device memory is
+// owned entirely by its own pooled allocator, or a caller on a latency-critical
+// path that cannot take the device-wide stall a cudaMalloc may cause.  For them
+// this file keeps the scratch in one file-scope device array, sized once at
+// load time, so a call needs nothing but the caller's inputs and outputs.
 //
 // There is no counterpart to this entry point in the source pages; it is an
 // interface convenience around the same kernel (k_dualpath) and computes
@@ -37,28 +36,32 @@ static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocBytes];
 
 std::mutex g_setup_mu;
 uint8_t* g_scratch_addr[kMaxDevices] = {};
-uint32_t g_epoch[kMaxDevices] = {};   // last partial-slot epoch per device (calls are serialized)
+int g_sms[kMaxDevices] = {};
 
 // Device address of the array on the current device, looked up (and the array
 // cleared) on the first call for that device.  In host code the array's name is
 // only a host-side stand-in, so the kernel receives this looked-up address.
-cudaError_t scratch_for_current_device(uint8_t** out, int* dev_out) {
+cudaError_t scratch_for_current_device(uint8_t** out, int* sms_out) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-  *dev_out = dev;
   std::lock_guard<std::mutex> lk(g_setup_mu);
   if (!g_scratch_addr[dev]) {
     void* p = nullptr;
     e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
     if (e != cudaSuccess) return e;
+    int sms = 0;
+    e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
     e = cudaMemset(p, 0, kNoAllocBytes);
     if (e == cudaSuccess) e = cudaDeviceSynchronize();
     if (e != cudaSuccess) return e;
+    g_sms[dev] = sms > 0 ? sms : 1;
     g_scratch_addr[dev] = static_cast<uint8_t*>(p);
   }
   *out = g_scratch_addr[dev];
+  *sms_out = g_sms[dev];
   return cudaSuccess;
 }
 
@@ -93,8 +96,8 @@ extern "C" ovl_status ovl_dualpath_forward_noalloc(const void* qs, const void* d
   if (T == 0) return OVL_OK;
 
   uint8_t* scratch = nullptr;
-  int dev = 0;
-  cudaError_t e = scratch_for_current_device(&scratch, &dev);
+  int sms = 1;
+  cudaError_t e = scratch_for_current_device(&scratch, &sms);
   if (e != cudaSuccess) {
     cudaGetLastError();
     return OVL_E_CUDA;
@@ -104,12 +107,17 @@ extern "C" ovl_status ovl_dualpath_forward_noalloc(const void* qs, const void* d
   const uint64_t need = kNoAllocPartial + 8ull * 8 * rtot;
   if (n_terms && need > kNoAllocBytes) return OVL_E_OOM;   // more scratch than the static array holds
   cudaStream_t st = static_cast<cudaStream_t>(stream);
-  // The status word must start at zero.
-  e = cudaMemsetAsync(scratch, 0, kNoAllocPartial, st);
+  // Clear the status word and every partial-sum slot this call's launches can
+  // use (at most 8 tokens x total rank x one shrink CTA per SM, 8 bytes each);
+  // the launches then tag their slots with epochs 1, 2, ... counted in this
+  // call alone, so no slot written by an earlier call is ever accepted.
+  const uint64_t used = n_terms ? kNoAllocPartial + 8ull * 8 * rtot * static_cast<uint64_t>(sms) : kNoAllocPartial;
+  e = cudaMemsetAsync(scratch, 0, static_cast<size_t>(std::min<uint64_t>(used, kNoAllocBytes)), st);
   if (e != cudaSuccess) {
     cudaGetLastError();
     return OVL_E_CUDA;
   }
+  uint32_t epoch = 0;
   a.qs = static_cast<const uint8_t*>(qs);
   a.dpl = static_cast<const uint8_t*>(d);
   a.m = d_out;
@@ -124,7 +132,7 @@ extern "C" ovl_status ovl_dualpath_forward_noalloc(const void* qs, const void* d
   a.ws.status = reinterpret_cast<uint32_t*>(scratch + kNoAllocStatus);
   a.ws.partial = reinterpret_cast<float*>(scratch + kNoAllocPartial);
   a.ws.partial_floats = (kNoAllocBytes - kNoAllocPartial) / sizeof(float);
-  a.ws.epoch_counter = &g_epoch[dev];
+  a.ws.epoch_counter = &epoch;
   // B rows are bulk-copied in 16-byte granules only when that stays inside the
   // caller's B arrays.
   a.b_pad = 1;

@@ -822,6 +822,15 @@ cudaError_t launch_tc(const ovl_ctx* c, const ovl_tensor_desc& td, const void* x
   return launch_fused_gemm(L, st);
 }
 
+// A pending OVL_PHASE_DEVICE_WAIT injection applies to the next decode launch
+// that has a low-rank term (the gather it disturbs exists only then).
+uint32_t take_device_wait_injection(ovl_ctx* c, uint32_t nl) {
+  if (nl == 0 || c->inject_phase != OVL_PHASE_DEVICE_WAIT || c->inject_code >= 0) return 0u;
+  c->inject_phase = 0;
+  c->inject_code = 0;
+  return 1u;
+}
+
 // One event per forward call: forward work on a context is stream-ordered, so
 // once the latest record has completed every earlier forward has too.
 ovl_status record_use(ovl_ctx* c, const std::vector<Adapter*>& used, cudaStream_t st) {
@@ -906,6 +915,7 @@ ovl_status ovl_linear_forward(ovl_ctx* ctx, uint32_t tensor, const void* x, uint
     a.rtot = rtot;
     for (uint32_t i = 0; i < nl; ++i) a.lora[i] = terms[i];
     a.ws = ctx->ws;
+    a.epoch = take_device_wait_injection(ctx, nl) ? kEpochWithhold : 0u;
     cudaError_t e = launch_dualpath(a, st);
     if (e == cudaSuccess) e = apply_sparse(ctx, &tensor, 1, x, x_dtype, T, &y, &used, st);
     if (e != cudaSuccess) return cuda_fail(ctx, e, "dual-path launch");
@@ -1013,6 +1023,7 @@ ovl_status ovl_linear_forward_multi(ovl_ctx* ctx, uint32_t n, const uint32_t* te
   a.xdt = x_dtype;
   a.T = T;
   a.ws = ctx->ws;
+  a.epoch = take_device_wait_injection(ctx, a.nl) ? kEpochWithhold : 0u;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   cudaError_t e = launch_dualpath(a, st);
   if (e == cudaSuccess) e = apply_sparse(ctx, tensors, n, x, x_dtype, T, ys, &used, st);
@@ -1159,7 +1170,9 @@ ovl_status ovl_check_device(ovl_ctx* ctx, void* stream) {
 ovl_status ovl_debug_inject(ovl_ctx* ctx, uint32_t phase, ovl_status code) {
   if (!ctx) return OVL_E_ARG;
   std::lock_guard<std::mutex> lk(ctx->mu);
-  if (code > 0 || phase < OVL_PHASE_VALIDATION || phase > OVL_PHASE_SWAP) return fail(ctx, OVL_E_ARG, "bad injection");
+  if (code > 0 || phase < OVL_PHASE_VALIDATION || phase > OVL_PHASE_DEVICE_WAIT) return fail(ctx, OVL_E_ARG, "bad injection");
+  if (phase == OVL_PHASE_DEVICE_WAIT && code != 0 && code != OVL_E_DEVICE_TIMEOUT)
+    return fail(ctx, OVL_E_ARG, "a device-wait injection takes OVL_E_DEVICE_TIMEOUT");
   ctx->inject_phase = code ? phase : 0;
   ctx->inject_code = code;
   return ok(ctx);

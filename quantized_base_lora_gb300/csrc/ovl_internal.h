@@ -35,11 +35,12 @@ struct LoraRef {
 // word)}: a reader accepts a slot once it carries its own launch's epoch, so no
 // slot ever needs clearing between launches.  The epoch counter is host memory
 // (launcher only); epochs start at 1 and the slots are cleared when it wraps.
+// An epoch is below 2^31: bit 31 of DualArgs::epoch carries a test request.
 struct Workspace {
   uint32_t* status;               // one status word (device)
   float* partial;                 // partial-sum slots (device), 8 bytes each
   size_t partial_floats;          // size of that region in floats
-  uint32_t* epoch_counter;        // host: last epoch handed out
+  uint32_t* epoch_counter;        // host: last epoch handed out (wraps below 2^31)
   float* tc_scratch;              // tensor-core path scratch (device, 256-byte aligned)
   size_t tc_scratch_bytes;        // 0: the tensor-core path is not available
 };
@@ -58,6 +59,7 @@ struct DualSeg {
 };
 
 constexpr int kMaxMulti = 4;
+constexpr uint32_t kEpochWithhold = 0x80000000u;
 constexpr uint32_t kTokTile = 64;       // tokens per tensor-core launch
 
 // Fused dual-path forward over a token chunk (T <= 8).  Single-tensor callers
@@ -76,7 +78,10 @@ struct DualArgs {
   uint32_t xdt, T;
   uint32_t nl;            // number of low-rank terms
   uint32_t rtot;          // sum of ranks
-  uint32_t epoch;         // this launch's partial-slot epoch (filled by the launcher)
+  uint32_t epoch;         // this launch's partial-slot epoch (filled by the launcher, < 2^31);
+                          // bit 31 (kEpochWithhold) is a test-only request: CTA 0 tags its partial
+                          // sums with an epoch no reader accepts and the gather polls about a
+                          // millisecond, so that bounded wait runs out
   uint32_t nseg;          // 0: single tensor (qs/dpl/m/y); else seg[0..nseg)
   // Per-token term selection (segmented batches): when tok_sel is set, token t
   // of the launch receives only term tok_term[t] (-1: base only).

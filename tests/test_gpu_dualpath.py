@@ -209,7 +209,7 @@ def test_activation_scale_extremes_stay_within_bound():
     x[1, 32:64] *= np.float32(1e-30)                  # tiny block
     x[2, 64:96] *= np.float32(1e20)                   # huge block
     x[3, ::7] *= np.float32(1e-6)                     # mixed magnitudes inside blocks
-    x[3, 96:128] *= np.float32(1e-35)                 # below 2^-104: the block is flushed to zero
+    x[3, 96:128] *= np.float32(1e-35)                 # below 2^-104: the block takes the fp32 route
     xd, x64 = x_device(x, "f32")
     y = fwd(rt, 0, xd)
     assert_within_bound(y, deq_of(base, 0), [], x64, "extremes")
@@ -278,3 +278,78 @@ def test_tensor_core_path(case):
     y2 = fwd(rt, 0, xd)                                  # deterministic
     assert np.array_equal(y.view(np.uint32), y2.view(np.uint32))
     rt.close()
+
+
+# ----------------------------------------------------------------- outliers on zero-weight columns
+# A block whose largest activation meets a zero weight while its other
+# activations are ~1e7 times smaller: sum_j |w_ij x_j| is made of the small
+# elements only, so they must keep their own precision (the decode kernel
+# takes such blocks through plain fp32).  Outlier columns vary inside the
+# block; every other block carries no outlier, so marked and unmarked blocks
+# meet in one launch.
+OUTLIER_CASES = [  # (quant, d_out, d_in, T, ranks, xdtype)
+    (S.Q8_0, 64, 32, 1, (), "f32"),
+    (S.Q8_0, 64, 32, 2, (4,), "bf16"),
+    (S.Q8_0, 300, 4096, 1, (16,), "bf16"),
+    (S.Q8_0, 300, 4096, 1, (), "f32"),
+    (S.Q8_0, 300, 4096, 2, (16,), "f32"),
+    (S.Q8_0, 300, 4096, 3, (16,), "bf16"),
+    (S.Q4_0, 200, 4096, 1, (8,), "bf16"),
+    (S.Q4_0, 200, 4096, 3, (), "f32"),
+    (S.Q8_0, 160, 14336, 1, (16,), "bf16"),      # two register records per lane
+    (S.Q4_0, 96, 14336, 2, (), "f32"),
+]
+
+
+def outlier_layer(quant, m, n, T, ranks, seed):
+    rng = np.random.default_rng(seed)
+    W = S.gaussian(rng, (m, n), 0.02)
+    cols = np.array([32 * b + (7 * b) % 32 for b in range(0, n // 32, 2)])
+    W[:, cols] = 0.0                                 # code 0 (q8_0) / 8 (q4_0): weight exactly 0
+    base = S.build_base(quant, [(0, 0, W)])
+    ads = []
+    for k, r in enumerate(ranks):
+        A = S.gaussian(rng, (r, n), 0.01)
+        B = S.gaussian(rng, (m, r), 0.01)
+        ads.append((S.build_adapter(base, [0], [r], [(A, B)]), [2.0, 0.5][k % 2]))
+    x = S.gaussian(rng, (T, n), 1.0) * np.float32(1e-3)
+    sign = np.where(rng.standard_normal((T, cols.size)) < 0, -1.0, 1.0).astype(np.float32)
+    x[:, cols] = np.float32(1e4) * sign
+    return base, ads, x.astype(np.float32)
+
+
+@pytest.mark.parametrize("case", OUTLIER_CASES,
+                         ids=[f"q{c[0]}_{c[1]}x{c[2]}_T{c[3]}_r{'-'.join(map(str, c[4]))}_{c[5]}" for c in OUTLIER_CASES])
+def test_outlier_on_zero_weight_stays_within_bound(case):
+    require_gpu()
+    quant, m, n, T, ranks, xdt = case
+    base, ads, x = outlier_layer(quant, m, n, T, ranks, seed=m + n + T)
+    rt = make_runtime(base, arena_bytes=64 << 20)
+    hs = [stage(rt, ad) for ad, _ in ads]
+    assert rt.activate(hs, [s for _, s in ads])[0] == 0
+    xd, x64 = x_device(x, xdt)
+    y = fwd(rt, 0, xd)
+    assert_within_bound(y, deq_of(base, 0), lora_terms(ads, 0), x64, str(case))
+    y2 = fwd(rt, 0, xd)
+    assert np.array_equal(y.view(np.uint32), y2.view(np.uint32))   # deterministic
+    rt.close()
+
+
+def test_outlier_blocks_in_multi_tensor_launch(block_q8):
+    """q+k+v in one launch, two blocks of x holding an outlier ~1e9 times
+    their neighbours: every CTA of every tensor adds the marked blocks."""
+    import quantized_base_lora_gb300 as q
+    base, ad, rt = block_q8
+    rng = np.random.default_rng(17)
+    x = S.gaussian(rng, (1, 4096), 1.0) * np.float32(1e-4)
+    x[0, 5] = np.float32(3e5)
+    x[0, 4000] = np.float32(-2e6)
+    xd, x64 = x_device(x, "bf16")
+    group = [0, 1, 2]
+    ys = [torch.full((1, base.tensors[i].d_out), float("nan"), device="cuda") for i in group]
+    st = q.ovl_linear_forward_multi(rt.ctx, group, xd.data_ptr(), q.OVL_BF16, 1, [y.data_ptr() for y in ys],
+                                    int(torch.cuda.current_stream().cuda_stream))
+    torch.cuda.synchronize()
+    assert st == 0 and rt.check_device() == 0
+    for i, y in zip(group, ys):
+        assert_within_bound(y.cpu().numpy(), deq_of(base, i), lora_terms([(ad, 2.0)], i), x64, f"outlier {i}")

@@ -150,6 +150,8 @@ def test_switch_refused_while_forward_in_flight(env):
     q, base, ad_a, ad_b, s, rt = env
     ha = stage(rt, ad_a)
     xd = torch.randn(1, 256, device="cuda")
+    rt.forward(0, xd)                  # first use loads the kernel (lazy module loading waits for the device)
+    torch.cuda.synchronize()
     torch.cuda._sleep(400_000_000)                           # keeps the stream busy (~0.2 s)
     rt.forward(0, xd)
     before = snapshot(rt)
@@ -234,3 +236,40 @@ def test_switch_transcript_matches_oracle():
     assert got == g["transcript"]
     assert rt.base_digest()[1] == d0
     rt.close()
+
+
+@pytest.mark.parametrize("multi", [False, True])
+def test_device_wait_timeout_is_reported_and_recovers(env, multi):
+    """A bounded device-side wait that runs out ([OVR] TDD and Fault-Injection
+    Matrix): the injected launch withholds one CTA's low-rank partial sums and
+    polls about a millisecond.  Its outputs come back NaN, the status check
+    reports OVL_E_DEVICE_TIMEOUT once, the state is unchanged, and the next
+    forward is exact again."""
+    from gpu_common import assert_within_bound, deq_of, lora_terms, x_device
+    q, base, ad_a, ad_b, s, rt = env
+    x = S.single_layer_256()[3]
+    ha = stage(rt, ad_a)
+    assert rt.activate([ha], [s])[0] == 0
+    xd, x64 = x_device(x, "f32")
+    sh = int(torch.cuda.current_stream().cuda_stream)
+    before = snapshot(rt)
+    digest = rt.base_digest()[1]
+    assert q.ovl_debug_inject(rt.ctx, q.OVL_PHASE_DEVICE_WAIT, q.OVL_E_CUDA) == q.OVL_E_ARG
+    assert q.ovl_debug_inject(rt.ctx, q.OVL_PHASE_DEVICE_WAIT, q.OVL_E_DEVICE_TIMEOUT) == 0
+    y = torch.zeros((1, 256), device="cuda")
+    if multi:
+        st = q.ovl_linear_forward_multi(rt.ctx, [0], xd.data_ptr(), q.OVL_F32, 1, [y.data_ptr()], sh)
+    else:
+        st = q.ovl_linear_forward(rt.ctx, 0, xd.data_ptr(), q.OVL_F32, 1, y.data_ptr(), q.OVL_PATH_DUAL, 0, 0, sh)
+    assert st == 0
+    torch.cuda.synchronize()
+    assert bool(torch.isnan(y).all()), "outputs of a timed-out launch must be NaN"
+    assert rt.check_device() == q.OVL_E_DEVICE_TIMEOUT
+    assert rt.check_device() == 0                       # read and cleared
+    assert snapshot(rt) == before and rt.base_digest()[1] == digest
+    y2 = rt.forward(0, xd)
+    torch.cuda.synchronize()
+    assert rt.check_device() == 0
+    terms = lora_terms([(ad_a, s)], 0)
+    assert_within_bound(y2.cpu().numpy(), deq_of(base, 0), terms, x64, "after timeout")
+    rt.activate([], [])

@@ -1,14 +1,15 @@
 """The allocation-free dual-path forward (ovl_dualpath_forward_noalloc).
 
 It exists for callers that can neither lend the library an arena nor allocate
-device memory at call time (for example code running inside a global-mode
-stream capture, or an embedder whose device memory belongs to its own pooled
-allocator).  Its scratch lives in one file-scope device array that every call
-reuses.  This test calls it twice in a row through the C ABI -- the second call
-runs on whatever the first left in the array -- and checks both outputs against
-the regular entry point (ovl_linear_forward) and the oracle, within the same
-per-output tolerance as the other parity tests.  Self-contained: it passes in a
-fresh process and after the rest of the suite.  Kept last in collection order.
+device memory when they call: an embedder whose device memory belongs to its
+own pooled allocator, or a latency-critical caller that cannot take the
+device-wide stall a cudaMalloc may cause.  Its scratch lives in one file-scope
+device array that every call reuses.  This test calls it twice in a row
+through the C ABI -- the second call runs on whatever the first left in the
+array -- and checks both outputs against the regular entry point
+(ovl_linear_forward) and the oracle, within the same per-output tolerance as
+the other parity tests.  Self-contained: it passes in a fresh process and after
+the rest of the suite.  Kept last in collection order.
 """
 import numpy as np
 import pytest
@@ -20,19 +21,26 @@ from gpu_common import assert_within_bound, deq_of, lora_terms, make_runtime, re
 pytestmark = pytest.mark.gpu
 
 CASES = [
-    # quant, d_out, d_in, T, ranks, scales, x dtype
-    (S.Q8_0, 1024, 4096, 1, (16,), (2.0,), "bf16"),
-    (S.Q4_0, 1000, 288, 3, (5, 7), (1.0, 0.5), "f32"),
+    # quant, d_out, d_in, T, ranks, scales, x dtype, outliers
+    (S.Q8_0, 1024, 4096, 1, (16,), (2.0,), "bf16", False),
+    (S.Q4_0, 1000, 288, 3, (5, 7), (1.0, 0.5), "f32", False),
     # 8 tokens at an aligned d_in: linear_forward takes the tensor-core route
     # here, this entry point the decode kernel's 8-token tiles
-    (S.Q8_0, 512, 2048, 8, (16, 4), (1.0, 0.5), "bf16"),
+    (S.Q8_0, 512, 2048, 8, (16, 4), (1.0, 0.5), "bf16", False),
+    # 24 tokens: three launches of 8-token tiles in one call, sharing the slots
+    (S.Q8_0, 512, 4096, 24, (16,), (2.0,), "bf16", False),
+    # outliers ~1e7 times their block neighbours, on columns whose weights are 0
+    (S.Q8_0, 300, 4096, 2, (16,), (2.0,), "f32", True),
 ]
 
 
 def _build(case, seed):
-    quant, m, n, T, ranks, scales, xdt = case
+    quant, m, n, T, ranks, scales, xdt, outliers = case
     rng = np.random.default_rng(seed)
     W = S.gaussian(rng, (m, n), 0.02)
+    cols = np.array([32 * b + (5 * b) % 32 for b in range(0, n // 32, 3)])
+    if outliers:
+        W[:, cols] = 0.0
     base = S.build_base(quant, [(0, 0, W)])
     ads = []
     for r, s in zip(ranks, scales):
@@ -40,6 +48,9 @@ def _build(case, seed):
         B = S.gaussian(rng, (m, r), 0.01)
         ads.append((S.build_adapter(base, [0], [r], [(A, B)]), s))
     x = S.gaussian(rng, (T, n), 1.0)
+    if outliers:
+        x *= np.float32(1e-3)
+        x[:, cols] = np.float32(1e4)
     return base, ads, x
 
 
