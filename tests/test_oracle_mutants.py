@@ -157,8 +157,42 @@ def test_composition_id_ignores_the_scale(monkeypatch):
     assert caught(P.test_composition_id_invariants)
 
 
+def test_base_key_offsets_packed_as_u32(monkeypatch):
+    import hashlib
+    import struct
+
+    def bad(digest, quant, tensors):
+        tensors = list(tensors)
+        h = hashlib.sha256(b"OVLB" + digest + struct.pack("<II", quant, len(tensors)))
+        for t in tensors:
+            h.update(struct.pack("<IIIIII", *[v & 0xFFFFFFFF for v in t]))
+        return h.digest()
+    plant(monkeypatch, "base_key", bad)
+    assert caught(P.test_base_key_field_by_field)
+
+
+def test_adapter_key_rank_and_tensor_swapped(monkeypatch):
+    AK = M.adapter_key
+    plant(monkeypatch, "adapter_key", lambda dg, targets: AK(dg, [(r, ti, ao, bo) for ti, r, ao, bo in targets]))
+    assert caught(P.test_adapter_key_field_by_field)
+
+
+def test_composition_id_without_the_runtime_tag(monkeypatch):
+    monkeypatch.setattr(M, "RUNTIME_TAG", b"")
+    assert caught(P.test_composition_id_field_by_field)
+
+
+def test_tree_digest_hashes_the_whole_buffer_once(monkeypatch):
+    import hashlib
+    plant(monkeypatch, "tree_digest", lambda buf, leaf=M.LEAF: hashlib.sha256(
+        hashlib.sha256(bytes(memoryview(buf).cast("B"))).digest()).digest())
+    assert caught(P.test_tree_digest_multi_leaf_closed_forms)
+
+
 @pytest.mark.parametrize("pin", [P.test_q4_0_nibble_order_hand_built, P.test_unit_outer_product_moves_one_weight_by_s,
                                  P.test_q4_k_sub_block_staircase_hand_evaluated,
-                                 P.test_sparse_single_entry_moves_exactly_one_weight])
+                                 P.test_sparse_single_entry_moves_exactly_one_weight,
+                                 P.test_base_key_field_by_field, P.test_adapter_key_field_by_field,
+                                 P.test_composition_id_field_by_field, P.test_tree_digest_multi_leaf_closed_forms])
 def test_pins_pass_without_a_planted_mistake(pin):
     assert not caught(pin)

@@ -508,6 +508,68 @@ def test_tree_digest_matches_caller_side_digest(size):
     assert O.tree_digest(buf) == S.content_digest(buf)
 
 
+# The identity byte strings, assembled field by field from the C header's text
+# (little-endian u32 / u64 fields, 4-byte tags, a 16-byte runtime tag) with
+# int.to_bytes and hashlib: values are chosen so that a field packed at the
+# wrong width, two fields swapped or a dropped field changes the digest.
+def _u32(v):
+    return int(v).to_bytes(4, "little")
+
+
+def _u64(v):
+    return int(v).to_bytes(8, "little")
+
+
+ID_TENSORS = [(3, 6, 14336, 4096, 0x1_0000_0100, 0x2_0000_0200),
+              (31, 2, 1024, 8192, 256, 0x3_FFFF_FF00)]
+ID_TARGETS = [(5, 16, 0x1_0000_0010, 0x3_0000_0020), (9, 64, 4096, 0x7_0000_2000)]
+
+
+def test_base_key_field_by_field():
+    dg = bytes(range(100, 132))
+    raw = b"OVLB" + dg + _u32(O.Q4_0) + _u32(len(ID_TENSORS))
+    for layer, proj, d_out, d_in, qs_off, d_off in ID_TENSORS:
+        raw += _u32(layer) + _u32(proj) + _u32(d_out) + _u32(d_in) + _u64(qs_off) + _u64(d_off)
+    assert len(raw) == 4 + 32 + 8 + 2 * 32
+    assert O.base_key(dg, O.Q4_0, ID_TENSORS) == hashlib.sha256(raw).digest()
+
+
+def test_adapter_key_field_by_field():
+    dg = bytes(range(200, 232))
+    raw = b"OVLA" + dg + _u32(len(ID_TARGETS))
+    for tensor, rank, a_off, b_off in ID_TARGETS:
+        raw += _u32(tensor) + _u32(rank) + _u64(a_off) + _u64(b_off)
+    assert len(raw) == 4 + 32 + 4 + 2 * 24
+    assert O.adapter_key(dg, ID_TARGETS) == hashlib.sha256(raw).digest()
+
+
+def test_composition_id_field_by_field():
+    bk = hashlib.sha256(b"base").digest()
+    k1, k2 = hashlib.sha256(b"one").digest(), hashlib.sha256(b"two").digest()
+    tag = b"ovl-gb300 v1" + bytes(4)                   # 16 bytes, zero padded
+    scales = [2.0, -0.75]
+    raw = b"OVLC" + tag + bk + _u32(O.MODE_TABLE) + _u32(2)
+    for k, sc in zip((k1, k2), scales):
+        raw += k + np.float32(sc).tobytes()            # IEEE-754 binary32 bits, little-endian
+    assert O.composition_id(bk, O.MODE_TABLE, list(zip((k1, k2), scales))) == hashlib.sha256(raw).digest()
+    # an empty composition is recorded with mode STACK whatever mode was asked
+    empty = hashlib.sha256(b"OVLC" + tag + bk + _u32(O.MODE_STACK) + _u32(0)).digest()
+    assert O.composition_id(bk, O.MODE_TABLE, []) == empty
+    assert O.composition_id(bk, O.MODE_STACK, []) == empty
+
+
+def test_tree_digest_multi_leaf_closed_forms():
+    """Two and three leaves: SHA256(SHA256(l0) | SHA256(l1) [| SHA256(l2)]),
+    the last leaf short."""
+    rng = np.random.default_rng(11)
+    for size in (O.LEAF + 100, 2 * O.LEAF + 1):
+        buf = rng.integers(0, 256, size=size, dtype=np.uint8).tobytes()
+        leaves = [buf[i:i + 65536] for i in range(0, size, 65536)]
+        assert len(leaves) == (2 if size < 2 * 65536 else 3)
+        want = hashlib.sha256(b"".join(hashlib.sha256(l).digest() for l in leaves)).digest()
+        assert O.tree_digest(np.frombuffer(buf, np.uint8)) == want
+
+
 def test_composition_id_invariants():
     bk = O.base_key(b"\1" * 32, O.Q8_0, [(0, 0, 256, 256, 0, 65536)])
     ka = O.adapter_key(b"\2" * 32, [(0, 8, 0, 8192)])
