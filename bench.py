@@ -254,85 +254,60 @@ def run_ours(args, world, rank, local):
     d_outs = [t.d_out for t in base.tensors]
     y_off = np.concatenate([[0], np.cumsum(d_outs)]).astype(int)
     ybuf = torch.empty(int(y_off[-1]), dtype=torch.float32, device=dev)
-    x_addr = {d: v.data_ptr() for d, v in xs.items()}
     stream = torch.cuda.Stream(device=dev)
     sh = int(stream.cuda_stream)
-
-    groups = [[0, 1, 2], [3], [4, 5], [6]]          # qkv | o | gate+up | down
-
+    step = block_step(q, base.tensors, sh)
+    x_addr = {d: v.data_ptr() for d, v in xs.items()}
     y_ptr = [ybuf.data_ptr() + 4 * int(y_off[i]) for i in range(len(d_outs))]
-
-    def step(rt, xmap):
-        # xmap: d_in -> device address of that step's activations (bf16)
-        for grp in groups:
-            xp = xmap[base.tensors[grp[0]].d_in]
-            if len(grp) == 1:
-                st = q.ovl_linear_forward(rt.ctx, grp[0], xp, q.OVL_BF16, 1, y_ptr[grp[0]], q.OVL_PATH_DUAL, 0, 0, sh)
-            else:
-                st = q.ovl_linear_forward_multi(rt.ctx, grp, xp, q.OVL_BF16, 1, [y_ptr[i] for i in grp], sh)
-            if st != 0:
-                raise q.OvlError(st, q.ovl_last_error(rt.ctx))
 
     with torch.cuda.stream(stream):
         for i in range(max(args.warmup, 3)):
-            step(rts[i % N_COPIES], x_addr)
+            step(rts[i % N_COPIES], x_addr, y_ptr)
     stream.synchronize()
     for rt in rts:
         q.check(q.ovl_check_device(rt.ctx, sh), rt.ctx)
 
-    # ---- device-resident timed region
+    # ---- device-resident timed regions: REPEATS regions of exactly K steps,
+    # each bracketed by a barrier and a synchronize and timed by one event pair
+    # on the launching stream (an event between two launches would cut the
+    # programmatic dependency that lets a launch stream while the previous
+    # grid drains); the median region is the reported one.
     clk = ClockSampler(local)
     clk.start()
     time.sleep(0.3)
-    barrier(world)
-    torch.cuda.synchronize()
-    # One event pair around the whole region: an event recorded between two
-    # launches would cut the programmatic dependency that lets each launch's
-    # CTAs start streaming while the previous grid drains.
-    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    with torch.cuda.stream(stream):
-        ev0.record(stream)
-        for i in range(args.steps):
-            step(rts[i % N_COPIES], x_addr)
-        ev1.record(stream)
-    stream.synchronize()
-    torch.cuda.synchronize()
-    barrier(world)
+
+    def one_region(i0):
+        with torch.cuda.stream(stream):
+            for i in range(args.steps):
+                step(rts[(i0 + i) % N_COPIES], x_addr, y_ptr)
+
+    region_ms = timed_regions(one_region, stream, world)
     clocks = clk.stop()
-    total_ms = ev0.elapsed_time(ev1)
     for rt in rts:
         q.check(q.ovl_check_device(rt.ctx, sh), rt.ctx)
 
-    # ---- end to end: pinned host x in, host y out, every step
-    x_pin = {d: torch.from_numpy(v.view(np.int16)).pin_memory() for d, v in xs_host.items()}
-    x_dev = {d: torch.empty(v.shape, dtype=torch.int16, device=dev) for d, v in xs_host.items()}
-    xdev_addr = {d: v.data_ptr() for d, v in x_dev.items()}
-    y_pin = torch.empty(int(y_off[-1]), dtype=torch.float32).pin_memory()
-    h2d = sum(v.nbytes for v in xs_host.values())
-    d2h = int(y_off[-1]) * 4
-    torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    with torch.cuda.stream(stream):
-        e0.record(stream)
-        for i in range(args.steps):
-            for d in x_dev:
-                x_dev[d].copy_(x_pin[d], non_blocking=True)
-            step(rts[i % N_COPIES], xdev_addr)
-            y_pin.copy_(ybuf, non_blocking=True)
-        e1.record(stream)
-    stream.synchronize()
-    e2e_ms = e0.elapsed_time(e1)
+    # ---- end to end through the same C-ABI calls: every step copies its x in
+    # from pinned host memory and its y out to pinned host memory, on a copy
+    # stream, double-buffered and ordered by events, so the copies of one step
+    # overlap the compute of the previous one.
+    e2e_ms, h2d, d2h = e2e_region(torch, step, rts, xs_host, int(y_off[-1]), y_off, stream, dev, args.steps)
+
+    # ---- tok/s: one decode token through the 32-layer stack of the block,
+    # every layer with its own seeds (224 projection calls, 128 launches)
+    tok = decode32_tok_s(args, q, torch, dev, stream) if world == 1 else None
 
     eff = effective_bytes(base, ad)
     alg = algorithmic_bytes(base, ad)
-    t_max = max_over_ranks(total_ms, world)
+    med_ms = statistics.median(region_ms)
+    t_max = max_over_ranks(med_ms, world)
     e2e_max = max_over_ranks(e2e_ms, world)
     if rank != 0:
         return
     peak, peak_kind = peaks()
-    mean_step_s = total_ms / args.steps / 1e3
+    mean_step_s = med_ms / args.steps / 1e3
     achieved = alg / mean_step_s / 1e9
     value = world * eff * args.steps / (t_max / 1e3) / 1e9
+    mhz = clocks.get("sm_mhz") or 0.0
     out = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": max(args.warmup, 3), "ms_per_step": t_max / args.steps, "higher_is_better": True,
@@ -340,21 +315,29 @@ def run_ours(args, world, rank, local):
         "config": {"workload": WORKLOAD, "global_batch": world, "seq_len": 1, "parallelism": f"replicas x{world}",
                    "l2": f"{N_COPIES} identical base copies rotated per step ({N_COPIES} x "
                          f"{eff / 1e6:.1f} MB > 129 MB L2); no flush inside the timed region",
-                   "effective_bytes_per_step": eff, "algorithmic_bytes_per_step": alg},
-        "tok_s": world * args.steps / (t_max / 1e3),
-        "tok_s_per_gpu": args.steps / (t_max / 1e3),
+                   "effective_bytes_per_step": eff, "algorithmic_bytes_per_step": alg,
+                   "timing": f"{REPEATS} regions of {args.steps} steps each; value from the median region"},
+        "repeats": {"ms_per_step": [r / args.steps for r in region_ms],
+                    "us_per_step_x_sm_mhz": [r / args.steps * 1e3 * mhz for r in region_ms],
+                    "sm_mhz_median": mhz},
+        "tok_s": tok["tok_s"] if tok else None,
+        "tok_s_note": ("decode tokens/s through the 32-layer stack of the block (every layer its own seeds, "
+                       "rank-16 LoRA on all 224 projections), 1 / time of one token's 224 projection calls; "
+                       "measured at N=1 only") if tok else "measured at N=1 only",
+        "tok_s_detail": tok,
+        "block_steps_per_s": world * args.steps / (t_max / 1e3),
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": K1_TRAFFIC_PER_LAUNCH,
-                     "algorithmic_bytes_per_launch": alg / len(groups),
+                     "algorithmic_bytes_per_launch": alg / len(GROUPS),
                      "traffic_note": "dram__bytes_read.sum + dram__bytes_write.sum per k_dualpath launch, mean over "
                                      "the step's launches, from one ncu capture of this kernel build on this workload",
                      "kernel": "k_dualpath (4 launches per step: qkv, o, gate+up, down)",
-                     "note": f"peak = {peak_kind} HBM copy bandwidth; achieved = algorithmic bytes per step / mean "
-                             f"step, CUDA events on the launching stream around the timed region (a step is "
-                             f"only k_dualpath launches)"},
+                     "note": f"peak = {peak_kind} HBM copy bandwidth; achieved = algorithmic bytes per step / step "
+                             f"time of the median region, CUDA events on the launching stream (a step is only "
+                             f"k_dualpath launches)"},
         "e2e": {"value": world * eff * args.steps / (e2e_max / 1e3) / 1e9, "unit": "GB/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-        "gpu_launches": len(groups) * args.steps,
+        "gpu_launches": len(GROUPS) * args.steps * REPEATS,
         "clocks": clocks,
     }
     if world == 1:
@@ -365,35 +348,174 @@ def run_ours(args, world, rank, local):
         rt.close()
 
 
+GROUPS = [[0, 1, 2], [3], [4, 5], [6]]          # qkv | o | gate+up | down
+REPEATS = 5
+
+
+def block_step(q, tensors, sh, layer_base: int = 0):
+    """One decode step of a block: q+k+v, o, gate+up, down (four calls, the
+    multi-tensor ones for tensors that share x).  step(rt, x_addr, y_ptr):
+    x_addr maps d_in to the device address of that step's bf16 activations,
+    y_ptr[i] is the output of tensor i of the block."""
+    def step(rt, x_addr, y_ptr, layer_base=layer_base):
+        for grp in GROUPS:
+            xp = x_addr[tensors[grp[0]].d_in]
+            if len(grp) == 1:
+                st = q.ovl_linear_forward(rt.ctx, layer_base + grp[0], xp, q.OVL_BF16, 1, y_ptr[grp[0]],
+                                          q.OVL_PATH_DUAL, 0, 0, sh)
+            else:
+                st = q.ovl_linear_forward_multi(rt.ctx, [layer_base + i for i in grp], xp, q.OVL_BF16, 1,
+                                                [y_ptr[i] for i in grp], sh)
+            if st != 0:
+                raise q.OvlError(st, q.ovl_last_error(rt.ctx))
+    return step
+
+
+def timed_regions(one_region, stream, world, repeats=REPEATS):
+    """Device ms of `repeats` regions, each one call of one_region(start index)
+    between a barrier + synchronize on both sides, timed by one event pair on
+    `stream`."""
+    import torch
+    out = []
+    for r in range(repeats):
+        barrier(world)
+        torch.cuda.synchronize()
+        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        ev0.record(stream)
+        one_region(r)
+        ev1.record(stream)
+        stream.synchronize()
+        torch.cuda.synchronize()
+        barrier(world)
+        out.append(ev0.elapsed_time(ev1))
+    return out
+
+
+def e2e_region(torch, step, rts, xs_host, n_y, y_off, stream, dev, steps):
+    """End-to-end ms of `steps` steps: H2D of each step's x from pinned host
+    memory and D2H of its y into pinned host memory on a copy stream, two
+    device buffers of each, ordered by events:
+      copy:    H2D(i+1) after step i-1 freed its x buffer, then D2H(i) after step i;
+      compute: step i after H2D(i) and after D2H(i-2) freed its y buffer."""
+    copy = torch.cuda.Stream(device=dev)
+    x_pin = {d: torch.from_numpy(v.view(np.int16)).pin_memory() for d, v in xs_host.items()}
+    x_dev = [{d: torch.empty(v.shape, dtype=torch.int16, device=dev) for d, v in xs_host.items()} for _ in range(2)]
+    y_dev = [torch.empty(n_y, dtype=torch.float32, device=dev) for _ in range(2)]
+    y_pin = [torch.empty(n_y, dtype=torch.float32).pin_memory() for _ in range(2)]
+    x_addr = [{d: v.data_ptr() for d, v in xb.items()} for xb in x_dev]
+    y_ptr = [[yb.data_ptr() + 4 * int(y_off[i]) for i in range(len(y_off) - 1)] for yb in y_dev]
+    ev_x = [torch.cuda.Event() for _ in range(2)]
+    ev_y = [torch.cuda.Event() for _ in range(2)]
+    ev_out = [torch.cuda.Event() for _ in range(2)]
+    h2d = sum(v.nbytes for v in xs_host.values())
+    d2h = n_y * 4
+
+    def h2d_copy(i):
+        b = i % 2
+        if i >= 2:
+            copy.wait_event(ev_y[b])              # step i-2 has read x buffer b
+        with torch.cuda.stream(copy):
+            for d in x_dev[b]:
+                x_dev[b][d].copy_(x_pin[d], non_blocking=True)
+        ev_x[b].record(copy)
+
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(copy)
+    h2d_copy(0)
+    for i in range(steps):
+        b = i % 2
+        stream.wait_event(ev_x[b])
+        if i >= 2:
+            stream.wait_event(ev_out[b])          # y buffer b copied out by D2H(i-2)
+        with torch.cuda.stream(stream):
+            step(rts[i % len(rts)], x_addr[b], y_ptr[b])
+        ev_y[b].record(stream)
+        if i + 1 < steps:
+            h2d_copy(i + 1)
+        copy.wait_event(ev_y[b])
+        with torch.cuda.stream(copy):
+            y_pin[b].copy_(y_dev[b], non_blocking=True)
+        ev_out[b].record(copy)
+    e1.record(copy)
+    copy.synchronize()
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1), h2d, d2h
+
+
+def decode32_tok_s(args, q, torch, dev, stream):
+    """Tokens/s of one decode token through LAYERS layers of the 8B-shape block
+    (q8_0, every layer with its own seeds, ~7.4 GB), a rank-16 adapter (own
+    seeds per layer and projection, s = 2.0) on all 224 projections."""
+    from quantized_base_lora_gb300.runtime import Runtime
+    from synth.stack import layer_stride, stack_adapter
+    rt = Runtime(arena_bytes=256 << 20)
+    stride = layer_stride(S.Q8_0)
+    stack = load_stack(rt, torch, dev)
+    ad = stack_adapter(stack, adapter=0, rank=RANK)
+    st, h = rt.stage(ad, S.content_digest(ad.payload))
+    q.check(st, rt.ctx)
+    q.check(rt.activate([h], [SCALE])[0], rt.ctx)
+    sh = int(stream.cuda_stream)
+    one = stack.tensors[:7]
+    xs = {d: torch.from_numpy(S.to_bf16_bits(S.activations(1, d)).view(np.int16)).to(dev).view(torch.bfloat16)
+          for d in (4096, 14336)}
+    x_addr = {d: v.data_ptr() for d, v in xs.items()}
+    ys = [torch.empty((1, t.d_out), dtype=torch.float32, device=dev) for t in one]
+    y_ptr = [y.data_ptr() for y in ys]
+    step = block_step(q, one, sh)
+    n = len(one)
+
+    def token():
+        for l in range(LAYERS):
+            step(rt, x_addr, y_ptr, layer_base=l * n)
+
+    with torch.cuda.stream(stream):
+        for _ in range(3):
+            token()
+    stream.synchronize()
+    q.check(q.ovl_check_device(rt.ctx, sh), rt.ctx)
+    k = max(3, min(args.steps, 20))
+
+    def region(_):
+        with torch.cuda.stream(stream):
+            for _ in range(k):
+                token()
+
+    ms = timed_regions(region, stream, 1)
+    q.check(q.ovl_check_device(rt.ctx, sh), rt.ctx)
+    one_block = S.Base(S.Q8_0, one, np.zeros(0, np.uint8))
+    alg = LAYERS * algorithmic_bytes(one_block, None)
+    med = statistics.median(ms) / k
+    peak, kind = peaks()
+    rt.close()
+    rt.base = None
+    torch.cuda.empty_cache()
+    return {"tok_s": 1e3 / med, "ms_per_token": med, "tokens_per_region": k,
+            "repeats_ms_per_token": [m / k for m in ms],
+            "launches_per_token": LAYERS * len(GROUPS),
+            "roofline": {"bound": "hbm", "achieved": alg / (med / 1e3) / 1e9, "peak": peak, "unit": "GB/s",
+                         "frac": alg / (med / 1e3) / 1e9 / peak, "algorithmic_bytes_per_token": alg,
+                         "note": f"peak = {kind} HBM copy bandwidth"},
+            "base": f"{LAYERS} layers x 231.7 MB q8_0 ({LAYERS * stride / 1e9:.2f} GB incl. 64 KiB padding)"}
+
+
 # ---------------------------------------------------------------- other workloads
-LEAF = 65536
-
-
-def replicated_digest(layer: np.ndarray, copies: int) -> bytes:
-    """Content digest of `copies` back-to-back copies of `layer` (a multiple
-    of the 64 KiB leaf): the leaves of one copy repeat."""
-    import hashlib
-    assert layer.nbytes % LEAF == 0
-    mv = memoryview(np.ascontiguousarray(layer)).cast("B")
-    leaves = b"".join(hashlib.sha256(mv[i:i + LEAF]).digest() for i in range(0, layer.nbytes, LEAF))
-    return hashlib.sha256(leaves * copies).digest()
-
-
 def timed_steps(step, steps, warmup, stream):
-    """Mean device ms per step: warm-up, then one event pair around `steps`."""
+    """Median device ms per step over REPEATS regions of `steps` steps (after
+    the warm-up), each region timed by one event pair on `stream`."""
     import torch
     with torch.cuda.stream(stream):
         for i in range(max(warmup, 3)):
             step(i)
     stream.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    with torch.cuda.stream(stream):
-        e0.record(stream)
-        for i in range(steps):
-            step(i)
-        e1.record(stream)
-    stream.synchronize()
-    return e0.elapsed_time(e1) / steps
+
+    def region(r):
+        with torch.cuda.stream(stream):
+            for i in range(steps):
+                step(r * steps + i)
+
+    return statistics.median(timed_regions(region, stream, 1)) / steps
 
 
 def emit(line: dict):
@@ -728,98 +850,36 @@ WORKLOADS["jit-prefill"] = workload_jit_prefill
 LAYERS = 32
 
 
-class _Replicated:
-    """A payload of `copies` back-to-back copies of one layer's bytes (each
-    padded to a multiple of the 64 KiB leaf) with per-copy offsets."""
-
-    def __init__(self, one: np.ndarray, copies: int):
-        self.stride = (one.nbytes + LEAF - 1) // LEAF * LEAF
-        self.layer = np.zeros(self.stride, dtype=np.uint8)
-        self.layer[:one.nbytes] = one
-        self.copies = copies
-        self.digest = replicated_digest(self.layer, copies)
-
-
-def _layers_base(rt, copies):
-    """32 device copies of the 8B-shape q8_0 layer in one buffer, registered
-    as one base of 224 tensors (layer-major)."""
-    import torch
+def load_stack(rt, torch, dev, n_layers=LAYERS):
+    """Generate the n-layer stack of the 8B-shape q8_0 block (every layer its
+    own seeds) straight into one device buffer and register it as the base of
+    `rt` (n_layers x 7 tensors, layer-major)."""
     import quantized_base_lora_gb300 as q
-    one = S.block_base(S.Q8_0)
-    rep = _Replicated(one.buf, copies)
-    dev = torch.empty(copies * rep.stride, dtype=torch.uint8, device="cuda")
-    first = torch.from_numpy(rep.layer).cuda()
-    for l in range(copies):
-        dev[l * rep.stride:(l + 1) * rep.stride].copy_(first)
-    del first
-    tensors = [(l, t.proj, t.d_out, t.d_in, l * rep.stride + t.qs_off, l * rep.stride + t.d_off)
-               for l in range(copies) for t in one.tensors]
-    q.check(q.ovl_load_base(rt.ctx, S.Q8_0, tensors, dev.data_ptr(), dev.numel(), rep.digest,
+    from synth.stack import LayerStack, layer_stride
+    buf = torch.empty(n_layers * layer_stride(S.Q8_0), dtype=torch.uint8, device=dev)
+
+    def sink(layer, off, padded):
+        buf[off:off + padded.nbytes].copy_(torch.from_numpy(padded))
+
+    stack = LayerStack(S.Q8_0, n_layers, sink)
+    torch.cuda.synchronize()
+    tensors = [(t.layer, t.proj, t.d_out, t.d_in, t.qs_off, t.d_off) for t in stack.tensors]
+    q.check(q.ovl_load_base(rt.ctx, S.Q8_0, tensors, buf.data_ptr(), buf.numel(), stack.digest,
                             int(torch.cuda.current_stream().cuda_stream)), rt.ctx)
-    rt.base, rt.tensors = dev, tensors
-    return one, rep
-
-
-class _LayersAdapter:
-    """Rank-r adapter of seed `adapter` on all 7 tensors of every layer, the
-    factors of one layer repeated in every layer (payload replicated)."""
-
-    def __init__(self, one, adapter, rank, copies):
-        ad = S.block_adapter(one, adapter=adapter, rank=rank)
-        rep = _Replicated(ad.payload, copies)
-        n = len(one.tensors)
-        self.targets = [l * n + i for l in range(copies) for i in ad.targets]
-        self.ranks = [r for _ in range(copies) for r in ad.ranks]
-        self.a_off = [l * rep.stride + o for l in range(copies) for o in ad.a_off]
-        self.b_off = [l * rep.stride + o for l in range(copies) for o in ad.b_off]
-        self.payload = np.tile(rep.layer, copies)
-        self.digest = rep.digest
+    rt.base, rt.tensors = buf, tensors
+    return stack
 
 
 def workload_decode32(args):
     import torch
     import quantized_base_lora_gb300 as q
-    from quantized_base_lora_gb300.runtime import Runtime
-    rt = Runtime(arena_bytes=256 << 20)
-    one, rep = _layers_base(rt, LAYERS)
-    ad = _LayersAdapter(one, 0, RANK, LAYERS)
-    st, h = rt.stage(ad, ad.digest)
-    q.check(st, rt.ctx)
-    q.check(rt.activate([h], [SCALE])[0], rt.ctx)
     stream = torch.cuda.Stream()
-    sh = int(stream.cuda_stream)
-    xs = {d: torch.from_numpy(S.to_bf16_bits(S.activations(1, d)).view(np.int16)).cuda().view(torch.bfloat16)
-          for d in (4096, 14336)}
-    xa = {d: v.data_ptr() for d, v in xs.items()}
-    n = len(one.tensors)
-    ys = [torch.empty((1, t.d_out), dtype=torch.float32, device="cuda") for t in one.tensors]
-    yp = [y.data_ptr() for y in ys]
-    groups = [[0, 1, 2], [3], [4, 5], [6]]
-
-    def step(i):
-        for l in range(LAYERS):
-            for grp in groups:
-                xp = xa[one.tensors[grp[0]].d_in]
-                if len(grp) == 1:
-                    st = q.ovl_linear_forward(rt.ctx, l * n + grp[0], xp, q.OVL_BF16, 1, yp[grp[0]],
-                                              q.OVL_PATH_DUAL, 0, 0, sh)
-                else:
-                    st = q.ovl_linear_forward_multi(rt.ctx, [l * n + j for j in grp], xp, q.OVL_BF16, 1,
-                                                    [yp[j] for j in grp], sh)
-                if st != 0:
-                    raise q.OvlError(st, q.ovl_last_error(rt.ctx))
-    steps = max(3, min(args.steps, 50))
-    ms = timed_steps(step, steps, min(args.warmup, 3), stream)
-    _check_all([rt], sh)
-    eff = LAYERS * (effective_bytes(one, None))
-    alg = LAYERS * (algorithmic_bytes(one, None))
+    tok = decode32_tok_s(args, q, torch, torch.device("cuda", 0), stream)
     emit({"workload": "decode32", "metric": "32-layer decode tok/s (8B shape, q8_0 + r16 on all 224 tensors)",
-          "unit": "tok/s", "value": 1e3 / ms, "ms_per_token": ms, "steps": steps,
-          "effective_gbs": eff / (ms / 1e3) / 1e9,
-          "roofline": hbm_roofline(alg, ms, f"k_dualpath ({LAYERS * len(groups)} launches per token)"),
-          "config": {"base": f"{LAYERS} device copies of the 8B-shape q8_0 layer ({LAYERS * rep.stride / 1e9:.2f} GB)",
-                     "adapter": "r16 s=2.0 on all 224 tensors (one layer's factors repeated)",
-                     "x": "bf16, the same activation per d_in for every layer", "l2": "7.6 GB working set"}})
+          "unit": "tok/s", "value": tok["tok_s"], "ms_per_token": tok["ms_per_token"], "detail": tok,
+          "roofline": tok["roofline"],
+          "config": {"base": tok["base"], "adapter": "r16 s=2.0 on all 224 tensors, own seeds per tensor",
+                     "x": "bf16, the same activation per d_in for every layer", "l2": "7.4 GB working set"}})
 
 
 WORKLOADS["decode32"] = workload_decode32
@@ -833,17 +893,19 @@ def workload_switch(args):
     import torch
     import quantized_base_lora_gb300 as q
     from quantized_base_lora_gb300.runtime import Runtime
+    from synth.stack import stack_adapter
     rt = Runtime(arena_bytes=768 << 20)
-    one, rep = _layers_base(rt, LAYERS)
-    ads = [_LayersAdapter(one, a, RANK, LAYERS) for a in range(4)]
-    bad = bytes([ads[3].digest[0] ^ 0xFF]) + ads[3].digest[1:]
+    stack = load_stack(rt, torch, torch.device("cuda", 0))
+    ads = [stack_adapter(stack, adapter=a, rank=RANK) for a in range(4)]
+    digests = [S.content_digest(ad.payload) for ad in ads]
+    bad = bytes([digests[3][0] ^ 0xFF]) + digests[3][1:]
     lat = {"stage": [], "stage_corrupt": [], "activate": [], "rollback": []}
     status = {}
     handles = []
     torch.cuda.synchronize()
     for a in range(4):
         t0 = time.perf_counter()
-        st, h = rt.stage(ads[a], ads[a].digest if a < 3 else bad)
+        st, h = rt.stage(ads[a], digests[a] if a < 3 else bad)
         lat["stage" if a < 3 else "stage_corrupt"].append(time.perf_counter() - t0)
         status[st] = status.get(st, 0) + 1
         handles.append(h)
@@ -872,8 +934,8 @@ def workload_switch(args):
           "unit": "us", "value": summary["activate"]["p50_us"], "higher_is_better": False,
           "latency": summary, "op_status_counts": st_counts,
           "stage_bytes": int(ads[0].payload.nbytes),
-          "config": {"base": f"{LAYERS} layers of the 8B-shape q8_0 block (device copies)",
-                     "adapters": "4 x r16 on all 224 tensors, a3 declared digest corrupted",
+          "config": {"base": f"{LAYERS} layers of the 8B-shape q8_0 block, every layer its own seeds",
+                     "adapters": "4 x r16 on all 224 tensors (own seeds per tensor), a3 declared digest corrupted",
                      "ops": "100: activate a_(i mod 4) / rollback alternately"}})
 
 
