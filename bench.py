@@ -53,11 +53,10 @@ N_COPIES = 3
 
 
 # DRAM bytes (read + write) per k_dualpath launch of the decode step, mean over
-# its four launches (q+k+v, o, gate+up, down: 28.03 + 18.46 + 127.29 + 63.85 MB
-# per step), measured by ncu with --metrics dram__bytes_read.sum,
-# dram__bytes_write.sum on this workload.  Set to None whenever k_dualpath
-# changes until it is measured again.
-K1_TRAFFIC_PER_LAUNCH = 59_408_736
+# its four launches, measured by ncu with --metrics dram__bytes_read.sum,
+# dram__bytes_write.sum on this workload.  None whenever k_dualpath has changed
+# since the counters were taken, until it is measured again.
+K1_TRAFFIC_PER_LAUNCH = None
 
 
 def peaks():
@@ -286,11 +285,9 @@ def run_ours(args, world, rank, local):
     for rt in rts:
         q.check(q.ovl_check_device(rt.ctx, sh), rt.ctx)
 
-    # ---- end to end through the same C-ABI calls: every step copies its x in
-    # from pinned host memory and its y out to pinned host memory, on a copy
-    # stream, double-buffered and ordered by events, so the copies of one step
-    # overlap the compute of the previous one.
-    e2e_ms, h2d, d2h = e2e_region(torch, step, rts, xs_host, int(y_off[-1]), y_off, stream, dev, args.steps)
+    # ---- end to end through the same C-ABI calls: every step stages its x
+    # from page-locked host memory and its y lands in page-locked host memory
+    e2e_ms, h2d, d2h = e2e_region(torch, q, step, rts, xs_host, int(y_off[-1]), y_off, stream, dev, args.steps)
 
     # ---- tok/s: one decode token through the 32-layer stack of the block,
     # every layer with its own seeds (224 projection calls, 128 launches)
@@ -336,7 +333,10 @@ def run_ours(args, world, rank, local):
                              f"time of the median region, CUDA events on the launching stream (a step is only "
                              f"k_dualpath launches)"},
         "e2e": {"value": world * eff * args.steps / (e2e_max / 1e3) / 1e9, "unit": "GB/s",
-                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "how": "per step: ovl_stage_activations of both activations (page-locked host -> device, one "
+                       "kernel in the programmatic launch chain), then the 4 forward calls with y in page-locked "
+                       f"host memory; median of {REPEATS} regions of {args.steps} steps"},
         "gpu_launches": len(GROUPS) * args.steps * REPEATS,
         "clocks": clocks,
     }
@@ -391,56 +391,40 @@ def timed_regions(one_region, stream, world, repeats=REPEATS):
     return out
 
 
-def e2e_region(torch, step, rts, xs_host, n_y, y_off, stream, dev, steps):
-    """End-to-end ms of `steps` steps: H2D of each step's x from pinned host
-    memory and D2H of its y into pinned host memory on a copy stream, two
-    device buffers of each, ordered by events:
-      copy:    H2D(i+1) after step i-1 freed its x buffer, then D2H(i) after step i;
-      compute: step i after H2D(i) and after D2H(i-2) freed its y buffer."""
-    copy = torch.cuda.Stream(device=dev)
-    x_pin = {d: torch.from_numpy(v.view(np.int16)).pin_memory() for d, v in xs_host.items()}
-    x_dev = [{d: torch.empty(v.shape, dtype=torch.int16, device=dev) for d, v in xs_host.items()} for _ in range(2)]
-    y_dev = [torch.empty(n_y, dtype=torch.float32, device=dev) for _ in range(2)]
+def e2e_region(torch, q, step, rts, xs_host, n_y, y_off, stream, dev, steps):
+    """End-to-end ms of `steps` steps through the public C ABI: every step
+    stages its activations (both d_in, one page-locked host buffer) into the
+    device with ovl_stage_activations, whose kernel joins the programmatic
+    launch chain, and the step's calls write y straight into page-locked host
+    memory (two host buffers, alternating)."""
+    x_cat = np.concatenate([xs_host[d].reshape(-1) for d in (4096, 14336)])
+    x_pin = torch.from_numpy(x_cat.view(np.int16)).pin_memory()
+    x_dev = torch.empty(x_pin.shape, dtype=torch.int16, device=dev)
     y_pin = [torch.empty(n_y, dtype=torch.float32).pin_memory() for _ in range(2)]
-    x_addr = [{d: v.data_ptr() for d, v in xb.items()} for xb in x_dev]
-    y_ptr = [[yb.data_ptr() + 4 * int(y_off[i]) for i in range(len(y_off) - 1)] for yb in y_dev]
-    ev_x = [torch.cuda.Event() for _ in range(2)]
-    ev_y = [torch.cuda.Event() for _ in range(2)]
-    ev_out = [torch.cuda.Event() for _ in range(2)]
-    h2d = sum(v.nbytes for v in xs_host.values())
+    x_addr = {4096: x_dev.data_ptr(), 14336: x_dev.data_ptr() + 4096 * 2}
+    y_ptr = [[yb.data_ptr() + 4 * int(y_off[i]) for i in range(len(y_off) - 1)] for yb in y_pin]
+    h2d = x_cat.nbytes
     d2h = n_y * 4
+    sh = int(stream.cuda_stream)
 
-    def h2d_copy(i):
-        b = i % 2
-        if i >= 2:
-            copy.wait_event(ev_y[b])              # step i-2 has read x buffer b
-        with torch.cuda.stream(copy):
-            for d in x_dev[b]:
-                x_dev[b][d].copy_(x_pin[d], non_blocking=True)
-        ev_x[b].record(copy)
+    def one(i):
+        st = q.ovl_stage_activations(x_dev.data_ptr(), x_pin.data_ptr(), h2d, sh)
+        if st != 0:
+            raise q.OvlError(st, "stage activations")
+        step(rts[i % len(rts)], x_addr, y_ptr[i % 2])
 
-    torch.cuda.synchronize()
-    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record(copy)
-    h2d_copy(0)
-    for i in range(steps):
-        b = i % 2
-        stream.wait_event(ev_x[b])
-        if i >= 2:
-            stream.wait_event(ev_out[b])          # y buffer b copied out by D2H(i-2)
+    with torch.cuda.stream(stream):
+        for i in range(3):
+            one(i)
+    stream.synchronize()
+
+    def region(r):
         with torch.cuda.stream(stream):
-            step(rts[i % len(rts)], x_addr[b], y_ptr[b])
-        ev_y[b].record(stream)
-        if i + 1 < steps:
-            h2d_copy(i + 1)
-        copy.wait_event(ev_y[b])
-        with torch.cuda.stream(copy):
-            y_pin[b].copy_(y_dev[b], non_blocking=True)
-        ev_out[b].record(copy)
-    e1.record(copy)
-    copy.synchronize()
-    torch.cuda.synchronize()
-    return e0.elapsed_time(e1), h2d, d2h
+            for i in range(steps):
+                one(r * steps + i)
+
+    ms = timed_regions(region, stream, 1)
+    return statistics.median(ms), h2d, d2h
 
 
 def decode32_tok_s(args, q, torch, dev, stream):

@@ -359,6 +359,24 @@ ovl_status ovl_dualpath_forward_noalloc(const void* qs, const void* d, uint32_t 
                                         const uint32_t* rank, const float* scale, uint32_t n_terms,
                                         const void* x, uint32_t x_dtype, uint32_t T, float* y, void* stream);
 
+/* Copy one decode step's activations from page-locked host memory into device
+ * memory inside the stream's programmatic launch chain.  No counterpart in the
+ * source pages: a runtime helper for decode loops around the dual-path calls.
+ * A plain host-to-device copy between two forwards makes the next launch wait
+ * for the copy engine and start cold; this call's kernel reads `src_host`
+ * before its grid dependency resolves, lets the next launch's CTAs start
+ * streaming weights at once, and writes `dst` only after the preceding kernel
+ * on `stream` has completed (so it never overwrites activations that earlier
+ * kernels still read).  src_host: page-locked (registered) host memory, or
+ * device or managed memory; dst: device (or managed or page-locked) memory;
+ * nbytes: any size, with dst and src_host equally aligned modulo 16.  The call
+ * allocates nothing; the caller keeps both buffers unchanged until the copy
+ * has run.  Errors: OVL_E_ARG (null pointer, pageable host memory, different
+ * alignment modulo 16), OVL_E_CUDA.  nbytes = 0 is a no-op.  The forward calls
+ * also accept page-locked host memory for y: the kernels then write each
+ * output straight to the host. */
+ovl_status ovl_stage_activations(void* dst, const void* src_host, size_t nbytes, void* stream);
+
 /* Recompute the content digest of the base's device bytes now (device leaf
  * hashing on `stream`, synchronizes).  Used to check that the base stays
  * bit-identical across switches ([DTD] §2 Oracle Invariant). */

@@ -107,6 +107,7 @@ def _load():
         "ovl_version": ([], C.c_char_p),
         "ovl_dualpath_forward_noalloc": ([P, P, U32, U32, U32, C.POINTER(P), C.POINTER(P), C.POINTER(U32),
                                           C.POINTER(C.c_float), U32, P, U32, U32, P, P], I32),
+        "ovl_stage_activations": ([P, P, SZ, P], I32),
     }
     for name, (args, res) in sig.items():
         fn = getattr(lib, name)
@@ -120,7 +121,7 @@ EXPORTED = ("ovl_create", "ovl_destroy", "ovl_load_base", "ovl_stage_adapter", "
             "ovl_activate", "ovl_rollback", "ovl_linear_forward", "ovl_linear_forward_multi", "ovl_materialize_layer",
             "ovl_segmented_forward", "ovl_base_digest", "ovl_get_state", "ovl_get_entry",
             "ovl_check_device", "ovl_debug_inject", "ovl_last_error", "ovl_sha256",
-            "ovl_content_digest", "ovl_version", "ovl_dualpath_forward_noalloc")
+            "ovl_content_digest", "ovl_version", "ovl_dualpath_forward_noalloc", "ovl_stage_activations")
 
 
 class OvlError(RuntimeError):
@@ -297,6 +298,10 @@ def ovl_check_device(ctx, stream: int = 0) -> int:
 
 def ovl_debug_inject(ctx, phase: int, code: int) -> int:
     return lib.ovl_debug_inject(ctx, int(phase), int(code))
+
+
+def ovl_stage_activations(dst_ptr: int, src_host_ptr: int, nbytes: int, stream: int = 0) -> int:
+    return lib.ovl_stage_activations(C.c_void_p(dst_ptr), C.c_void_p(src_host_ptr), int(nbytes), C.c_void_p(stream))
 
 
 def ovl_dualpath_forward_noalloc(qs_ptr: int, d_ptr: int, quant: int, d_out: int, d_in: int, A_ptrs, B_ptrs,
