@@ -56,7 +56,7 @@ N_COPIES = 3
 # its four launches, measured by ncu with --metrics dram__bytes_read.sum,
 # dram__bytes_write.sum on this workload.  None whenever k_dualpath has changed
 # since the counters were taken, until it is measured again.
-K1_TRAFFIC_PER_LAUNCH = None
+K1_TRAFFIC_PER_LAUNCH = 59_420_384
 
 
 def peaks():
@@ -564,6 +564,35 @@ def _check_all(rts, sh):
         q.check(q.ovl_check_device(rt.ctx, sh), rt.ctx)
 
 
+def workload_decode_block(args):
+    """The headline decode step alone (the 8B-shape q8_0 block + rank-16 LoRA,
+    three base copies rotated, activations device-resident): no 32-layer,
+    end-to-end or CPU legs.  Small enough to run under a profiler."""
+    import torch
+    import quantized_base_lora_gb300 as q
+    base = S.block_base(S.Q8_0)
+    ad = S.block_adapter(base, adapter=0, rank=RANK)
+    rts = _contexts(base, [ad], [SCALE], N_COPIES, 64)
+    stream = torch.cuda.Stream()
+    sh = int(stream.cuda_stream)
+    xs = {d: torch.from_numpy(S.to_bf16_bits(S.activations(1, d)).view(np.int16)).cuda().view(torch.bfloat16)
+          for d in (4096, 14336)}
+    ys = [torch.empty((1, t.d_out), dtype=torch.float32, device="cuda") for t in base.tensors]
+    step = block_step(q, base.tensors, sh)
+    x_addr = {d: v.data_ptr() for d, v in xs.items()}
+    y_ptr = [y.data_ptr() for y in ys]
+    ms = timed_steps(lambda i: step(rts[i % N_COPIES], x_addr, y_ptr), args.steps, args.warmup, stream)
+    _check_all(rts, sh)
+    alg = algorithmic_bytes(base, ad)
+    emit({"workload": "decode-block", "metric": METRIC, "unit": "GB/s",
+          "value": effective_bytes(base, ad) / (ms / 1e3) / 1e9, "ms_per_step": ms, "steps": args.steps,
+          "roofline": hbm_roofline(alg, ms, "k_dualpath (4 launches per step)"),
+          "config": {"workload": WORKLOAD, "l2": f"{N_COPIES} base copies rotated"}})
+
+
+WORKLOADS["decode-block"] = workload_decode_block
+
+
 def workload_q4_stacked(args):
     import torch
     base = S.block_base(S.Q4_0)
@@ -763,6 +792,7 @@ def workload_prefill_dual(args):
                                  "note": f"peak = {tkind}"}}
     emit({"workload": "prefill-dual", "metric": "dual-path multi-token step (8B shape, q8_0 + r16, tensor cores)",
           "unit": "tok/s", "value": per_T[64]["tok_s"], "per_T": per_T, "steps": args.steps,
+          "tf32_cublas_tflops_8192cube": tf32_cublas_tflops(),
           "config": {"base": "8B-shape block q8_0 (231.7 MB)", "adapter": "r16 s=2.0 on all 7", "x": "bf16",
                      "T": [64, 256, 512], "l2": f"{N_COPIES} base copies rotated"}})
 
@@ -771,14 +801,47 @@ WORKLOADS["prefill-dual"] = workload_prefill_dual
 
 
 def tf32_peak():
-    """Dense TF32 tensor peak: the measured bf16 GEMM peak x the nominal
-    tf32/bf16 ratio (1.1 / 2.25 PFLOP/s)."""
+    """Dense TF32 tensor peak for the roofline: the measured bf16 GEMM burst peak
+    (MEASURED_PEAKS.json) x the nominal dense tf32/bf16 ratio of GB300 (1.1 / 2.25
+    PFLOP/s, the profiling recipe's table), as the recipe prescribes for a
+    contraction in a dtype the peaks file does not carry."""
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
             p = json.load(f)
-        return float(p["bf16_tflops"]) * 1.1 / 2.25, "measured bf16 x nominal tf32/bf16"
+        return float(p["bf16_tflops"]) * 1.1 / 2.25, "measured bf16 burst x nominal tf32/bf16 (1.1/2.25)"
     except Exception:
-        return 1900.0 * 1.1 / 2.25, "fallback bf16 x nominal tf32/bf16"
+        return 1900.0 * 1.1 / 2.25, "fallback bf16 x nominal tf32/bf16 (1.1/2.25)"
+
+
+_TF32_MEASURED = {}
+
+
+def tf32_cublas_tflops(m=8192, n=8192, k=8192):
+    """A torch (cuBLAS) TF32 matmul of m x k by k x n on this GPU, best of 5
+    after warm-up: context for the derived TF32 peak, not its denominator."""
+    if (m, n, k) in _TF32_MEASURED:
+        return _TF32_MEASURED[(m, n, k)]
+    import torch
+    old = torch.backends.cuda.matmul.allow_tf32
+    torch.backends.cuda.matmul.allow_tf32 = True
+    try:
+        a = torch.randn(m, k, device="cuda")
+        b = torch.randn(k, n, device="cuda")
+        for _ in range(3):
+            torch.matmul(a, b)
+        best = float("inf")
+        for _ in range(5):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            torch.matmul(a, b)
+            e1.record()
+            torch.cuda.synchronize()
+            best = min(best, e0.elapsed_time(e1))
+        del a, b
+    finally:
+        torch.backends.cuda.matmul.allow_tf32 = old
+    _TF32_MEASURED[(m, n, k)] = 2.0 * m * n * k / (best / 1e3) / 1e12
+    return _TF32_MEASURED[(m, n, k)]
 
 
 def workload_jit_prefill(args):
@@ -821,6 +884,8 @@ def workload_jit_prefill(args):
     emit({"workload": "jit-prefill", "metric": "per-layer JIT prefill time (8B-shape q8_0 layer + r16, T=512)",
           "unit": "ms", "value": ms, "higher_is_better": False, "steps": steps,
           "tok_s": T / (ms / 1e3), "gemm_tflops": gemm_flop / (ms / 1e3) / 1e12,
+          "tf32_cublas_tflops_8192cube": tf32_cublas_tflops(),
+          "tf32_cublas_tflops_prefill_shape": tf32_cublas_tflops(512, 14336, 4096),
           "roofline": {"bound": "tensor" if t_tc > t_mem else "hbm",
                        "ideal_ms_hbm": t_mem, "ideal_ms_tensor": t_tc, "frac": max(t_mem, t_tc) / ms,
                        "algorithmic_bytes": alg_bytes, "gemm_flop": gemm_flop, "merge_flop": merge_flop,
