@@ -52,7 +52,7 @@ constexpr int kRecBytes = 112;  // per (token, block) activation record: 7 x 16 
 #define OVL_K1_MAX_NS 8
 #endif
 #ifndef OVL_K1_SOFT_BYTES
-#define OVL_K1_SOFT_BYTES (113 * 1024)
+#define OVL_K1_SOFT_BYTES (150 * 1024)
 #endif
 #ifndef OVL_K1_STAGE_BYTES
 #define OVL_K1_STAGE_BYTES 16384
@@ -64,17 +64,20 @@ constexpr int kRecBytes = 112;  // per (token, block) activation record: 7 x 16 
 #define OVL_K1_MAX_GROUPS 4
 #endif
 constexpr int kMaxNS = OVL_K1_MAX_NS;
-constexpr int kMaxThreads = 10 * 32;       // up to 8 consumer warps + producer + helper
+constexpr int kMaxThreads = 18 * 32;       // up to 16 consumer warps + producer + helper
 
-// Every variant fits two CTAs per SM (registers, and shared memory for the
-// plans under the soft budget), so a CTA of the next launch is resident and
-// streaming its weights while this grid drains.  Variants that stream at most
-// two rows per stage serve wide rows (d_in >= 8K for q8_0) and keep two
-// activation records per lane in registers.
+// One CTA per SM: its ring (up to 150 KB of shared memory) is as deep as the
+// SM's memory latency needs, and registers are not capped for a second CTA.
+// Measured on the 8B-shape decode step, one deep ring per SM beat two
+// co-resident CTAs of consecutive launches with half the ring each (the next
+// launch's CTA still becomes resident on each SM as soon as this grid's CTA
+// there exits, and streams its ring while the rest of the grid drains).
+// Variants that stream at most two rows per stage serve wide rows (d_in >= 8K
+// for q8_0) and keep two activation records per lane in registers.
 template <int TT, int RG>
 struct K1Shape {
   static constexpr int threads = kMaxThreads;
-  static constexpr int min_blocks = 2;
+  static constexpr int min_blocks = 1;
   static constexpr int reg_records = (RG <= 2 && TT == 1) ? 2 : 1;
 };
 constexpr uint32_t reg_records_of(int tt, int rg) { return (rg <= 2 && tt == 1) ? 2u : 1u; }
@@ -1297,10 +1300,11 @@ int device_sms() {
   return n > 0 ? n : 1;
 }
 
-// Shared-memory plan for one launch; returns false if it cannot fit.  A plan
-// under kSoftBudget leaves room for a CTA of the next launch on the same SM,
-// which then prefetches its weights while this grid drains.
-// Two CTAs of 113 KB plus the 1 KB the SM reserves per CTA fill its 228 KB.
+// Shared-memory plan for one launch; returns false if it cannot fit.  The
+// soft budget (150 KB) sizes the ring: 8 stages of 4 rows for d_in = 4096,
+// 4 stages of 2 rows for d_in = 14336 (q8_0).  Deeper rings (10 and 6 stages)
+// and mixed plans where only some consecutive launches fit side by side on
+// an SM measured slower.
 constexpr uint32_t kSoftBudget = OVL_K1_SOFT_BYTES;
 
 bool plan(DualCfg& c, const DualArgs& a, int tt, int rg, uint32_t rows_max, uint32_t b_need) {
