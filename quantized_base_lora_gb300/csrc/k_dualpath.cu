@@ -1370,7 +1370,7 @@ cudaError_t launch_dualpath(const DualArgs& a_in, cudaStream_t st) {
   c.rowbytes = a0.quant == OVL_Q8_0 ? a0.n : a0.n / 2;
   // column warps: fewest blocks per lane, then fewest idle lanes
   uint32_t best_w = 1, best_b = 0, best_waste = ~0u;
-  for (uint32_t w = 1; w <= 8; ++w) {
+  for (uint32_t w = 1; w <= kMaxThreads / 32 - 2; ++w) {
     const uint32_t b = (c.nb + 32 * w - 1) / (32 * w);
     const uint32_t waste = b * 32 * w - c.nb;
     if (best_b == 0 || b < best_b || (b == best_b && waste < best_waste)) {
