@@ -125,6 +125,7 @@ enum {                                                /* activation phases ([DTD
   OVL_PHASE_DEVICE_WAIT = 6   /* a bounded device-side wait of the next decode launch (tests) */
 };
 
+enum { OVL_ADAPTER_LORA = 1, OVL_ADAPTER_SPARSE = 2 };/* adapter type in a manifest */
 enum {
   OVL_MAX_STACK = 8,          /* adapters in one STACK composition */
   OVL_MAX_TABLE = 32,         /* slots in one TABLE composition */
@@ -171,6 +172,24 @@ typedef struct {
   float scale;
   uint32_t total_rank;        /* sum of ranks over the adapter's targets */
 } ovl_entry;
+
+typedef struct {
+  char name[64];                    /* NUL-terminated */
+  uint8_t file_digest[32];          /* content digest of the adapter's payload */
+  uint8_t required_base_digest[32]; /* valid when has_required_base */
+  uint32_t type;                    /* OVL_ADAPTER_LORA or OVL_ADAPTER_SPARSE */
+  uint32_t load_order;
+  uint32_t rank;                    /* 0 = not given */
+  uint32_t n_targets;               /* 0 = not given */
+  uint32_t has_required_base;
+  float merge_weight;               /* binary32, the entry's scale */
+} ovl_manifest_entry;
+
+typedef struct {
+  uint8_t base_digest[32];
+  uint32_t quant, mode, n_adapters;
+  ovl_manifest_entry adapters[OVL_MAX_TABLE];   /* in increasing load_order */
+} ovl_manifest;
 
 /* Create a context on CUDA device `device` over a caller-owned device arena of
  * arena_bytes bytes (>= 16 MiB, 256-byte aligned).  The arena holds the device
@@ -377,6 +396,45 @@ ovl_status ovl_dualpath_forward_noalloc(const void* qs, const void* d, uint32_t 
  * output straight to the host. */
 ovl_status ovl_stage_activations(void* dst, const void* src_host, size_t nbytes, void* stream);
 
+/* Composition manifest ([OVR] §"Composition Identity and Manifest Schema":
+ * base model hash, quantization profile, runtime tag and the ordered adapter
+ * list with name, file hash, load order and merge weight; [DTD] §11
+ * AdapterManifestV0: adapter type, rank, required base checksum).  The
+ * document is one strict JSON object (UTF-8, at most 1 MiB, no comments, no
+ * duplicate keys; any key not listed is an error):
+ *   "base_model_hash": "sha256:<64 lowercase hex>"          required
+ *   "quantization":    "q8_0" | "q4_0" | "q4_K"             required
+ *   "runtime":         {"name": "ovl-gb300", "version": "v1"} optional; another value is version skew
+ *   "mode":            "stack" | "table"                     optional, default "stack"
+ *   "tokenizer_id", "timestamp_utc": strings                 optional, informational
+ *   "adapters": [ { "name": 1..63 bytes, unique;  "file_hash": "sha256:<hex>", unique;
+ *                   "load_order": integer 1..2^31-1, unique;  "merge_weight": number;
+ *                   "type": "lora" (default) | "sparse";  "rank": integer;
+ *                   "required_base_hash": "sha256:<hex>";  "targets": [tensor index, ...] } ]
+ * The adapters apply in increasing load_order with scale = merge_weight
+ * rounded to binary32.  Parsing needs no device.
+ * Errors: OVL_E_ARG (not JSON, missing or malformed field, unknown field,
+ * ambiguous load_order, non-finite weight, runtime skew, more than
+ * OVL_MAX_TABLE adapters), OVL_E_QUANT (unknown quantization profile),
+ * OVL_E_DUPLICATE (a name or file_hash listed twice).  The message is read
+ * with ovl_last_error(NULL). */
+ovl_status ovl_manifest_parse(const char* text, size_t len, ovl_manifest* out);
+
+/* Activate the composition a manifest describes: each adapter is found among
+ * the context's staged adapters by its payload content digest (the content
+ * address), then activated in load order with its merge weight, exactly as
+ * ovl_activate would (same composition id, idempotency, rollback slot, busy
+ * policy).  Checked against the context before anything changes:
+ * base_model_hash against the loaded base (OVL_E_HASH), quantization against
+ * its profile (OVL_E_QUANT), a file_hash with no staged adapter (OVL_E_HASH),
+ * the staged adapter's type (OVL_E_ARG), rank (every target, OVL_E_SHAPE),
+ * targets (same tensors in the same order, OVL_E_SHAPE) and
+ * required_base_hash (OVL_E_HASH).  Any failure, at parsing or later, leaves
+ * the active composition and the rollback slot unchanged ([OVR] §"TDD and
+ * Fault-Injection Matrix": malformed manifests and wrong hashes are rejected
+ * deterministically with no state change). */
+ovl_status ovl_activate_manifest(ovl_ctx* ctx, const char* text, size_t len, uint8_t composition_id_out[32]);
+
 /* Recompute the content digest of the base's device bytes now (device leaf
  * hashing on `stream`, synchronizes).  Used to check that the base stays
  * bit-identical across switches ([DTD] §2 Oracle Invariant). */
@@ -411,7 +469,8 @@ ovl_status ovl_check_device(ovl_ctx* ctx, void* stream);
 ovl_status ovl_debug_inject(ovl_ctx* ctx, uint32_t phase, ovl_status code);
 
 /* Message of the last failed call on ctx (static storage owned by ctx; "" after
- * success).  ctx NULL returns the message of the last failed ovl_create.
+ * success).  ctx NULL returns the message of the last failed call that has no
+ * context on this thread (ovl_create, ovl_manifest_parse).
  * ([MODELD] §"Observability": why an adapter failed to load.) */
 const char* ovl_last_error(ovl_ctx* ctx);
 

@@ -38,6 +38,7 @@ OVL_F32, OVL_BF16 = 1, 2
 OVL_MODE_STACK, OVL_MODE_TABLE = 1, 2
 OVL_PATH_DUAL, OVL_PATH_JIT = 1, 2
 OVL_SWITCH_REJECT, OVL_SWITCH_DRAIN = 1, 2
+OVL_ADAPTER_LORA, OVL_ADAPTER_SPARSE = 1, 2
 (OVL_PHASE_VALIDATION, OVL_PHASE_ALLOCATION, OVL_PHASE_STAGING,
  OVL_PHASE_CHECKSUM, OVL_PHASE_SWAP, OVL_PHASE_DEVICE_WAIT) = 1, 2, 3, 4, 5, 6
 OVL_MAX_STACK, OVL_MAX_TABLE, OVL_MAX_RANK, OVL_MAX_TOTAL_RANK, OVL_MAX_T, OVL_MAX_SEGMENTS = 8, 32, 128, 256, 512, 64
@@ -76,6 +77,17 @@ class ovl_entry(C.Structure):
                 ("total_rank", C.c_uint32)]
 
 
+class ovl_manifest_entry(C.Structure):
+    _fields_ = [("name", C.c_char * 64), ("file_digest", C.c_uint8 * 32), ("required_base_digest", C.c_uint8 * 32),
+                ("type", C.c_uint32), ("load_order", C.c_uint32), ("rank", C.c_uint32), ("n_targets", C.c_uint32),
+                ("has_required_base", C.c_uint32), ("merge_weight", C.c_float)]
+
+
+class ovl_manifest(C.Structure):
+    _fields_ = [("base_digest", C.c_uint8 * 32), ("quant", C.c_uint32), ("mode", C.c_uint32),
+                ("n_adapters", C.c_uint32), ("adapters", ovl_manifest_entry * 32)]
+
+
 def _load():
     if not os.path.exists(LIB_PATH):
         raise ImportError(f"libovl.so is not built ({LIB_PATH}); run python quantized_base_lora_gb300/build.py")
@@ -108,6 +120,8 @@ def _load():
         "ovl_dualpath_forward_noalloc": ([P, P, U32, U32, U32, C.POINTER(P), C.POINTER(P), C.POINTER(U32),
                                           C.POINTER(C.c_float), U32, P, U32, U32, P, P], I32),
         "ovl_stage_activations": ([P, P, SZ, P], I32),
+        "ovl_manifest_parse": ([C.c_char_p, SZ, C.POINTER(ovl_manifest)], I32),
+        "ovl_activate_manifest": ([P, C.c_char_p, SZ, B32], I32),
     }
     for name, (args, res) in sig.items():
         fn = getattr(lib, name)
@@ -121,7 +135,8 @@ EXPORTED = ("ovl_create", "ovl_destroy", "ovl_load_base", "ovl_stage_adapter", "
             "ovl_activate", "ovl_rollback", "ovl_linear_forward", "ovl_linear_forward_multi", "ovl_materialize_layer",
             "ovl_segmented_forward", "ovl_base_digest", "ovl_get_state", "ovl_get_entry",
             "ovl_check_device", "ovl_debug_inject", "ovl_last_error", "ovl_sha256",
-            "ovl_content_digest", "ovl_version", "ovl_dualpath_forward_noalloc", "ovl_stage_activations")
+            "ovl_content_digest", "ovl_version", "ovl_dualpath_forward_noalloc", "ovl_stage_activations",
+            "ovl_manifest_parse", "ovl_activate_manifest")
 
 
 class OvlError(RuntimeError):
@@ -298,6 +313,31 @@ def ovl_check_device(ctx, stream: int = 0) -> int:
 
 def ovl_debug_inject(ctx, phase: int, code: int) -> int:
     return lib.ovl_debug_inject(ctx, int(phase), int(code))
+
+
+def ovl_manifest_parse(text):
+    """Parse a composition manifest (str or bytes) without a device: (status,
+    dict with base_digest, quant, mode and the adapters in load order)."""
+    raw = text.encode() if isinstance(text, str) else bytes(text)
+    m = ovl_manifest()
+    st = lib.ovl_manifest_parse(raw, len(raw), C.byref(m))
+    if st != 0:
+        return st, None
+    ads = []
+    for i in range(m.n_adapters):
+        e = m.adapters[i]
+        ads.append({"name": e.name.decode(), "file_digest": bytes(e.file_digest), "type": e.type,
+                    "load_order": e.load_order, "merge_weight": e.merge_weight, "rank": e.rank,
+                    "n_targets": e.n_targets,
+                    "required_base_digest": bytes(e.required_base_digest) if e.has_required_base else None})
+    return st, {"base_digest": bytes(m.base_digest), "quant": m.quant, "mode": m.mode, "adapters": ads}
+
+
+def ovl_activate_manifest(ctx, text):
+    raw = text.encode() if isinstance(text, str) else bytes(text)
+    out = _b32()
+    st = lib.ovl_activate_manifest(ctx, raw, len(raw), out)
+    return st, bytes(out)
 
 
 def ovl_stage_activations(dst_ptr: int, src_host_ptr: int, nbytes: int, stream: int = 0) -> int:

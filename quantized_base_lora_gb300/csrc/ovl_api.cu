@@ -174,6 +174,15 @@ namespace {
 
 thread_local std::string g_create_err;
 
+}  // namespace
+
+void set_context_free_error(const std::string& msg) { g_create_err = msg; }
+
+ovl_status activate_locked(ovl_ctx* ctx, const ovl_adapter_h* h, const float* scale, uint32_t n, uint32_t mode,
+                           uint8_t composition_id_out[32]);
+
+namespace {
+
 // Makes `dev` current for the scope of a call and restores the caller's device.
 struct DeviceGuard {
   int prev = -1;
@@ -645,6 +654,59 @@ ovl_status ovl_activate(ovl_ctx* ctx, const ovl_adapter_h* h, const float* scale
                         uint8_t composition_id_out[32]) {
   if (!ctx) return OVL_E_ARG;
   std::lock_guard<std::mutex> lk(ctx->mu);
+  return ovl::activate_locked(ctx, h, scale, n, mode, composition_id_out);
+}
+
+ovl_status ovl_activate_manifest(ovl_ctx* ctx, const char* text, size_t len, uint8_t composition_id_out[32]) {
+  using namespace ovl;
+  if (!ctx) return OVL_E_ARG;
+  std::lock_guard<std::mutex> lk(ctx->mu);
+  Manifest m;
+  std::string err;
+  if (ovl_status st = parse_manifest(text, len, &m, &err)) return fail(ctx, st, err);
+  if (!ctx->base_loaded) return fail(ctx, OVL_E_STATE, "no base loaded");
+  if (std::memcmp(m.base_hash, ctx->base_digest, 32) != 0)
+    return fail(ctx, OVL_E_HASH, "base_model_hash is not the loaded base's digest");
+  if (m.quant != ctx->quant) return fail(ctx, OVL_E_QUANT, "quantization is not the loaded base's profile");
+  std::vector<ovl_adapter_h> hs;
+  std::vector<float> ws;
+  for (const ManifestAdapter& e : m.adapters) {
+    const Adapter* found = nullptr;   // staged adapters in increasing handle order
+    for (const auto& kv : ctx->staged)
+      if (std::memcmp(kv.second.digest, e.file_hash, 32) == 0) {
+        found = &kv.second;
+        break;
+      }
+    const std::string who = "adapter \"" + e.name + "\": ";
+    if (!found) return fail(ctx, OVL_E_HASH, who + "no staged adapter has this file_hash");
+    if (found->sparse != (e.type == OVL_ADAPTER_SPARSE))
+      return fail(ctx, OVL_E_ARG, who + "type does not match the staged adapter");
+    if (e.rank)
+      for (const Target& t : found->targets)
+        if (t.rank != e.rank) return fail(ctx, OVL_E_SHAPE, who + "rank does not match the staged adapter");
+    if (e.has_targets) {
+      std::vector<uint32_t> got;
+      if (found->sparse)
+        for (const SparseTarget& t : found->sp) got.push_back(t.tensor);
+      else
+        for (const Target& t : found->targets) got.push_back(t.tensor);
+      if (got != e.targets) return fail(ctx, OVL_E_SHAPE, who + "targets do not match the staged adapter");
+    }
+    if (e.has_required_base && std::memcmp(e.required_base, ctx->base_digest, 32) != 0)
+      return fail(ctx, OVL_E_HASH, who + "required_base_hash is not the loaded base's digest");
+    hs.push_back(found->h);
+    ws.push_back(e.merge_weight);
+  }
+  return activate_locked(ctx, hs.data(), ws.data(), static_cast<uint32_t>(hs.size()), m.mode, composition_id_out);
+}
+
+}  // extern "C"
+
+namespace ovl {
+
+// The body of ovl_activate with the context's lock held.
+ovl_status activate_locked(ovl_ctx* ctx, const ovl_adapter_h* h, const float* scale, uint32_t n, uint32_t mode,
+                           uint8_t composition_id_out[32]) {
   if (ovl_status s = injected(ctx, OVL_PHASE_VALIDATION)) return s;
   if (!ctx->base_loaded) return fail(ctx, OVL_E_STATE, "no base loaded");
   if (n && (!h || !scale)) return fail(ctx, OVL_E_ARG, "null argument");
@@ -685,6 +747,10 @@ ovl_status ovl_activate(ovl_ctx* ctx, const ovl_adapter_h* h, const float* scale
   if (composition_id_out) std::memcpy(composition_id_out, comp->id, 32);
   return ok(ctx);
 }
+
+}  // namespace ovl
+
+extern "C" {
 
 ovl_status ovl_rollback(ovl_ctx* ctx, uint8_t composition_id_out[32]) {
   if (!ctx) return OVL_E_ARG;

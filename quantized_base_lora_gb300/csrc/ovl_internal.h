@@ -5,6 +5,9 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include <string>
+#include <vector>
+
 #include "../../include/ovl.h"
 
 namespace ovl {
@@ -184,6 +187,31 @@ cudaError_t launch_leaf_digests(const uint8_t* data, size_t n, uint8_t* leaf_dig
                                 cudaStream_t st);
 // Scan `n` fp32 values at `p`; increments *flag (device) if any is NaN/Inf.
 cudaError_t launch_finite_scan(const float* p, size_t n, uint32_t* flag, cudaStream_t st);
+
+// A parsed composition manifest (ovl_manifest.cu): adapters in increasing
+// load_order.
+struct ManifestAdapter {
+  std::string name;
+  uint8_t file_hash[32] = {};
+  uint32_t type = OVL_ADAPTER_LORA;
+  uint32_t load_order = 0;
+  float merge_weight = 0.f;
+  uint32_t rank = 0;                 // 0: not given
+  bool has_required_base = false;
+  uint8_t required_base[32] = {};
+  bool has_targets = false;
+  std::vector<uint32_t> targets;
+};
+struct Manifest {
+  uint8_t base_hash[32] = {};
+  uint32_t quant = 0, mode = OVL_MODE_STACK;
+  std::vector<ManifestAdapter> adapters;
+};
+constexpr const char* kManifestRuntimeName = "ovl-gb300";
+constexpr const char* kManifestRuntimeVersion = "v1";
+ovl_status parse_manifest(const char* text, size_t len, Manifest* out, std::string* err);
+// Message returned by ovl_last_error(NULL) (failures that have no context).
+void set_context_free_error(const std::string& msg);
 
 // Host-side digests (library's own SHA-256).
 void host_sha256(const void* data, size_t n, uint8_t out[32]);
