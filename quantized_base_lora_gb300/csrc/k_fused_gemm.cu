@@ -59,9 +59,11 @@ constexpr uint32_t kDGroup = 8;           // K-blocks per code group (two stages
 constexpr uint32_t kDBytes = BM * kDGroup * 2;   // one scale tile: 128 rows x 8 f16
 // One thread can issue a tcgen05.mma only every ~110 cycles, while an M = 128,
 // N = 64, K = 8 tf32 MMA takes the tensor core ~37: several issuing threads,
-// each with its own accumulator over its own share of K, keep it busy.
-constexpr uint32_t kIssuers = 4;          // MMA-issuing threads (lane 0 of warps 1 .. kIssuers)
-constexpr uint32_t kKbPerIssuer = kSub / kIssuers;
+// each with its own accumulator over its own share of K, keep it busy.  With
+// 128-token chunks (N = 128, ~74 cycles an MMA) two issuers suffice, and each
+// dequantized weight feeds twice the multiply-adds.
+constexpr uint32_t kIssuers = 4;          // MMA-issuing warps (lane 0 of warps 1 .. kIssuers); a launch uses nis
+constexpr uint32_t kWideTile = 128;       // token chunk of the two-issuer form
 constexpr uint32_t kTmemCols = 512;       // accumulators (bn columns each), then the stages' weight operands
 constexpr uint32_t kMaxStages = 3;
 constexpr uint32_t kMaxGroups = 4;
@@ -73,6 +75,7 @@ constexpr uint32_t kThreads = (kGroupWarp + 1) * 32;   // producer, MMA issuers,
 constexpr uint32_t kTimeoutFused = 5;
 static_assert(kSub % kIssuers == 0, "stage split");
 static_assert(kIssuers * kTokTile + 2 * kStageCols <= kTmemCols, "TMEM budget: two stages at the widest token tile");
+static_assert(2 * kWideTile + 2 * kStageCols <= kTmemCols, "TMEM budget: two stages, two issuers at 128 tokens");
 
 constexpr uint32_t kMaxFusedTensors = 4;   // tensors sharing x in one launch (q+k+v, gate+up)
 
@@ -95,9 +98,10 @@ struct FusedMaps {
 struct FusedArgs {
   uint32_t nt;              // tensors in this launch
   uint32_t n, T, quant;
-  uint32_t bn;            // UMMA N (multiple of 16, <= kTokTile)
+  uint32_t bn;            // UMMA N (multiple of 16, <= kWideTile)
+  uint32_t nis;           // MMA issuers: 4 (bn <= 64) or 2 (bn up to 128); each owns kSub / nis K-blocks
   uint32_t ns;            // pipeline stages (activation tiles + TMEM weight operands)
-  uint32_t acol;          // first TMEM column of the weight operands: kIssuers bn
+  uint32_t acol;          // first TMEM column of the weight operands: nis bn
   uint32_t ng;            // code-group buffers
   uint32_t kblocks;       // n / 32
   uint32_t splits;        // CTAs (one cluster) sharing a row tile, each with kbs K-blocks
@@ -235,15 +239,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 32) {
     for (uint32_t i = 0; i < g.ns; ++i) {
       mbar_init(&full[i], 1);
-      mbar_init(&empty[i], kIssuers);    // one commit per issuer
-      for (uint32_t w = 0; w < kIssuers; ++w)
-        mbar_init(&conv[w * kMaxStages + i], kConvWarps / kIssuers);   // the converters of its K-blocks
+      mbar_init(&empty[i], g.nis);    // one commit per issuer
+      for (uint32_t w = 0; w < g.nis; ++w)
+        mbar_init(&conv[w * kMaxStages + i], kConvWarps / g.nis);   // the converters of its K-blocks
     }
     for (uint32_t i = 0; i < g.ng; ++i) {
       mbar_init(&dfull[i], 1);
       mbar_init(&dempty[i], kConvWarps);
     }
-    mbar_init(accum, kIssuers);
+    mbar_init(accum, g.nis);
     mbar_init(red, 4);   // one arrival per epilogue warp (in the cluster) whose rows this CTA owns
     mbar_fence_init();
   }
@@ -323,10 +327,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         gph ^= 1u;
       }
     }
-  } else if (warp >= 1 && warp <= kIssuers && lane == 0) {
-    // ---- MMA issuers: issuer w takes K-blocks [w kKbPerIssuer, (w + 1) kKbPerIssuer)
-    // of every stage into its own accumulator (columns [w bn, (w + 1) bn))
-    const uint32_t w = warp - 1, j0 = w * kKbPerIssuer;
+  } else if (warp >= 1 && warp <= g.nis && lane == 0) {
+    // ---- MMA issuers: issuer w takes K-blocks [w kpi, (w + 1) kpi) of every
+    // stage (kpi = kSub / nis) into its own accumulator (columns [w bn, (w + 1) bn))
+    const uint32_t kpi = kSub / g.nis;
+    const uint32_t w = warp - 1, j0 = w * kpi;
     const uint32_t dacc = taddr + w * g.bn;
     uint32_t st = 0, ph = 0;
     for (uint32_t s = 0; s < stot; ++s) {
@@ -340,14 +345,13 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint64_t b0 = sdesc_sw128(smem_u32(tiles + st * g.stage_bytes));
       const uint64_t bstep = static_cast<uint64_t>(g.xbytes >> 4);   // next tile, in descriptor address units
       if (s < g.bstages) {
-#pragma unroll
-        for (uint32_t i = 0; i < kKbPerIssuer * (BK / 8); ++i) {
+        for (uint32_t i = 0; i < kpi * (BK / 8); ++i) {
           const uint32_t j = j0 + (i >> 2), kk = i & 3u;
           umma_tf32_ts(dacc, acol + BK * j + 8 * kk, b0 + j * bstep + 2u * kk, g.idesc, (s | i) != 0);
         }
       } else {
         const uint32_t nk = nsub(s);
-        for (uint32_t j = j0; j < j0 + kKbPerIssuer && j < nk; ++j)
+        for (uint32_t j = j0; j < j0 + kpi && j < nk; ++j)
           for (uint32_t kk = 0; kk < BK / 8; ++kk)
             umma_tf32_ts(dacc, acol + BK * j + 8 * kk, b0 + j * bstep + 2u * kk, g.idesc, 1u);
       }
@@ -362,7 +366,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ---- converters: row r = TMEM lane r (a warp reaches only its own lane
     // quarter, warp mod 4); warp h of a quarter takes K-block h of each stage
     const uint32_t quarter = warp & 3u, h = (warp - kConv0) >> 2, r = quarter * 32 + lane;
-    uint64_t* myconv = conv + (h / kKbPerIssuer) * kMaxStages;
+    uint64_t* myconv = conv + (h / (kSub / g.nis)) * kMaxStages;
     const uint32_t lanes = taddr + ((quarter * 32u) << 16);
     uint32_t st = 0, ph = 0, ds = 0, gph = 0;   // stage slot and parity; group slot and parity
     for (uint32_t s = 0; s < stot; ++s) {
@@ -453,8 +457,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (uint32_t j = 0; j < 32; ++j) sum[j] = __uint_as_float(acc[j]);
       }
-#pragma unroll
-      for (uint32_t w = 1; w < kIssuers; ++w) {
+      for (uint32_t w = 1; w < g.nis; ++w) {
         uint32_t acc[32];
         tmem_ld32(taddr + ((quarter * 32u) << 16) + w * g.bn + c0, acc);
 #pragma unroll
@@ -554,7 +557,7 @@ struct ShrinkArgs {
   // the launch's terms in order, each tensor's followed by a padding term
   // (A null) up to a multiple of 32 rows; padding rows of v are zero
   LoraRef lora[OVL_MAX_TABLE + kMaxFusedTensors];
-  int8_t tok_term[kTokTile];
+  int8_t tok_term[kWideTile];
 };
 
 constexpr uint32_t kShrinkRows = 2;     // factor rows per block
@@ -678,9 +681,14 @@ uint32_t sm_count() {
 
 bool fused_gemm_supported(uint32_t m, uint32_t n) { return m > 0 && n >= 256 && n % 256 == 0; }
 
-size_t fused_gemm_scratch_bytes(uint32_t T, uint32_t n, uint32_t vcols) {
-  const uint32_t tc = std::min<uint32_t>(T, kTokTile);
+// Scratch of one token chunk of `tile` tokens (the widened activations, then s v).
+size_t chunk_scratch_bytes(uint32_t T, uint32_t n, uint32_t vcols, uint32_t tile) {
+  const uint32_t tc = std::min<uint32_t>(T, tile);
   return (static_cast<size_t>(tc) * n * 4 + 255) / 256 * 256 + static_cast<size_t>(tc) * vcols * 4;
+}
+
+size_t fused_gemm_scratch_bytes(uint32_t T, uint32_t n, uint32_t vcols) {
+  return chunk_scratch_bytes(T, n, vcols, kTokTile);
 }
 
 cudaError_t launch_fused_gemm(const FusedLaunch& L, cudaStream_t st) {
@@ -740,12 +748,21 @@ cudaError_t launch_fused_gemm(const FusedLaunch& L, cudaStream_t st) {
     splits = 4;
   else if (tiles * 2 <= sm_count() && L.n % (BK * kDGroup * 2) == 0)
     splits = 2;
+  // 128-token chunks (two issuers, N = 128: each dequantized weight feeds twice
+  // the multiply-adds) when there are that many tokens, no split-K (its
+  // receive buffer and the 64 KB stages do not fit together), no per-token
+  // selection, and the scratch holds a chunk; 64 otherwise.
+  const uint32_t tile =
+      (L.T >= kWideTile && splits == 1 && !L.tok_sel &&
+       chunk_scratch_bytes(L.T, L.n, vcols, kWideTile) <= L.scratch_bytes)
+          ? kWideTile
+          : kTokTile;
   const size_t esz = L.xdt == OVL_BF16 ? 2 : 4;
   float* xf = L.scratch;
   float* v = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(L.scratch) +
-                                      (static_cast<size_t>(std::min<uint32_t>(L.T, kTokTile)) * L.n * 4 + 255) / 256 * 256);
-  for (uint32_t t0 = 0; t0 < L.T; t0 += kTokTile) {
-    const uint32_t tc = std::min<uint32_t>(kTokTile, L.T - t0);
+                                      (static_cast<size_t>(std::min<uint32_t>(L.T, tile)) * L.n * 4 + 255) / 256 * 256);
+  for (uint32_t t0 = 0; t0 < L.T; t0 += tile) {
+    const uint32_t tc = std::min<uint32_t>(tile, L.T - t0);
     const void* xc = static_cast<const uint8_t*>(L.x) + static_cast<size_t>(t0) * L.n * esz;
     cudaError_t e;
     cudaLaunchAttribute at[1];
@@ -762,7 +779,7 @@ cudaError_t launch_fused_gemm(const FusedLaunch& L, cudaStream_t st) {
       s.rtot = vcols;
       s.rpad = vcols;
       s.tok_sel = L.tok_sel;
-      for (uint32_t t = 0; t < kTokTile; ++t) s.tok_term[t] = (L.tok_sel && t < tc) ? L.tok_host[t0 + t] : -1;
+      for (uint32_t t = 0; t < kWideTile; ++t) s.tok_term[t] = (L.tok_sel && t < tc) ? L.tok_host[t0 + t] : -1;
       cudaLaunchConfig_t cs{};
       cs.gridDim = dim3(vcols / kShrinkRows, (tc + kShrinkToks - 1) / kShrinkToks);
       const bool wide = cs.gridDim.x * cs.gridDim.y <= 2 * sm_count();
@@ -788,6 +805,7 @@ cudaError_t launch_fused_gemm(const FusedLaunch& L, cudaStream_t st) {
     g.T = tc;
     g.quant = L.quant;
     g.bn = (tc + 15) / 16 * 16;
+    g.nis = g.bn > kTokTile ? 2u : kIssuers;
     g.kblocks = L.n / BK;
     g.splits = splits;
     g.kbs = g.kblocks / g.splits;
@@ -796,7 +814,7 @@ cudaError_t launch_fused_gemm(const FusedLaunch& L, cudaStream_t st) {
     g.gbytes = BM * kDGroup * qrow + kDBytes;   // multiple of 1024: every group stays swizzle-aligned
     g.xbytes = g.bn * 128;                      // multiple of 2048
     g.stage_bytes = kSub * g.xbytes;
-    g.acol = kIssuers * g.bn;
+    g.acol = g.nis * g.bn;
     g.ns = std::min<uint32_t>(kMaxStages, (kTmemCols - g.acol) / kStageCols);
     g.recv_bytes = g.splits > 1 ? BM * (g.bn + 4) * 4 : 0u;
     const uint32_t left = kSmemCap - 1024 - 512 - g.ns * g.stage_bytes - g.recv_bytes;

@@ -353,3 +353,38 @@ def test_outlier_blocks_in_multi_tensor_launch(block_q8):
     assert st == 0 and rt.check_device() == 0
     for i, y in zip(group, ys):
         assert_within_bound(y.cpu().numpy(), deq_of(base, i), lora_terms([(ad, 2.0)], i), x64, f"outlier {i}")
+
+
+# ----------------------------------------------------------------- 128-token chunks (two MMA issuers, N = 128)
+# Layers large enough to need no split-K (gate+up of the 8B block: 224 row
+# tiles) take 128-token chunks when T >= 128: each dequantized weight feeds 128
+# multiply-adds.  T = 200 is one full chunk and a ragged one of 72 tokens.
+@pytest.mark.parametrize("quant", [S.Q8_0, S.Q4_0, S.Q4_K])
+@pytest.mark.parametrize("T", [128, 200])
+def test_wide_token_chunks_gate_up(quant, T):
+    require_gpu()
+    import quantized_base_lora_gb300 as q
+    base = S.block_base(quant, projs=("gate", "up"))
+    ad = S.block_adapter(base, adapter=0, rank=16)
+    rt = make_runtime(base, arena_bytes=256 << 20)
+    h = stage(rt, ad)
+    assert rt.activate([h], [2.0])[0] == 0
+    x = S.activations(T, 4096, seed=7000 + T)
+    xd, x64 = x_device(x, "bf16")
+    ys = [torch.full((T, t.d_out), float("nan"), device="cuda") for t in base.tensors]
+    st = q.ovl_linear_forward_multi(rt.ctx, [0, 1], xd.data_ptr(), q.OVL_BF16, T, [y.data_ptr() for y in ys],
+                                    int(torch.cuda.current_stream().cuda_stream))
+    torch.cuda.synchronize()
+    assert st == 0 and rt.check_device() == 0
+    rows = np.random.default_rng(T).choice(T, min(T, 24), replace=False)
+    for i, y in enumerate(ys):
+        got = y.cpu().numpy()
+        assert np.isfinite(got).all()
+        assert_within_bound(got[rows], deq_of(base, i), lora_terms([(ad, 2.0)], i), x64[rows], f"wide q{quant} {i} T={T}")
+    # deterministic
+    y0 = ys[0].clone()
+    st = q.ovl_linear_forward_multi(rt.ctx, [0, 1], xd.data_ptr(), q.OVL_BF16, T, [y.data_ptr() for y in ys],
+                                    int(torch.cuda.current_stream().cuda_stream))
+    torch.cuda.synchronize()
+    assert torch.equal(y0, ys[0])
+    rt.close()
