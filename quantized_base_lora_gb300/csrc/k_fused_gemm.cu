@@ -108,6 +108,7 @@ struct FusedArgs {
   uint32_t kbs;           // base K-blocks per CTA: kblocks / splits, a multiple of kDGroup
   uint32_t bstages;       // base stages per CTA: kbs / kSub
   uint32_t recv_bytes;    // split-K receive buffer: BM x bn fp32 (0 without splits)
+  uint32_t recv_alias;    // 1: the receive buffer lies in the activation tiles
   uint32_t qrow;          // raw code bytes per row and K-block (32 or 16)
   uint32_t gbytes;        // one code group: codes (128-byte swizzled boxes) then scales
   uint32_t xbytes;        // one activation tile: bn rows x 128 bytes
@@ -202,8 +203,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint8_t* sm = sm_raw + ((1024u - (smem_u32(sm_raw) & 1023u)) & 1023u);
   uint8_t* tiles = sm;                                   // ns x kSub activation tiles
   uint8_t* gring = sm + g.ns * g.stage_bytes;            // ng code groups (codes, then scales)
-  float* recv = reinterpret_cast<float*>(gring + g.ng * g.gbytes);   // split-K partials of the rows this CTA owns
-  uint64_t* full = reinterpret_cast<uint64_t*>(gring + g.ng * g.gbytes + g.recv_bytes);
+  // split-K partials of the rows this CTA owns: their own area, or (recv_alias)
+  // the activation tiles, which are free once every CTA of the cluster is past
+  // its last MMA
+  float* recv = reinterpret_cast<float*>(g.recv_alias ? tiles : gring + g.ng * g.gbytes);
+  uint64_t* full = reinterpret_cast<uint64_t*>(gring + g.ng * g.gbytes + (g.recv_alias ? 0u : g.recv_bytes));
   uint64_t* empty = full + kMaxStages;
   uint64_t* conv = empty + kMaxStages;     // [issuer][stage]
   uint64_t* dfull = conv + kIssuers * kMaxStages;
@@ -430,6 +434,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   }
   __syncwarp();
+  if (g.recv_alias) {
+    // every CTA of the cluster past its last MMA (the tiles hold no operand
+    // any more) before any partial lands in them; all waits above are bounded
+    if (!mbar_wait_bounded(accum, 0)) latch_status(g.status, kTimeoutFused);
+    tc_fence_after();
+    cluster_sync_all();
+  }
 
   // ---- epilogue (the first four converter warps, one per TMEM lane quarter:
   // 32 rows; column = token): the issuers' accumulators summed in a fixed order.
@@ -749,12 +760,11 @@ cudaError_t launch_fused_gemm(const FusedLaunch& L, cudaStream_t st) {
   else if (tiles * 2 <= sm_count() && L.n % (BK * kDGroup * 2) == 0)
     splits = 2;
   // 128-token chunks (two issuers, N = 128: each dequantized weight feeds twice
-  // the multiply-adds) when there are that many tokens, no split-K (its
-  // receive buffer and the 64 KB stages do not fit together), no per-token
-  // selection, and the scratch holds a chunk; 64 otherwise.
+  // the multiply-adds) when there are that many tokens, no per-token
+  // selection, and the scratch holds a chunk; 64 otherwise.  With split-K the
+  // receive buffer then shares the activation tiles.
   const uint32_t tile =
-      (L.T >= kWideTile && splits == 1 && !L.tok_sel &&
-       chunk_scratch_bytes(L.T, L.n, vcols, kWideTile) <= L.scratch_bytes)
+      (L.T >= kWideTile && !L.tok_sel && chunk_scratch_bytes(L.T, L.n, vcols, kWideTile) <= L.scratch_bytes)
           ? kWideTile
           : kTokTile;
   const size_t esz = L.xdt == OVL_BF16 ? 2 : 4;
@@ -817,7 +827,9 @@ cudaError_t launch_fused_gemm(const FusedLaunch& L, cudaStream_t st) {
     g.acol = g.nis * g.bn;
     g.ns = std::min<uint32_t>(kMaxStages, (kTmemCols - g.acol) / kStageCols);
     g.recv_bytes = g.splits > 1 ? BM * (g.bn + 4) * 4 : 0u;
-    const uint32_t left = kSmemCap - 1024 - 512 - g.ns * g.stage_bytes - g.recv_bytes;
+    g.recv_alias = g.splits > 1 && g.bn > kTokTile && g.recv_bytes <= g.ns * g.stage_bytes;
+    const uint32_t own_recv = g.recv_alias ? 0u : g.recv_bytes;
+    const uint32_t left = kSmemCap - 1024 - 512 - g.ns * g.stage_bytes - own_recv;
     g.ng = std::min<uint32_t>(kMaxGroups, left / g.gbytes);
     if (g.ng < 2) return cudaErrorInvalidConfiguration;
     g.tmem_cols = kTmemCols;
@@ -855,7 +867,7 @@ cudaError_t launch_fused_gemm(const FusedLaunch& L, cudaStream_t st) {
     // at least 120 KiB, so that two CTAs never share an SM (each holds all of
     // its SM's tensor memory)
     cfg.dynamicSmemBytes =
-        std::max<uint32_t>(g.ns * g.stage_bytes + g.ng * g.gbytes + g.recv_bytes + 512 + 1024, 120 * 1024);
+        std::max<uint32_t>(g.ns * g.stage_bytes + g.ng * g.gbytes + own_recv + 512 + 1024, 120 * 1024);
     cfg.stream = st;
     cudaLaunchAttribute ak[2];
     ak[0] = at[0];

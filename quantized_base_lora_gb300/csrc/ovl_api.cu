@@ -36,8 +36,13 @@ namespace {
 constexpr size_t kArenaAlign = 256;
 constexpr size_t kStatusOff = 0;
 constexpr size_t kPartialOff = 1024;
-constexpr size_t kPartialBytes = 8u << 20;
-constexpr size_t kReservedEnd = kPartialOff + kPartialBytes;
+// K1's partial-sum slots: at most 8 tokens x OVL_MAX_TOTAL_RANK x 152 shrink
+// CTAs x 8 bytes = 2.4 MiB; then the tensor-core scratch, which holds a
+// 128-token chunk of 14336-wide activations in fp32 (7.3 MB) and its s v.
+constexpr size_t kPartialBytes = 3u << 20;
+constexpr size_t kTcOff = kPartialOff + kPartialBytes;
+constexpr size_t kTcBytes = 8u << 20;
+constexpr size_t kReservedEnd = kTcOff + kTcBytes;
 constexpr size_t kMinArena = 16u << 20;
 constexpr uint32_t kMaxTableRank = 1024;   // sum of ranks of a TABLE composition on one tensor
 constexpr char kRuntimeTag[16] = {'o', 'v', 'l', '-', 'g', 'b', '3', '0', '0', ' ', 'v', '1', 0, 0, 0, 0};
@@ -398,9 +403,9 @@ ovl_status ovl_create(ovl_ctx** out, int device, void* arena_dev, size_t arena_b
   // lower half: the dual path's partial-sum slots; upper half: scratch of the
   // tensor-core path (widened activations, low-rank vectors)
   c->ws.partial = reinterpret_cast<float*>(c->arena + kPartialOff);
-  c->ws.partial_floats = kPartialBytes / 2 / sizeof(float);
-  c->ws.tc_scratch = reinterpret_cast<float*>(c->arena + kPartialOff + kPartialBytes / 2);
-  c->ws.tc_scratch_bytes = kPartialBytes / 2;
+  c->ws.partial_floats = kPartialBytes / sizeof(float);
+  c->ws.tc_scratch = reinterpret_cast<float*>(c->arena + kTcOff);
+  c->ws.tc_scratch_bytes = kTcBytes;
   c->ws.epoch_counter = &c->slot_epoch;
   *out = c;
   return OVL_OK;
