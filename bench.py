@@ -193,7 +193,29 @@ def cpu_baseline(base, ad, xs, budget_s=12.0):
             break
     return {"value": done_bytes / el / 1e9, "unit": "GB/s", "cores": os.cpu_count(), "kind": "oracle",
             "sample": f"{n} projection calls (q, k, v, o, gate, up, down in turn) of the same block, fp64 numpy oracle "
-                      f"(dequantize + GEMV + low-rank), {el:.1f} s; numpy BLAS may use all {os.cpu_count()} cores"}
+                      f"(dequantize + GEMV + low-rank), {el:.1f} s; numpy BLAS may use all {os.cpu_count()} cores, "
+                      f"the elementwise dequantization runs on one"}
+
+
+def cpu_baseline_one_thread(budget_s=10.0):
+    """The same oracle leg in a child process whose BLAS runs one thread (the
+    thread count of numpy's BLAS is fixed when it loads, so it is set in the
+    child's environment)."""
+    code = ("import json, sys; sys.path.insert(0, %r); import numpy as np; import synth as S; import bench; "
+            "base = S.block_base(S.Q8_0); ad = S.block_adapter(base, adapter=0, rank=bench.RANK); "
+            "xs = {d: S.bf16_bits_to_f32(S.to_bf16_bits(S.activations(1, d))).astype(np.float64) "
+            "for d in (4096, 14336)}; print(json.dumps(bench.cpu_baseline(base, ad, xs, budget_s=%r)))"
+            % (ROOT, budget_s))
+    env = dict(os.environ, OPENBLAS_NUM_THREADS="1", OMP_NUM_THREADS="1", MKL_NUM_THREADS="1",
+               BLIS_NUM_THREADS="1", VECLIB_MAXIMUM_THREADS="1")
+    try:
+        p = subprocess.run([sys.executable, "-c", code], env=env, capture_output=True, text=True, timeout=600)
+        out = json.loads(p.stdout.strip().splitlines()[-1])
+        out["cores"] = 1
+        out["sample"] = out["sample"].split("; numpy BLAS")[0] + "; every BLAS pool limited to one thread"
+        return out
+    except Exception as e:   # reported, not fatal: the all-core figure stands
+        return {"value": None, "cores": 1, "kind": "oracle", "error": str(e)[:200]}
 
 
 def run_reference(args, world, rank):
@@ -343,6 +365,7 @@ def run_ours(args, world, rank, local):
     if world == 1:
         xs64 = {d: S.bf16_bits_to_f32(v).astype(np.float64) for d, v in xs_host.items()}
         out["cpu_baseline"] = cpu_baseline(base, ad, xs64)
+        out["cpu_baseline"]["one_thread"] = cpu_baseline_one_thread()
     print(json.dumps(out))
     for rt in rts:
         rt.close()
