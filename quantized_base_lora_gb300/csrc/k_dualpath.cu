@@ -72,15 +72,16 @@ constexpr int kMaxThreads = 18 * 32;       // up to 16 consumer warps + producer
 // co-resident CTAs of consecutive launches with half the ring each (the next
 // launch's CTA still becomes resident on each SM as soon as this grid's CTA
 // there exits, and streams its ring while the rest of the grid drains).
-// Variants that stream at most two rows per stage serve wide rows (d_in >= 8K
-// for q8_0) and keep two activation records per lane in registers.
+// Up to 16 column warps cover a row of up to 16K weights with one 32-block
+// per lane, so single-token launches keep one activation record per lane in
+// registers (a second register record made the two-row variants spill).
 template <int TT, int RG>
 struct K1Shape {
   static constexpr int threads = kMaxThreads;
   static constexpr int min_blocks = 1;
-  static constexpr int reg_records = (RG <= 2 && TT == 1) ? 2 : 1;
+  static constexpr int reg_records = 1;
 };
-constexpr uint32_t reg_records_of(int tt, int rg) { return (rg <= 2 && tt == 1) ? 2u : 1u; }
+constexpr uint32_t reg_records_of(int, int) { return 1u; }
 constexpr uint32_t kRecBudget = 128 * 1024;
 constexpr uint32_t kSmemBudget = 220 * 1024;
 
@@ -463,6 +464,15 @@ __device__ __forceinline__ float dot_q4(const uint8_t* wp, const uint4 (&r)[7]) 
   sl = dp4a_uu(l2, r[5].x, sl); sl = dp4a_uu(h2, r[5].y, sl);
   sl = dp4a_uu(l3, r[5].z, sl); sl = dp4a_uu(h3, r[5].w, sl);
   return limb_combine(sh, static_cast<int>(sm), static_cast<int>(sl));
+}
+
+// dot_q4 with zero accumulator starts: sum(code * X) for codes 0..15 (q4_K,
+// whose minimum term needs sum(X) separately).
+__device__ __forceinline__ float dot_q4_zero(const uint8_t* wp, const uint4 (&r)[7]) {
+  uint4 z = r[6];
+  z.y = 0u; z.z = 0u; z.w = 0u;
+  const uint4 rz[7] = {r[0], r[1], r[2], r[3], r[4], r[5], z};
+  return dot_q4(wp, rz);
 }
 
 // Sum over the 32 lanes of v[lane >> (5 - log2 N)] for all N values at once
@@ -1094,20 +1104,22 @@ __global__ void __launch_bounds__(K1Shape<TT, RG>::threads, K1Shape<TT, RG>::min
       if constexpr (QK4) {
         // Sub-block j = b mod 8 of a 256-weight super-block: weight
         // d*sc_j*code - dmin*m_j, so the block sum is
-        // xs*(d*sc_j*sum(code*X) - dmin*m_j*sum(X)).  The record's accumulator
-        // starts hold -8*sum(X) in limbs, so dot_q4 gives sum((code-8)*X).
-        const float sx8 = -limb_combine(static_cast<int>(r[6].y), static_cast<int>(r[6].z), static_cast<int>(r[6].w));
+        // xs*(d*sc_j*sum(code*X) - dmin*m_j*sum(X)).  sum(code*X) comes from
+        // zero accumulator starts; the record's starts hold -8*sum(X), so
+        // xs*sum(X) is -xs/8 times their value (exact: powers of two), once
+        // per block for all rows.
+        const float xs0 = -0.125f * xs * limb_combine(static_cast<int>(r[6].y), static_cast<int>(r[6].z), static_cast<int>(r[6].w));
         const uint32_t j6 = 6u * (b & 7u);
         const uint8_t* hb = reinterpret_cast<const uint8_t*>(sd) + (b >> 3) * 16u;
 #pragma unroll
         for (int rr = 0; rr < RG; ++rr) {
           const uint8_t* wp = sq + rr * c.rowbytes + b * kBlockBytes;
-          const float P = dot_q4(wp, r) + sx8;                       // sum(code*X)
+          const float P = dot_q4_zero(wp, r);                         // sum(code*X)
           const uint4 h = *reinterpret_cast<const uint4*>(hb + static_cast<size_t>(rr) * c.nb * 2);
           float dsc, dmn;
           q4k_scales(h, j6, &dsc, &dmn);
-          acc[t * RG + rr] = fmaf(dsc * xs, P, acc[t * RG + rr]);
-          acc[t * RG + rr] = fmaf(-dmn * xs, 0.125f * sx8, acc[t * RG + rr]);
+          acc[t * RG + rr] = fmaf(dsc, xs * P, acc[t * RG + rr]);
+          acc[t * RG + rr] = fmaf(-dmn, xs0, acc[t * RG + rr]);
         }
       } else {
 #pragma unroll
@@ -1386,8 +1398,13 @@ cudaError_t launch_dualpath(const DualArgs& a_in, cudaStream_t st) {
   while (tt < static_cast<int>(Tneed)) tt *= 2;
   while (tt > 1 && tt * c.nb * kRecBytes > kRecBudget) tt /= 2;
   int rg = 2;
-  if (tt == 1)
-    while (rg < 8 && 2 * rg * c.rowbytes <= OVL_K1_STAGE_BYTES) rg *= 2;
+  if (tt == 1) {
+    // 4-bit rows take twice the instructions per byte: their stages hold up
+    // to twice the bytes (4 rows of d_in = 14336), which halves the per-stage
+    // wait, reduction and release per weight.
+    const uint32_t stage_target = a0.quant == OVL_Q8_0 ? OVL_K1_STAGE_BYTES : 2 * OVL_K1_STAGE_BYTES;
+    while (rg < 8 && 2 * rg * c.rowbytes <= stage_target) rg *= 2;
+  }
   const uint32_t max_cw = kMaxThreads / 32 - 2;
   c.ng = std::max<uint32_t>(1, std::min<uint32_t>(OVL_K1_MAX_GROUPS, max_cw / c.nwc));
   KernelFn fn = pick(a0.quant, tt, rg);
