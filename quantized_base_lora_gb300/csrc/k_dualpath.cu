@@ -879,9 +879,13 @@ __global__ void __launch_bounds__(K1Shape<TT, RG>::threads, K1Shape<TT, RG>::min
           bulk_prefetch_l2(sp.lo, sp.bytes);
         }
       uint32_t issued = 0;
+      uint32_t slot = 0, lap = 0;   // slot = s mod ns, lap = s / ns, kept as counters
       for (uint32_t s = 0; s < nst; ++s) {
-        const uint32_t slot = s % c.ns;
-        if (s >= c.ns && !mbar_wait_bounded(&empty[slot], ((s / c.ns) - 1) & 1)) {
+        if (s != 0 && ++slot == c.ns) {
+          slot = 0;
+          ++lap;
+        }
+        if (lap != 0 && !mbar_wait_bounded(&empty[slot], (lap - 1) & 1)) {
           latch(a.ws.status, kDevTimeoutEmpty);
           *abort_flag = 1u;
           break;
@@ -1083,10 +1087,15 @@ __global__ void __launch_bounds__(K1Shape<TT, RG>::threads, K1Shape<TT, RG>::min
 
   // 3. stream the base rows
   bool ok = true;
+  // slot = s mod ns and the barrier phase (s / ns) & 1, kept as counters
+  uint32_t slot = grp, phase = 0;
   for (uint32_t s = grp; s < nst; s += c.ng) {
-    const uint32_t slot = s % c.ns;
+    if (s != grp && (slot += c.ng) >= c.ns) {
+      slot -= c.ns;
+      phase ^= 1u;
+    }
     // warp-uniform decision: the shuffles below need every lane
-    if (!__all_sync(0xffffffffu, mbar_wait_bounded(&full[slot], (s / c.ns) & 1))) {
+    if (!__all_sync(0xffffffffu, mbar_wait_bounded(&full[slot], phase))) {
       latch(a.ws.status, kDevTimeoutFull);
       *abort_flag = 1u;
       ok = false;
