@@ -64,6 +64,7 @@ constexpr int kRecBytes = 112;  // per (token, block) activation record: 7 x 16 
 #define OVL_K1_MAX_GROUPS 4
 #endif
 constexpr int kMaxNS = OVL_K1_MAX_NS;
+constexpr uint32_t kPreDepStages = 2;     // ring stages copied to shared memory before the grid dependency
 constexpr int kMaxThreads = 18 * 32;       // up to 16 consumer warps + producer + helper
 
 // One CTA per SM: its ring (up to 150 KB of shared memory) is as deep as the
@@ -889,6 +890,25 @@ __global__ void __launch_bounds__(K1Shape<TT, RG>::threads, K1Shape<TT, RG>::min
           latch(a.ws.status, kDevTimeoutEmpty);
           *abort_flag = 1u;
           break;
+        }
+        if (s == kPreDepStages) {
+          // Only the first stages go to shared memory before the grid
+          // dependency resolves; the rest of the ring's worth of quantized
+          // rows is requested into L2.  Their copies to shared memory, issued
+          // after the dependency, hit L2, and the activation reads that the
+          // records need right after the dependency do not queue behind a
+          // full ring of weights arriving at this SM.  (Prefetching the
+          // scale rows as well measured slower.)
+          const uint32_t ra = row0 + s * RG;
+          const uint32_t ahead = c.ns > kPreDepStages ? c.ns - kPreDepStages : 0u;
+          const size_t q0 = static_cast<size_t>(ra) * c.rowbytes;
+          const uint32_t rows_ahead = min(row1 - ra, ahead * RG);
+          const size_t len = static_cast<size_t>(rows_ahead) * c.rowbytes;
+          for (size_t off = 0; off < len; off += 16384) {
+            const uint32_t b = static_cast<uint32_t>(len - off < 16384 ? len - off : 16384);
+            bulk_prefetch_l2(sg.qs + q0 + off, b);
+          }
+          griddep_wait();
         }
         if (*abort_flag) break;
         const uint32_t r0 = row0 + s * RG;
