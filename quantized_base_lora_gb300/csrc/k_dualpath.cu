@@ -109,6 +109,7 @@ struct DualCfg {
   uint32_t div32;                // 1: rtot * n * gs < 2^32, chunk arithmetic fits 32 bits
   uint32_t smem;
   uint32_t off_mk;               // marked-block map: 1 + TT * map_words(nb) words
+  uint32_t xfull;                // 1: the helper stages all of x (single token) for a chunk read with 16-byte loads
 };
 
 // Words per token of the marked-block map.
@@ -1001,11 +1002,18 @@ __global__ void __launch_bounds__(K1Shape<TT, RG>::threads, K1Shape<TT, RG>::min
       for (uint32_t e = lane; e < n2; e += 32) cp_async16(sXw + (n1 + e) * 16, gx + e * 16);
       cp_async_commit();
       xw = sXw;
+    } else if (c.xfull && cta < c.gs) {
+      uint8_t* sXw = sm + c.off_xw;
+      const uint8_t* gx = static_cast<const uint8_t*>(a.x);
+      const uint32_t nvec = a.n * (a.xdt == OVL_BF16 ? 2u : 4u) / 16u;
+      for (uint32_t e = lane; e < nvec; e += 32) cp_async16(sXw + e * 16, gx + e * 16);
+      cp_async_commit();
     }
     cp_async_wait_all();
     __syncwarp();
     if (c.stage_x) named_bar(2, nthr + 32);         // the consumers have staged x
-    const void* xsrc = c.stage_x ? static_cast<const void*>(sm + c.off_x) : a.x;
+    const void* xsrc = c.stage_x ? static_cast<const void*>(sm + c.off_x)
+                                 : (c.xfull ? static_cast<const void*>(sm + c.off_xw) : a.x);
     if (vec) {
       unsigned long long* slots = reinterpret_cast<unsigned long long*>(a.ws.partial);
       const uint32_t rho_b = static_cast<uint32_t>((hi - 1) / a.n);
@@ -1370,6 +1378,7 @@ bool plan(DualCfg& c, const DualArgs& a, int tt, int rg, uint32_t rows_max, uint
   }
   c.off_xw = off;
   if (c.xwin) off = round_up(off + c.xwin * (a.xdt == OVL_BF16 ? 2 : 4), 128);
+  else if (c.xfull) off = round_up(off + a.n * (a.xdt == OVL_BF16 ? 2 : 4), 128);
   c.stage_q = rg * c.rowbytes;
   c.stage_bytes = round_up(c.stage_q + round_up(rg * c.nb * 2, 16) + 32, 128);
   // B rows: into the A chunk + x window area after the shrink when they fit
@@ -1492,6 +1501,14 @@ cudaError_t launch_dualpath(const DualArgs& a_in, cudaStream_t st) {
     c.shrink_vec = cap * esz_x <= 8192 && c.stage_a && a0.a16 && chunk + g < a0.n && (chunk + 24) * 4 <= 32768;
     c.xwin = c.shrink_vec ? static_cast<uint32_t>(cap) : 0;
   }
+  // Chunks over several factor rows (stacked or high-rank terms): the helper
+  // stages all of x once (16-byte copies, all in flight together), so its
+  // pass over the chunk reads x from shared memory instead of waiting on one
+  // global load after another.
+  c.xfull = 0;
+  if (a0.nl && tt == 1 && !c.shrink_vec && !c.stage_x && c.xvec && c.stage_a &&
+      static_cast<uint64_t>(a0.n) * esz_x <= 32768)
+    c.xfull = 1;
   // Bytes of the B stage of the largest CTA slice (16-byte spans per term).
   uint32_t b_need = 0;
   for (uint32_t i = 0; a0.nl && i < a0.nseg; ++i) {
