@@ -306,7 +306,16 @@ ovl_status ovl_rollback(ovl_ctx* ctx, uint8_t composition_id_out[32]);
  *   ([DTD] §1 Per-Layer JIT CoW Materialization; §5 Fresh-Base Oracle Definition).
  * STACK compositions only (OVL_E_STATE for TABLE).  T = 0 is a no-op.  Errors:
  * OVL_E_ARG (tensor index, dtype, path, T > OVL_MAX_T, null pointers, scratch too
- * small), OVL_E_STATE (no base), OVL_E_CUDA (launch failure). */
+ * small), OVL_E_STATE (no base), OVL_E_CUDA (launch failure).
+ * Co-residency: below 4 tokens the dual path is one launch of at most one CTA
+ * per SM, and every CTA waits for the low-rank partial sums of all the others.
+ * It therefore assumes that all CTAs of the launch are resident at the same
+ * time, which holds unless other work keeps SMs (or their shared memory) for
+ * the launch's duration: a kernel on another stream that occupies SMs for
+ * longer than ~2 s, or an execution context limited to fewer SMs than the
+ * device has.  The wait is bounded: when it runs out, that launch's outputs
+ * are NaN and ovl_check_device returns OVL_E_DEVICE_TIMEOUT; this call has
+ * already returned OVL_OK, since the failure exists only on the device. */
 ovl_status ovl_linear_forward(ovl_ctx* ctx, uint32_t tensor, const void* x, uint32_t x_dtype,
                               uint32_t T, float* y, uint32_t path, float* scratch,
                               size_t scratch_bytes, void* stream);
