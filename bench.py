@@ -362,13 +362,48 @@ def run_ours(args, world, rank, local):
         "gpu_launches": len(GROUPS) * args.steps * REPEATS,
         "clocks": clocks,
     }
+    for rt in rts:
+        rt.close()
     if world == 1:
         xs64 = {d: S.bf16_bits_to_f32(v).astype(np.float64) for d, v in xs_host.items()}
         out["cpu_baseline"] = cpu_baseline(base, ad, xs64)
         out["cpu_baseline"]["one_thread"] = cpu_baseline_one_thread()
+        out["secondary"] = secondary_workloads(args)
     print(json.dumps(out))
-    for rt in rts:
-        rt.close()
+
+
+SECONDARY = ("q4k-decode", "q4-stacked", "prefill-dual", "segmented")
+
+
+def secondary_workloads(args):
+    """The other workloads' key figures in the same run (50 steps each after 5
+    warm-up steps, median of REPEATS regions; each its own timed regions, none
+    inside the headline's): the line each `--workload` prints, reduced to its
+    value, step time and roofline fraction per token count."""
+    res = {}
+    sargs = argparse.Namespace(**{**vars(args), "steps": 50, "warmup": 5})
+    global emit
+    keep = emit
+    for name in SECONDARY:
+        got = []
+        emit = got.append
+        try:
+            WORKLOADS[name](sargs)
+        except Exception as e:   # reported, not fatal: the headline stands
+            got = [{"error": f"{type(e).__name__}: {e}"[:200]}]
+        finally:
+            emit = keep
+        line = got[-1] if got else {}
+        entry = {k: line.get(k) for k in ("metric", "value", "unit", "error") if line.get(k) is not None}
+        if "per_T" in line:
+            entry["per_T"] = {str(T): {"us_per_step": round(v["ms_per_step"] * 1e3, 2),
+                                       "frac": round(v["roofline"]["frac"], 4),
+                                       "bound": v["roofline"]["bound"]} for T, v in line["per_T"].items()}
+        elif "roofline" in line:
+            entry["frac"] = round(line["roofline"]["frac"], 4)
+            entry["bound"] = line["roofline"]["bound"]
+        res[name] = entry
+    return res
 
 
 GROUPS = [[0, 1, 2], [3], [4, 5], [6]]          # qkv | o | gate+up | down
