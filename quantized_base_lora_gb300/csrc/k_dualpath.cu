@@ -800,7 +800,7 @@ __device__ __noinline__ float marked_sum(const uint32_t* mk, const DualArgs& a, 
   return sum;
 }
 
-template <int QUANT, int TT, int RG>
+template <int QUANT, int TT, int RG, bool VX = false>
 __global__ void __launch_bounds__(K1Shape<TT, RG>::threads, K1Shape<TT, RG>::min_blocks)
     k_dualpath(const DualArgs a, const DualCfg c) {
   constexpr int NREG = K1Shape<TT, RG>::reg_records;
@@ -956,6 +956,17 @@ __global__ void __launch_bounds__(K1Shape<TT, RG>::threads, K1Shape<TT, RG>::min
     // gather every partial of every factor row (bounded polling on the epochs),
     // sum them in a fixed order into v and release the epilogue.
     if (!a.nl) return;
+    if constexpr (VX) {
+      // The low-rank vector v = A x of this launch comes from the shrink
+      // launch just before it (k_shrink_v, in the workspace's tensor-core
+      // scratch): read it once the grid dependency has resolved.
+      griddep_wait();
+      const float* vsrc = a.ws.tc_scratch;
+      for (uint32_t i = lane; i < a.T * a.rtot; i += 32) vsm[i] = vsrc[i];
+      __syncwarp();
+      if (lane == 0) mbar_arrive(vbar);
+      return;
+    }
     uint64_t lo = 0, hi = 0;
     if (cta < c.gs) shrink_bounds(a, c, cta, &lo, &hi);
     const bool vec = c.shrink_vec && cta < c.gs;
@@ -1325,9 +1336,60 @@ __global__ void __launch_bounds__(K1Shape<TT, RG>::threads, K1Shape<TT, RG>::min
   }
 }
 
+// The low-rank vector of a single-token launch with large factors (stacked or
+// high-rank terms): v[rho] = A_rho . x for every factor row rho of the launch,
+// one CTA per row: each thread takes 8 elements of every 2048 (16-byte loads
+// of A and x, several rounds in flight), then a fixed-order warp sum and a
+// fixed-order sum of the warps.  Written to `v` for the dual-path launch that
+// follows; spreading the rows over their own CTAs replaces the per-CTA chunks
+// and the grid-wide gather of the dual-path kernel, slow when chunks are long.
+constexpr uint32_t kShrinkVWarps = 8;
+__global__ void __launch_bounds__(kShrinkVWarps * 32) k_shrink_v(const DualArgs a, float* v) {
+  __shared__ float part[kShrinkVWarps];
+  griddep_launch_dependents();
+  griddep_wait();   // x may come from the preceding grid
+  const uint32_t warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rho = blockIdx.x;
+  const float* Arow = factor_ptr(a, static_cast<uint64_t>(rho) * a.n);
+  float acc0 = 0.f, acc1 = 0.f;
+#pragma unroll 4
+  for (uint32_t j = threadIdx.x * 8; j < a.n; j += kShrinkVWarps * 32 * 8) {
+    const float4 p = *reinterpret_cast<const float4*>(Arow + j);
+    const float4 q = *reinterpret_cast<const float4*>(Arow + j + 4);
+    float xv[8];
+    load_x8(a.x, a.xdt, j, xv);
+    acc0 = fmaf(p.x, xv[0], acc0); acc1 = fmaf(p.y, xv[1], acc1);
+    acc0 = fmaf(p.z, xv[2], acc0); acc1 = fmaf(p.w, xv[3], acc1);
+    acc0 = fmaf(q.x, xv[4], acc0); acc1 = fmaf(q.y, xv[5], acc1);
+    acc0 = fmaf(q.z, xv[6], acc0); acc1 = fmaf(q.w, xv[7], acc1);
+  }
+  const float s = warp_sum(acc0 + acc1);
+  if (lane == 0) part[warp] = s;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float t = part[0];
+#pragma unroll
+    for (uint32_t w = 1; w < kShrinkVWarps; ++w) t += part[w];
+    v[rho] = t;
+  }
+}
+
+// Single-token launches whose shrink chunks would be at least this many factor
+// elements per CTA take the separate shrink launch.
+constexpr uint64_t kShrinkVChunk = 2048;
+
 using KernelFn = void (*)(const DualArgs, const DualCfg);
 
-KernelFn pick(uint32_t quant, int tt, int rg) {
+KernelFn pick(uint32_t quant, int tt, int rg, bool vx) {
+  if (vx) {
+#define OVL_KV(Q, R_) \
+  if (quant == Q && tt == 1 && rg == R_) return k_dualpath<Q, 1, R_, true>;
+    OVL_KV(OVL_Q8_0, 2) OVL_KV(OVL_Q8_0, 4) OVL_KV(OVL_Q8_0, 8)
+    OVL_KV(OVL_Q4_0, 2) OVL_KV(OVL_Q4_0, 4) OVL_KV(OVL_Q4_0, 8)
+    OVL_KV(OVL_Q4_K, 2) OVL_KV(OVL_Q4_K, 4) OVL_KV(OVL_Q4_K, 8)
+#undef OVL_KV
+    return nullptr;
+  }
 #define OVL_K(Q, T_, R_) \
   if (quant == Q && tt == T_ && rg == R_) return k_dualpath<Q, T_, R_>;
   OVL_K(OVL_Q8_0, 1, 2) OVL_K(OVL_Q8_0, 1, 4) OVL_K(OVL_Q8_0, 1, 8)
@@ -1445,9 +1507,14 @@ cudaError_t launch_dualpath(const DualArgs& a_in, cudaStream_t st) {
   }
   const uint32_t max_cw = kMaxThreads / 32 - 2;
   c.ng = std::max<uint32_t>(1, std::min<uint32_t>(OVL_K1_MAX_GROUPS, max_cw / c.nwc));
-  KernelFn fn = pick(a0.quant, tt, rg);
-  if (!fn) return cudaErrorInvalidValue;
   const uint32_t G = std::min<uint32_t>(static_cast<uint32_t>(nsm), a0.m);
+  // large factors on a single token: the shrink runs as its own launch
+  const bool vx = tt == 1 && a0.nl && !a0.tok_sel && !(a0.epoch & kEpochWithhold) && a0.a16 &&
+                  (reinterpret_cast<uintptr_t>(a0.x) & 15) == 0 && a0.ws.tc_scratch &&
+                  a0.ws.tc_scratch_bytes >= static_cast<size_t>(a0.rtot) * 4 &&
+                  static_cast<uint64_t>(a0.rtot) * a0.n >= kShrinkVChunk * G;
+  KernelFn fn = pick(a0.quant, tt, rg, vx);
+  if (!fn) return cudaErrorInvalidValue;
   if (G < a0.nseg) return cudaErrorInvalidValue;
   // CTAs per tensor in proportion to its rows (at least one, at most one per row)
   {
@@ -1475,6 +1542,7 @@ cudaError_t launch_dualpath(const DualArgs& a_in, cudaStream_t st) {
     c.gs = static_cast<uint32_t>(std::min<uint64_t>({G_used, static_cast<uint64_t>(a0.rtot) * a0.n, slots}));
     if (c.gs == 0) return cudaErrorInvalidValue;
   }
+  if (vx) c.gs = 0;   // no shrink chunks, slots or gather in the dual-path launch
   c.div32 = static_cast<uint64_t>(a0.rtot) * a0.n * (static_cast<uint64_t>(c.gs) + 1) < (1ull << 32);
   if (a0.nl && static_cast<size_t>(tt) * a0.rtot * c.gs > a0.ws.partial_floats / 2) return cudaErrorInvalidValue;
   if (a0.nl && !a0.ws.epoch_counter) return cudaErrorInvalidValue;
@@ -1487,10 +1555,10 @@ cudaError_t launch_dualpath(const DualArgs& a_in, cudaStream_t st) {
   const bool reg_only = tt == 1 && c.bpl <= reg_records_of(tt, rg);
   c.stage_x = (reg_only || !x_small) ? 0 : (xa % 16 == 0 ? 16 : (xa % 4 == 0 ? 4 : 0));
   c.xvec = c.stage_x ? 1 : (xa % 16 == 0 ? 1 : 0);
-  c.stage_a = a0.nl && (static_cast<uint64_t>(a0.rtot) * a0.n / std::max<uint32_t>(c.gs, 1) + 2) * 4 <= 32768;
+  c.stage_a = a0.nl && !vx && (static_cast<uint64_t>(a0.rtot) * a0.n / std::max<uint32_t>(c.gs, 1) + 2) * 4 <= 32768;
   // Single-token launches with x left in global memory: the helper warp stages
   // the x window of its shrink chunk (16-byte copies) when it is small.
-  if (a0.nl && tt == 1 && !c.stage_x && c.xvec) {
+  if (a0.nl && !vx && tt == 1 && !c.stage_x && c.xvec) {
     const uint32_t g = 16 / esz_x;
     const uint64_t chunk = (static_cast<uint64_t>(a0.rtot) * a0.n + c.gs - 1) / c.gs;
     // pieces: at most chunk + 2g elements, and at most n + g when the chunk wraps
@@ -1565,6 +1633,19 @@ cudaError_t launch_dualpath(const DualArgs& a_in, cudaStream_t st) {
         ep = ++*a0.ws.epoch_counter;
       }
       a.epoch = ep | (a0.epoch & kEpochWithhold);
+    }
+    if (vx) {
+      cudaLaunchConfig_t cv{};
+      cv.gridDim = dim3(a.rtot);
+      cv.blockDim = dim3(kShrinkVWarps * 32);
+      cv.stream = st;
+      cudaLaunchAttribute av[1];
+      av[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+      av[0].val.programmaticStreamSerializationAllowed = 1;
+      cv.attrs = av;
+      cv.numAttrs = OVL_K1_PDL;
+      e = cudaLaunchKernelEx(&cv, k_shrink_v, a, a0.ws.tc_scratch);
+      if (e != cudaSuccess) return e;
     }
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = dim3(G_used);
