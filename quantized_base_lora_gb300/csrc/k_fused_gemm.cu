@@ -768,16 +768,26 @@ cudaError_t launch_fused_gemm(const FusedLaunch& L, cudaStream_t st) {
           ? kWideTile
           : kTokTile;
   const size_t esz = L.xdt == OVL_BF16 ? 2 : 4;
+  // Widening pass: as many whole token chunks as the scratch holds are
+  // widened (with their s v) by one launch, then each chunk runs its fused
+  // GEMM on its part of the widened copy (segmented batches: one chunk).
+  uint32_t wtok = tile;
+  if (!L.tok_sel)
+    while (wtok + tile <= (L.T + tile - 1) / tile * tile &&
+           chunk_scratch_bytes(wtok + tile, L.n, vcols, wtok + tile) <= L.scratch_bytes)
+      wtok += tile;
   float* xf = L.scratch;
   float* v = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(L.scratch) +
-                                      (static_cast<size_t>(std::min<uint32_t>(L.T, tile)) * L.n * 4 + 255) / 256 * 256);
-  for (uint32_t t0 = 0; t0 < L.T; t0 += tile) {
-    const uint32_t tc = std::min<uint32_t>(tile, L.T - t0);
-    const void* xc = static_cast<const uint8_t*>(L.x) + static_cast<size_t>(t0) * L.n * esz;
+                                      (static_cast<size_t>(std::min<uint32_t>(L.T, wtok)) * L.n * 4 + 255) / 256 * 256);
+  for (uint32_t w0 = 0; w0 < L.T; w0 += wtok) {
+    const uint32_t wc = std::min<uint32_t>(wtok, L.T - w0);
+    const void* xc = static_cast<const uint8_t*>(L.x) + static_cast<size_t>(w0) * L.n * esz;
     cudaError_t e;
     cudaLaunchAttribute at[1];
     at[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     at[0].val.programmaticStreamSerializationAllowed = 1;
+    const uint32_t tc = wc;   // tokens of the widening pass
+    const uint32_t t0 = w0;
     if (vcols) {
       // widened activations and s v of every tensor in one pass
       s.x = xc;
@@ -809,6 +819,9 @@ cudaError_t launch_fused_gemm(const FusedLaunch& L, cudaStream_t st) {
       e = cudaLaunchKernelEx(&cw, k_widen_kblk, xc, L.xdt, tc, L.n, xf);
     }
     if (e != cudaSuccess) return e;
+    for (uint32_t c0 = 0; c0 < wc; c0 += tile) {
+    const uint32_t tc = std::min<uint32_t>(tile, wc - c0);   // tokens of this fused GEMM
+    const uint32_t t0 = w0 + c0;
     FusedArgs g{};
     g.nt = L.nt;
     g.n = L.n;
@@ -843,20 +856,23 @@ cudaError_t launch_fused_gemm(const FusedLaunch& L, cudaStream_t st) {
       g.ts[i].y = L.t[i].y + static_cast<size_t>(t0) * L.t[i].m;
       for (uint32_t k = 0; k < L.t[i].nl; ++k) g.lora[ta[i].term0 + k] = L.t[i].lora[k];
     }
-    // K-block-major activations as {element e, token t, K-block j}:
-    // x[t][32 j + e] at ((j tc + t) 32 + e); one box = kSub tiles of bn tokens
+    // K-block-major activations of the pass as {element e, token t, K-block j}:
+    // x[t][32 j + e] at ((j wc + t) 32 + e); this chunk's tokens start at c0;
+    // one box = kSub tiles of bn tokens
     const uint32_t box[3] = {BK, g.bn, kSub};
     {
       const uint64_t dims[3] = {BK, tc, g.kblocks};
-      const uint64_t str[2] = {BK * 4, static_cast<uint64_t>(tc) * BK * 4};
-      if (!encode_map_3d(&maps.x, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, xf, dims, str, box, true))
+      const uint64_t str[2] = {BK * 4, static_cast<uint64_t>(wc) * BK * 4};
+      if (!encode_map_3d(&maps.x, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, xf + static_cast<size_t>(c0) * BK, dims, str, box,
+                         true))
         return cudaErrorInvalidValue;
     }
     if (vcols) {
       // s v as {rank within a chunk of 32, token, chunk}: v[t][32 c + e]
       const uint64_t dims[3] = {BK, tc, vcols / BK};
       const uint64_t str[2] = {static_cast<uint64_t>(vcols) * 4, BK * 4};
-      if (!encode_map_3d(&maps.v, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, v, dims, str, box, true))
+      if (!encode_map_3d(&maps.v, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, v + static_cast<size_t>(c0) * vcols, dims, str,
+                         box, true))
         return cudaErrorInvalidValue;
     } else {
       maps.v = maps.x;   // no low-rank K-blocks: never read
@@ -879,6 +895,7 @@ cudaError_t launch_fused_gemm(const FusedLaunch& L, cudaStream_t st) {
     cfg.numAttrs = g.splits > 1 ? 2 : 1;
     e = cudaLaunchKernelEx(&cfg, k_fused_gemm, maps, g);
     if (e != cudaSuccess) return e;
+    }
   }
   return cudaSuccess;
 }
