@@ -308,9 +308,11 @@ ovl_status ovl_rollback(ovl_ctx* ctx, uint8_t composition_id_out[32]);
  * OVL_E_ARG (tensor index, dtype, path, T > OVL_MAX_T, null pointers, scratch too
  * small), OVL_E_STATE (no base), OVL_E_CUDA (launch failure).
  * Co-residency: below 4 tokens the dual path is one launch of at most one CTA
- * per SM, and every CTA waits for the low-rank partial sums of all the others.
- * It therefore assumes that all CTAs of the launch are resident at the same
- * time, which holds unless other work keeps SMs (or their shared memory) for
+ * per SM, and every CTA waits for the low-rank partial sums of all the others
+ * (single tokens with long factor rows per CTA -- stacked or high-rank terms --
+ * instead run the low-rank shrink as a separate launch first, and then no CTA
+ * waits for another).  It therefore assumes that all CTAs of the launch are
+ * resident at the same time, which holds unless other work keeps SMs (or their shared memory) for
  * the launch's duration: a kernel on another stream that occupies SMs for
  * longer than ~2 s, or an execution context limited to fewer SMs than the
  * device has.  The wait is bounded: when it runs out, that launch's outputs
