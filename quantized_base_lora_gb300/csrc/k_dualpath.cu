@@ -1497,13 +1497,21 @@ cudaError_t launch_dualpath(const DualArgs& a_in, cudaStream_t st) {
   const uint32_t Tneed = a0.T < 8 ? a0.T : 8;
   while (tt < static_cast<int>(Tneed)) tt *= 2;
   while (tt > 1 && tt * c.nb * kRecBytes > kRecBudget) tt /= 2;
-  int rg = 2;
+  int rg = 2, rg_fallback = 2;
   if (tt == 1) {
-    // 4-bit rows take twice the instructions per byte: their stages hold up
-    // to twice the bytes (4 rows of d_in = 14336), which halves the per-stage
-    // wait, reduction and release per weight.
+    // One kernel instance per format for single-token launches: 4 rows a
+    // stage for q8_0, 8 for the 4-bit formats, whatever d_in (as long as two
+    // stages fit the ring).  A decode step then runs the same instance for
+    // every projection, and each launch starts on code the previous one left
+    // in the instruction caches: on the 8B-shape step (d_in 4096 and 14336)
+    // that took 52.6 us to 49.2 us, although the 14336-wide launch alone
+    // is slower in the larger stages.  Rows too wide for that take the
+    // largest stage of at most 16 KB (q8_0) or 32 KB (4-bit) that fits.
     const uint32_t stage_target = a0.quant == OVL_Q8_0 ? OVL_K1_STAGE_BYTES : 2 * OVL_K1_STAGE_BYTES;
     while (rg < 8 && 2 * rg * c.rowbytes <= stage_target) rg *= 2;
+    rg_fallback = rg;
+    const int rg_uniform = a0.quant == OVL_Q8_0 ? 4 : 8;
+    if (static_cast<uint64_t>(rg_uniform) * c.rowbytes <= 64 * 1024) rg = rg_uniform;
   }
   const uint32_t max_cw = kMaxThreads / 32 - 2;
   c.ng = std::max<uint32_t>(1, std::min<uint32_t>(OVL_K1_MAX_GROUPS, max_cw / c.nwc));
@@ -1585,7 +1593,13 @@ cudaError_t launch_dualpath(const DualArgs& a_in, cudaStream_t st) {
     for (uint32_t k = a0.seg[i].k0; k < a0.seg[i].k1; ++k) need += (rows * a0.lora[k].r * 4 + 15) / 16 * 16 + 16;
     b_need = static_cast<uint32_t>(std::min<uint64_t>(std::max<uint64_t>(b_need, need), 1u << 30));
   }
-  if (!plan(c, a0, tt, rg, rows_max, b_need)) return cudaErrorInvalidConfiguration;
+  if (!plan(c, a0, tt, rg, rows_max, b_need)) {
+    // the uniform stage does not fit beside this launch's other buffers
+    if (rg == rg_fallback) return cudaErrorInvalidConfiguration;
+    rg = rg_fallback;
+    fn = pick(a0.quant, tt, rg, vx);
+    if (!fn || !plan(c, a0, tt, rg, rows_max, b_need)) return cudaErrorInvalidConfiguration;
+  }
   if (c.ns % c.ng != 0 || c.ns > static_cast<uint32_t>(kMaxNS)) return cudaErrorInvalidConfiguration;
   const uint32_t threads = (c.nwc * c.ng + 2) * 32;   // consumers + producer + helper
   // one attribute / occupancy query per (kernel, shared-memory size)
