@@ -158,6 +158,8 @@ RAGGED = [  # (quant, d_out, d_in, T, ranks, xdtype)
     (S.Q8_0, 4096, 256, 1, (128, 128), "f32"),
     (S.Q8_0, 512, 4096, 1, (64, 64), "f32"),      # long shrink chunks: the separate shrink launch
     (S.Q4_K, 100, 2048, 1, (96, 16), "bf16"),    # rank 112 on 100 CTAs: the separate shrink launch
+    (S.Q8_0, 64, 20480, 1, (8,), "bf16"),        # rows too wide for 4-row stages; blocks past 16 warps in shared memory
+    (S.Q4_0, 96, 20480, 1, (4,), "f32"),
 ]
 
 
