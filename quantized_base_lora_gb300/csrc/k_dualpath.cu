@@ -110,6 +110,7 @@ struct DualCfg {
   uint32_t smem;
   uint32_t off_mk;               // marked-block map: 1 + TT * map_words(nb) words
   uint32_t xfull;                // 1: the helper stages all of x (single token) for a chunk read with 16-byte loads
+  uint32_t shrink_only;          // 1 (shrink-launch instances): this launch only computes v, one CTA per factor row
 };
 
 // Words per token of the marked-block map.
@@ -566,9 +567,6 @@ __device__ __forceinline__ XWindow x_window(uint64_t lo, uint64_t hi, uint32_t n
   if (je <= n) return XWindow{w0, min(n, (je + g - 1) / g * g), 0u};
   return XWindow{w0, n, (je - n + g - 1) / g * g};
 }
-__device__ __forceinline__ uint32_t x_window_index(const XWindow& w, uint32_t j) {
-  return j >= w.w0 ? j - w.w0 : (w.w1 - w.w0) + j;
-}
 
 // One low-rank term of this CTA's tensor, copied from the kernel parameters
 // into shared memory at the start so that the B stage and the epilogue do not
@@ -812,6 +810,40 @@ __global__ void __launch_bounds__(K1Shape<TT, RG>::threads, K1Shape<TT, RG>::min
   constexpr int LN = Log2<N>::v;
   constexpr uint32_t kBlockBytes = Q4 ? 16 : 32;
   extern __shared__ __align__(1024) uint8_t sm[];
+  if constexpr (VX) {
+    if (c.shrink_only) {
+      // v[rho] = A_rho . x for factor row rho = blockIdx.x: the shrink launch
+      // of a single-token launch with long factor rows, run by this same kernel
+      // so consecutive launches stay on one function.  Each thread takes 8
+      // elements of every blockDim.x * 8; fixed-order warp sums, then the
+      // warps' sums in warp order.
+      griddep_launch_dependents();
+      griddep_wait();   // x may come from the preceding grid
+      float* part = reinterpret_cast<float*>(sm);
+      const uint32_t rho = blockIdx.x, w = threadIdx.x >> 5, ln = threadIdx.x & 31;
+      const float* Arow = factor_ptr(a, static_cast<uint64_t>(rho) * a.n);
+      float acc0 = 0.f, acc1 = 0.f;
+      for (uint32_t j = threadIdx.x * 8; j < a.n; j += blockDim.x * 8) {
+        const float4 p = *reinterpret_cast<const float4*>(Arow + j);
+        const float4 q = *reinterpret_cast<const float4*>(Arow + j + 4);
+        float xv[8];
+        load_x8(a.x, a.xdt, j, xv);
+        acc0 = fmaf(p.x, xv[0], acc0); acc1 = fmaf(p.y, xv[1], acc1);
+        acc0 = fmaf(p.z, xv[2], acc0); acc1 = fmaf(p.w, xv[3], acc1);
+        acc0 = fmaf(q.x, xv[4], acc0); acc1 = fmaf(q.y, xv[5], acc1);
+        acc0 = fmaf(q.z, xv[6], acc0); acc1 = fmaf(q.w, xv[7], acc1);
+      }
+      const float sum = warp_sum(acc0 + acc1);
+      if (ln == 0) part[w] = sum;
+      __syncthreads();
+      if (threadIdx.x == 0) {
+        float t = part[0];
+        for (uint32_t i = 1; i < blockDim.x / 32; ++i) t += part[i];
+        a.ws.tc_scratch[rho] = t;
+      }
+      return;
+    }
+  }
   uint64_t* full = reinterpret_cast<uint64_t*>(sm);
   uint64_t* empty = full + kMaxNS;
   uint64_t* vbar = empty + kMaxNS;                  // low-rank vector ready
@@ -958,8 +990,9 @@ __global__ void __launch_bounds__(K1Shape<TT, RG>::threads, K1Shape<TT, RG>::min
     if (!a.nl) return;
     if constexpr (VX) {
       // The low-rank vector v = A x of this launch comes from the shrink
-      // launch just before it (k_shrink_v, in the workspace's tensor-core
-      // scratch): read it once the grid dependency has resolved.
+      // launch just before it (this kernel in its shrink-only mode, v in the
+      // workspace's tensor-core scratch): read it once the grid dependency
+      // has resolved.
       griddep_wait();
       const float* vsrc = a.ws.tc_scratch;
       for (uint32_t i = lane; i < a.T * a.rtot; i += 32) vsm[i] = vsrc[i];
@@ -1336,44 +1369,6 @@ __global__ void __launch_bounds__(K1Shape<TT, RG>::threads, K1Shape<TT, RG>::min
   }
 }
 
-// The low-rank vector of a single-token launch with large factors (stacked or
-// high-rank terms): v[rho] = A_rho . x for every factor row rho of the launch,
-// one CTA per row: each thread takes 8 elements of every 2048 (16-byte loads
-// of A and x, several rounds in flight), then a fixed-order warp sum and a
-// fixed-order sum of the warps.  Written to `v` for the dual-path launch that
-// follows; spreading the rows over their own CTAs replaces the per-CTA chunks
-// and the grid-wide gather of the dual-path kernel, slow when chunks are long.
-constexpr uint32_t kShrinkVWarps = 8;
-__global__ void __launch_bounds__(kShrinkVWarps * 32) k_shrink_v(const DualArgs a, float* v) {
-  __shared__ float part[kShrinkVWarps];
-  griddep_launch_dependents();
-  griddep_wait();   // x may come from the preceding grid
-  const uint32_t warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const uint32_t rho = blockIdx.x;
-  const float* Arow = factor_ptr(a, static_cast<uint64_t>(rho) * a.n);
-  float acc0 = 0.f, acc1 = 0.f;
-#pragma unroll 4
-  for (uint32_t j = threadIdx.x * 8; j < a.n; j += kShrinkVWarps * 32 * 8) {
-    const float4 p = *reinterpret_cast<const float4*>(Arow + j);
-    const float4 q = *reinterpret_cast<const float4*>(Arow + j + 4);
-    float xv[8];
-    load_x8(a.x, a.xdt, j, xv);
-    acc0 = fmaf(p.x, xv[0], acc0); acc1 = fmaf(p.y, xv[1], acc1);
-    acc0 = fmaf(p.z, xv[2], acc0); acc1 = fmaf(p.w, xv[3], acc1);
-    acc0 = fmaf(q.x, xv[4], acc0); acc1 = fmaf(q.y, xv[5], acc1);
-    acc0 = fmaf(q.z, xv[6], acc0); acc1 = fmaf(q.w, xv[7], acc1);
-  }
-  const float s = warp_sum(acc0 + acc1);
-  if (lane == 0) part[warp] = s;
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    float t = part[0];
-#pragma unroll
-    for (uint32_t w = 1; w < kShrinkVWarps; ++w) t += part[w];
-    v[rho] = t;
-  }
-}
-
 // Single-token launches whose shrink chunks would be at least this many factor
 // elements per CTA take the separate shrink launch.
 constexpr uint64_t kShrinkVChunk = 2048;
@@ -1649,16 +1644,21 @@ cudaError_t launch_dualpath(const DualArgs& a_in, cudaStream_t st) {
       a.epoch = ep | (a0.epoch & kEpochWithhold);
     }
     if (vx) {
+      // the shrink launch: the same kernel in its shrink-only mode, one CTA
+      // per factor row (consecutive launches stay on one function)
       cudaLaunchConfig_t cv{};
       cv.gridDim = dim3(a.rtot);
-      cv.blockDim = dim3(kShrinkVWarps * 32);
       cv.stream = st;
       cudaLaunchAttribute av[1];
       av[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
       av[0].val.programmaticStreamSerializationAllowed = 1;
       cv.attrs = av;
       cv.numAttrs = OVL_K1_PDL;
-      e = cudaLaunchKernelEx(&cv, k_shrink_v, a, a0.ws.tc_scratch);
+      DualCfg cvc = c;
+      cvc.shrink_only = 1;
+      cv.blockDim = dim3(threads);
+      cv.dynamicSmemBytes = 256;   // the warps' partial sums
+      e = cudaLaunchKernelEx(&cv, fn, a, cvc);
       if (e != cudaSuccess) return e;
     }
     cudaLaunchConfig_t cfg{};
