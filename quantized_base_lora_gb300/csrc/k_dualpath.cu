@@ -110,7 +110,7 @@ struct DualCfg {
   uint32_t smem;
   uint32_t off_mk;               // marked-block map: 1 + TT * map_words(nb) words
   uint32_t xfull;                // 1: the helper stages all of x (single token) for a chunk read with 16-byte loads
-  uint32_t shrink_only;          // 1 (shrink-launch instances): this launch only computes v, one CTA per factor row
+  uint32_t shrink_only;          // 1 (instances that read v): this launch only computes v, one CTA per factor row
 };
 
 // Words per token of the marked-block map.
@@ -1496,11 +1496,11 @@ cudaError_t launch_dualpath(const DualArgs& a_in, cudaStream_t st) {
   if (tt == 1) {
     // One kernel instance per format for single-token launches: 4 rows a
     // stage for q8_0, 8 for the 4-bit formats, whatever d_in (as long as two
-    // stages fit the ring).  A decode step then runs the same instance for
-    // every projection, and each launch starts on code the previous one left
-    // in the instruction caches: on the 8B-shape step (d_in 4096 and 14336)
-    // that took 52.6 us to 49.2 us, although the 14336-wide launch alone
-    // is slower in the larger stages.  Rows too wide for that take the
+    // stages fit the ring).  A decode step then runs the same kernel
+    // function for every projection; a launch that follows one of another
+    // function starts later (measured on the 8B-shape step, d_in 4096 and
+    // 14336: 52.6 us with two instances, 49.2 us with one, although the
+    // 14336-wide launch alone is slower in the larger stages).  Rows too wide for that take the
     // largest stage of at most 16 KB (q8_0) or 32 KB (4-bit) that fits.
     const uint32_t stage_target = a0.quant == OVL_Q8_0 ? OVL_K1_STAGE_BYTES : 2 * OVL_K1_STAGE_BYTES;
     while (rg < 8 && 2 * rg * c.rowbytes <= stage_target) rg *= 2;
