@@ -58,3 +58,31 @@ def test_sparse_overlay_bytes_formula():
     sp = S.build_sparse_adapter([0], [(idx, val)])
     assert idx.nbytes + val.nbytes == 6 * sp.nnz[0]
     assert sp.payload.nbytes >= 6 * sp.nnz[0] and sp.idx_off[0] % 16 == 0 and sp.val_off[0] % 16 == 0
+
+
+def test_secondary_workloads_reduce_each_line_and_survive_a_failure(monkeypatch):
+    """The default line's `secondary` block: each workload's last emitted line
+    reduced to value, per-token-count step time and roofline fraction; a
+    workload that raises is reported, not fatal; emit is restored."""
+    import argparse
+
+    def ok(args):
+        assert args.steps == 50 and args.warmup == 5
+        bench.emit({"metric": "m", "value": 2.0, "unit": "u",
+                    "per_T": {1: {"ms_per_step": 0.0425, "roofline": {"frac": 0.44444, "bound": "hbm"}}}})
+
+    def flat(args):
+        bench.emit({"metric": "s", "value": 88.0, "unit": "us", "roofline": {"frac": 0.1177, "bound": "tensor"}})
+
+    def boom(args):
+        raise RuntimeError("no device")
+
+    keep = bench.emit
+    monkeypatch.setattr(bench, "SECONDARY", ("a", "b", "c"))
+    monkeypatch.setattr(bench, "WORKLOADS", {"a": ok, "b": flat, "c": boom})
+    out = bench.secondary_workloads(argparse.Namespace(steps=200, warmup=10, gpus=1))
+    assert out["a"] == {"metric": "m", "value": 2.0, "unit": "u",
+                        "per_T": {"1": {"us_per_step": 42.5, "frac": 0.4444, "bound": "hbm"}}}
+    assert out["b"] == {"metric": "s", "value": 88.0, "unit": "us", "frac": 0.1177, "bound": "tensor"}
+    assert out["c"]["error"].startswith("RuntimeError")
+    assert bench.emit is keep
